@@ -1,0 +1,443 @@
+"""CPU oracle for the DeepSeek-V4-Flash compressed attention forward.
+
+TEST INFRASTRUCTURE ONLY. This module is the slow, plain, float64 statement of
+what the attention path computes. Only the tests, ``__graft_entry__.smoke()``
+and the CPU-baseline / reference leg of ``bench.py`` may import it. The CUDA
+library never calls it and shares no code with it.
+
+Sources (the three pages the method is taken from):
+  [PR]   Primus PR #930 "fix(deepseek-v4): correct V4-Flash attention math, wire
+         the MoE balance loss", Part 1 items 1-6 and 8.
+  [BLOG] "Enabling DeepSeek-V4-Flash Training on AMD Instinct MI355X GPUs with
+         Primus", sections "The DeepSeek-V4-Flash architecture", "Three attention
+         types, interleaved", "Kernel fusions", "Attention kernels for the three
+         layer types".
+
+Every floating-point step runs in float64.  Where the CUDA path stores a bf16
+tensor between steps (pooled entries, indexer keys, prepared indexer queries,
+the attention output), the oracle rounds to bf16 (nearest, ties to even) at the
+same point when ``store_bf16`` is set.
+
+Readings of points the pages leave open (each is listed in the design doc):
+  * pooling scores are per channel (a per-token scalar score is the special
+    case of a score that is constant across channels);
+  * a group member that does not exist (the previous group of entry 0) is left
+    out of the softmax;
+  * ``ape`` rows are chronological: with overlap the first ``ratio`` rows belong
+    to the previous group, the last ``ratio`` rows to the entry's own tokens;
+    projection half 0 carries the own tokens, half 1 the previous ones;
+  * entry s covers tokens [r*s, r*s + r) and is visible to query t iff
+    r*s + r - 1 <= t, i.e. s < (t + 1) // r; a trailing partial group is not an
+    entry;
+  * each pooled entry is RMS-normalised (weight g) before its rotation;
+  * RoPE acts on interleaved pairs of the last R dims with the usual
+    complex-multiply sign; de-rotation is rotation by the negated position;
+  * the sliding window of query t is tokens [max(0, t - W + 1), t]
+    (W = -1: all tokens <= t); window tokens and selected entries are separate
+    keys (no de-duplication);
+  * the indexer temperature (Hi * Di) ** -0.5 multiplies the per-head weights;
+  * top-k keeps the min(K, n_vis) best entries, equal scores going to the
+    lower index; short rows are padded with -1;
+  * the optional attention sink is one extra logit per head that enters the
+    softmax denominator only.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+F64 = np.float64
+
+
+# ---------------------------------------------------------------------------
+# Storage rounding
+# ---------------------------------------------------------------------------
+def round_to_bf16(x):
+    """Round to the nearest bfloat16 value (ties to even); result kept in float64.
+
+    bfloat16 keeps 8 significant bits.  With x = m * 2**e and 0.5 <= |m| < 1,
+    the representable neighbours are multiples of 2**(e - 8); numpy's ``rint``
+    rounds halfway cases to even.  Subnormal and overflowing values never occur
+    on this path and are not treated specially.
+    """
+    x = np.asarray(x, dtype=F64)
+    m, e = np.frexp(x)
+    return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+
+
+def maybe_bf16(x, store_bf16):
+    return round_to_bf16(x) if store_bf16 else np.asarray(x, dtype=F64)
+
+
+# ---------------------------------------------------------------------------
+# RoPE tables and rotation  ([PR] items 2 and 8; [BLOG] "Kernel fusions",
+# row "Interleaved partial RoPE")
+# ---------------------------------------------------------------------------
+def make_inv_freq(theta, rope_dim, yarn_factor=1.0, original_len=0,
+                  beta_fast=32.0, beta_slow=1.0):
+    """Inverse frequencies of the rotated pairs, returned as float32.
+
+    Base table: theta ** (-2j / rope_dim) for pair j.  [PR] item 8 pairs the
+    compressed base (40000 for Flash) with a YaRN factor (16) acting on this
+    table.  YaRN's "NTK-by-parts" rule (Peng et al. 2023, section 3.2) is used:
+    pair j has wavelength 2*pi / f_j; with ratio r_j = original_len / wavelength,
+    the ramp gamma(r) is 0 below beta_slow, 1 above beta_fast and linear in
+    between, and the new frequency is (1 - gamma) * f_j / s + gamma * f_j.
+    Interpolation applies only when yarn_factor > 1 and original_len > 0 (the
+    PR notes that the released model, with original_seq_len = 0, runs it off).
+    """
+    j = np.arange(rope_dim // 2, dtype=F64)
+    f = np.power(F64(theta), -2.0 * j / F64(rope_dim))
+    if yarn_factor > 1.0 and original_len > 0:
+        wavelength = 2.0 * math.pi / f
+        r = F64(original_len) / wavelength
+        gamma = np.clip((r - beta_slow) / (beta_fast - beta_slow), 0.0, 1.0)
+        f = (1.0 - gamma) * f / F64(yarn_factor) + gamma * f
+    return f.astype(np.float32)
+
+
+def yarn_attention_mscale(yarn_factor):
+    """YaRN's attention temperature 0.1 * ln(s) + 1 (Peng et al. 2023).
+
+    [PR] item 1: V4 must NOT multiply the softmax scale by this factor; the
+    oracle keeps it only so a test can show the scale it would have inflated.
+    """
+    return 0.1 * math.log(yarn_factor) + 1.0 if yarn_factor > 1.0 else 1.0
+
+
+def rope_rotate(x, pos, inv_freq):
+    """Rotate interleaved pairs of the last R = 2 * len(inv_freq) dims.
+
+    For pair j at channels (D-R+2j, D-R+2j+1) = (a, b) and angle
+    phi = pos * inv_freq[j] (float64 from the float32 table):
+        (a, b) -> (a cos phi - b sin phi, a sin phi + b cos phi).
+    ``pos`` broadcasts against ``x.shape[:-1]``.
+    """
+    x = np.array(x, dtype=F64, copy=True)
+    f = np.asarray(inv_freq, dtype=np.float32).astype(F64)
+    R = 2 * f.shape[0]
+    D = x.shape[-1]
+    phi = np.asarray(pos, dtype=F64)[..., None] * f
+    c, s = np.cos(phi), np.sin(phi)
+    a = x[..., D - R::2].copy()
+    b = x[..., D - R + 1::2].copy()
+    x[..., D - R::2] = a * c - b * s
+    x[..., D - R + 1::2] = a * s + b * c
+    return x
+
+
+def rope_derotate(x, pos, inv_freq):
+    """[PR] item 3: rotation at the negated position (applied to the output)."""
+    return rope_rotate(x, -np.asarray(pos, dtype=F64), inv_freq)
+
+
+# ---------------------------------------------------------------------------
+# Hadamard  ([PR] item 6e)
+# ---------------------------------------------------------------------------
+def hadamard_matrix(n):
+    """Normalised Sylvester Hadamard matrix H_n / sqrt(n) (n a power of two)."""
+    if n < 1 or (n & (n - 1)) != 0:
+        raise ValueError("Hadamard size must be a power of two")
+    h = np.ones((1, 1), dtype=F64)
+    while h.shape[0] < n:
+        h = np.block([[h, h], [h, -h]])
+    return h / math.sqrt(n)
+
+
+# ---------------------------------------------------------------------------
+# Counting rules  ([BLOG] "Three attention types, interleaved")
+# ---------------------------------------------------------------------------
+def num_entries(seqlen, ratio):
+    """Compressed entries of a sequence: one per complete group of ``ratio`` tokens."""
+    return seqlen // ratio if ratio > 0 else 0
+
+
+def n_visible(t, ratio):
+    """Entries visible to query t: those whose last own token r*s + r - 1 <= t."""
+    return (t + 1) // ratio if ratio > 0 else 0
+
+
+def window_range(t, window):
+    """Window tokens of query t as a half-open range [lo, t + 1)."""
+    if window == 0:
+        return t + 1, t + 1
+    if window < 0:
+        return 0, t + 1
+    return max(0, t - window + 1), t + 1
+
+
+def keys_read(t, ratio, window, topk):
+    """Number of keys query t attends to (entries plus window tokens)."""
+    nv = n_visible(t, ratio)
+    ne = min(topk, nv) if topk > 0 else nv
+    lo, hi = window_range(t, window)
+    return ne + (hi - lo)
+
+
+# ---------------------------------------------------------------------------
+# Compressor  ([BLOG] "Three attention types, interleaved": shared learned
+# pooling, CSA groups overlap; "Kernel fusions", row "Compressor pooling";
+# [PR] items 2 and 6e)
+# ---------------------------------------------------------------------------
+def group_members(s, ratio, overlap):
+    """(token, projection half, ape row) triples pooled into entry s."""
+    members = []
+    if overlap and s >= 1:
+        for i in range(ratio):
+            members.append((ratio * (s - 1) + i, 1, i))
+    for i in range(ratio):
+        members.append((ratio * s + i, 0, overlap * ratio + i))
+    return members
+
+
+def pooling_weights(cscore, ape, s, ratio, overlap):
+    """Softmax over the group members of score + ape, per channel.
+
+    cscore [B, S, 1+overlap, d]; returns (members, weights [B, G', d]).
+    """
+    members = group_members(s, ratio, overlap)
+    lam = np.stack([cscore[:, j, half, :].astype(F64) + ape[row, :].astype(F64)
+                    for (j, half, row) in members], axis=1)
+    lam = lam - lam.max(axis=1, keepdims=True)
+    e = np.exp(lam)
+    return members, e / e.sum(axis=1, keepdims=True)
+
+
+def compress(ckv, cscore, ape, norm_weight, inv_freq, ratio, overlap, eps,
+             hadamard=False, store_bf16=False):
+    """Pool the latent into compressed entries.
+
+    ckv, cscore: [B, S, 1+overlap, d]; ape: [(1+overlap)*ratio, d] float32;
+    norm_weight: [d] or None (ones).  Returns entries [B, N, d], N = S // ratio.
+    Steps per entry s: pooled = sum_m softmax_m(score + ape) * ckv_m;
+    e = pooled / sqrt(mean(pooled^2) + eps) * g; e = rot(e, ratio * s);
+    indexer keys additionally take e = H e with the normalised Hadamard H.
+    """
+    ckv = np.asarray(ckv, dtype=F64)
+    cscore = np.asarray(cscore, dtype=F64)
+    B, S, P, d = ckv.shape
+    if P != 1 + overlap:
+        raise ValueError("ckv must carry 1 + overlap projection halves")
+    N = num_entries(S, ratio)
+    g = np.ones(d, dtype=F64) if norm_weight is None else np.asarray(norm_weight, dtype=F64)
+    out = np.zeros((B, N, d), dtype=F64)
+    for s in range(N):
+        members, wts = pooling_weights(cscore, ape, s, ratio, overlap)
+        vals = np.stack([ckv[:, j, half, :] for (j, half, _) in members], axis=1)
+        out[:, s, :] = (wts * vals).sum(axis=1)
+    rms = np.sqrt((out * out).mean(axis=-1, keepdims=True) + F64(eps))
+    out = out / rms * g
+    out = rope_rotate(out, (ratio * np.arange(N))[None, :], inv_freq)
+    if hadamard:
+        out = out @ hadamard_matrix(d).T
+    return maybe_bf16(out, store_bf16)
+
+
+# ---------------------------------------------------------------------------
+# Lightning indexer  ([PR] items 4, 6a, 6e; [BLOG] "Kernel fusions", row
+# "Indexer scoring tail"; "Three attention types": keep the best 512)
+# ---------------------------------------------------------------------------
+def indexer_scale(idx_heads, idx_dim):
+    """[PR] item 6a: per-head weights scaled by Hi^-1/2 * Di^-1/2."""
+    return 1.0 / math.sqrt(idx_heads) / math.sqrt(idx_dim)
+
+
+def indexer_query_prep(iq, inv_freq, store_bf16=False):
+    """Queries rotated at their own positions t, then the normalised Hadamard.
+
+    iq: [B, S, Hi, Di] -> same shape.
+    """
+    iq = np.asarray(iq, dtype=F64)
+    S = iq.shape[1]
+    x = rope_rotate(iq, np.arange(S)[None, :, None], inv_freq)
+    x = x @ hadamard_matrix(iq.shape[-1]).T
+    return maybe_bf16(x, store_bf16)
+
+
+def indexer_scores(iq_prep, ikey, w, ratio, rows=None):
+    """I[b, t, s] = sum_h w[b,t,h] * (Hi*Di)^-1/2 * max(0, q~[b,t,h] . k[b,s]).
+
+    Defined for s < n_visible(t); other entries are -inf.  ``rows`` selects the
+    query positions (default: all).  Returns [B, len(rows), N].
+    """
+    iq_prep = np.asarray(iq_prep, dtype=F64)
+    ikey = np.asarray(ikey, dtype=F64)
+    w = np.asarray(w, dtype=F64)
+    B, S, Hi, Di = iq_prep.shape
+    N = ikey.shape[1]
+    rows = np.arange(S) if rows is None else np.asarray(rows)
+    c = indexer_scale(Hi, Di)
+    out = np.full((B, len(rows), N), -np.inf, dtype=F64)
+    for b in range(B):
+        for i, t in enumerate(rows):
+            nv = min(n_visible(int(t), ratio), N)
+            if nv == 0:
+                continue
+            dots = iq_prep[b, t] @ ikey[b, :nv].T          # [Hi, nv]
+            out[b, i, :nv] = (w[b, t] * c) @ np.maximum(dots, 0.0)
+    return out
+
+
+def topk_select(score_row, nvis, k):
+    """Best min(k, nvis) entries of one row; ties go to the lower index.
+
+    Returns (indices [k] int32 padded with -1, scores [k] padded with -inf),
+    ordered by decreasing score.
+    """
+    nvis = int(nvis)
+    idx = np.full(k, -1, dtype=np.int32)
+    val = np.full(k, -np.inf, dtype=F64)
+    if nvis <= 0 or k <= 0:
+        return idx, val
+    s = np.arange(nvis)
+    order = np.lexsort((s, -np.asarray(score_row[:nvis], dtype=F64)))
+    take = order[:min(k, nvis)]
+    idx[:len(take)] = take
+    val[:len(take)] = score_row[take]
+    return idx, val
+
+
+def indexer_topk(iq, ikey, w, inv_freq, ratio, k, store_bf16=False, rows=None,
+                 prepared=False):
+    """Indexer from un-rotated queries (or prepared ones) to top-k index sets.
+
+    Returns dict(idx [B,T,k] int32, iscore [B,T,k], scores [B,T,N]).
+    """
+    qp = np.asarray(iq, dtype=F64) if prepared else indexer_query_prep(iq, inv_freq, store_bf16)
+    sc = indexer_scores(qp, ikey, w, ratio, rows)
+    B, T, N = sc.shape
+    S = qp.shape[1]
+    rows_ = np.arange(S) if rows is None else np.asarray(rows)
+    idx = np.full((B, T, k), -1, dtype=np.int32)
+    isc = np.full((B, T, k), -np.inf, dtype=F64)
+    for b in range(B):
+        for i, t in enumerate(rows_):
+            idx[b, i], isc[b, i] = topk_select(sc[b, i], min(n_visible(int(t), ratio), N), k)
+    return {"idx": idx, "iscore": isc, "scores": sc}
+
+
+# ---------------------------------------------------------------------------
+# Sparse / dense multi-query attention  ([BLOG] "The DeepSeek-V4-Flash
+# architecture": 64 heads share one 512-d latent that is both key and value;
+# "Three attention types": selected entries plus a 128-token window; "Kernel
+# fusions", row "SWA / CSA / HCA attention": window and sink in one softmax;
+# [PR] item 1: scale head_dim ** -0.5; item 3: de-rotate the output at -t)
+# ---------------------------------------------------------------------------
+def attention_keys(b, t, kv, ent, idx, inv_freq, ratio, window):
+    """Keys (= values) of query t: the chosen entries, then the window tokens."""
+    parts = []
+    if ratio > 0 and ent is not None:
+        nv = min(n_visible(t, ratio), ent.shape[1])
+        if idx is not None:
+            sel = np.asarray(idx[b, t])
+            sel = sel[sel >= 0]
+            if np.any(sel >= nv):
+                raise ValueError("selected entry is not causally visible")
+        else:
+            sel = np.arange(nv)
+        parts.append(np.asarray(ent[b, sel], dtype=F64))
+    lo, hi = window_range(t, window)
+    if hi > lo:
+        u = np.arange(lo, hi)
+        parts.append(rope_rotate(np.asarray(kv[b, lo:hi], dtype=F64), u, inv_freq))
+    if not parts:
+        return np.zeros((0, kv.shape[-1]), dtype=F64)
+    return np.concatenate(parts, axis=0)
+
+
+def sparse_mqa(q, kv, ent, idx, sink, inv_freq, ratio, window, scale=None,
+               store_bf16=False, rows=None):
+    """Attention of every head of query t over its keys, de-rotated at -t.
+
+    q [B,S,H,D] (un-rotated), kv [B,S,D] (un-rotated window latent),
+    ent [B,N,D] (rotated entries) or None, idx [B,S,K] or None (all visible),
+    sink [H] or None.  Returns (o [B,T,H,D], lse [B,T,H]) for the ``rows``.
+    logits = scale * rot(q_h, t) . key; m = max(logits, sink);
+    o = sum_j exp(l_j - m) key_j / (sum_j exp(l_j - m) + exp(sink - m)).
+    An empty key set without a sink gives o = 0, lse = -inf.
+    """
+    q = np.asarray(q, dtype=F64)
+    B, S, H, D = q.shape
+    scale = D ** -0.5 if (scale is None or scale <= 0) else scale
+    rows = np.arange(S) if rows is None else np.asarray(rows)
+    o = np.zeros((B, len(rows), H, D), dtype=F64)
+    lse = np.full((B, len(rows), H), -np.inf, dtype=F64)
+    z = None if sink is None else np.asarray(sink, dtype=F64)
+    for b in range(B):
+        for i, t in enumerate(rows):
+            t = int(t)
+            keys = attention_keys(b, t, kv, ent, idx, inv_freq, ratio, window)
+            qr = rope_rotate(q[b, t], t, inv_freq)               # [H, D]
+            logits = scale * (qr @ keys.T)                       # [H, nk]
+            if keys.shape[0] == 0 and z is None:
+                continue
+            m = logits.max(axis=1) if keys.shape[0] else np.full(H, -np.inf)
+            if z is not None:
+                m = np.maximum(m, z)
+            e = np.exp(logits - m[:, None])
+            den = e.sum(axis=1)
+            if z is not None:
+                den = den + np.exp(z - m)
+            out = (e @ keys) / den[:, None]
+            o[b, i] = rope_derotate(out, t, inv_freq)
+            lse[b, i] = m + np.log(den)
+    return maybe_bf16(o, store_bf16), lse
+
+
+# ---------------------------------------------------------------------------
+# Grouped low-rank output projection  ([BLOG] "The DeepSeek-V4-Flash
+# architecture": 8 groups, each through a 1024-d bottleneck)
+# ---------------------------------------------------------------------------
+def grouped_wo_a(o, wo_a, store_bf16=False):
+    """y[b,t,g,:] = concat_{h in group g} o[b,t,h,:] @ wo_a[g].
+
+    o [B,T,H,D]; wo_a [G, (H/G)*D, rank]; returns [B, T, G*rank].
+    Group g holds heads g*H/G .. (g+1)*H/G - 1, concatenated along D.
+    """
+    o = np.asarray(o, dtype=F64)
+    B, T, H, D = o.shape
+    G, gin, rank = wo_a.shape
+    x = o.reshape(B, T, G, gin)
+    y = np.einsum("btgi,gir->btgr", x, np.asarray(wo_a, dtype=F64))
+    return maybe_bf16(y.reshape(B, T, G * rank), store_bf16)
+
+
+# ---------------------------------------------------------------------------
+# One attention layer
+# ---------------------------------------------------------------------------
+def attn_layer(cfg, x, rows=None):
+    """Whole forward of one layer as the CUDA library composes it.
+
+    cfg: dict with ratio, overlap, window, topk, rms_eps, store_bf16 and
+    optionally softmax_scale.  x: dict of numpy inputs (q, kv, ckv, cscore, ape,
+    norm_w, ickv, icscore, iape, inorm_w, iq, w, sink, inv_freq, wo_a).
+    Returns dict with ent, ikey, idx, iscore, o, lse and (if wo_a) y.
+    """
+    r, ov, W, K = cfg["ratio"], cfg["overlap"], cfg["window"], cfg["topk"]
+    bf = cfg.get("store_bf16", False)
+    eps = cfg.get("rms_eps", 1e-6)
+    res = {"ent": None, "ikey": None, "idx": None, "iscore": None}
+    if r > 0:
+        res["ent"] = compress(x["ckv"], x["cscore"], x["ape"], x.get("norm_w"),
+                              x["inv_freq"], r, ov, eps, hadamard=False, store_bf16=bf)
+        if K > 0:
+            res["ikey"] = compress(x["ickv"], x["icscore"], x["iape"], x.get("inorm_w"),
+                                   x["inv_freq"], r, ov, eps, hadamard=True, store_bf16=bf)
+            sel = indexer_topk(x["iq"], res["ikey"], x["w"], x["inv_freq"], r, K,
+                               store_bf16=bf, rows=rows)
+            res["idx"], res["iscore"] = sel["idx"], sel["iscore"]
+    idx_full = None
+    if res["idx"] is not None:
+        # sparse_mqa indexes idx by absolute position; scatter the sampled rows.
+        B, S = x["q"].shape[:2]
+        idx_full = np.full((B, S, K), -1, dtype=np.int32)
+        rr = np.arange(S) if rows is None else np.asarray(rows)
+        idx_full[:, rr] = res["idx"]
+    o, lse = sparse_mqa(x["q"], x["kv"], res["ent"], idx_full, x.get("sink"),
+                        x["inv_freq"], r, W, cfg.get("softmax_scale"),
+                        store_bf16=bf, rows=rows)
+    res["o"], res["lse"] = o, lse
+    if x.get("wo_a") is not None:
+        res["y"] = grouped_wo_a(o, x["wo_a"], store_bf16=bf)
+    return res

@@ -1,0 +1,81 @@
+"""Plant plausible mistakes in the oracle (CPU only) and check a pin catches each.
+
+Every mutation is applied with monkeypatch to the oracle module, one pin test is
+run against the mutated oracle, and that pin must fail.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import v4_oracle as O
+import tests.test_oracle_pins as P
+
+_rope = O.rope_rotate
+_mqa = O.sparse_mqa
+_had = O.hadamard_matrix
+_pw = O.pooling_weights
+_win = O.window_range
+_comp = O.compress
+
+
+def _flip_sign(x, pos, f):
+    return _rope(x, -np.asarray(pos, dtype=np.float64), f)
+
+
+def _inflated_scale(q, kv, ent, idx, sink, f, r, W, scale=None, **kw):
+    D = np.asarray(q).shape[-1]
+    return _mqa(q, kv, ent, idx, sink, f, r, W, scale=D ** -0.5 * O.yarn_attention_mscale(16.0), **kw)
+
+
+def _ties_high(row, nvis, k):
+    idx = np.full(k, -1, dtype=np.int32)
+    val = np.full(k, -np.inf)
+    if nvis <= 0:
+        return idx, val
+    s = np.arange(nvis)
+    order = np.lexsort((-s, -np.asarray(row[:nvis])))[:min(k, nvis)]
+    idx[:len(order)] = order
+    val[:len(order)] = row[order]
+    return idx, val
+
+
+def _no_ape(cscore, ape, s, r, ov):
+    return _pw(cscore, np.zeros_like(ape), s, r, ov)
+
+
+def _window_off_by_one(t, W):
+    lo, hi = _win(t, W)
+    return (lo, hi - 1) if hi > lo else (lo, hi)
+
+
+def _unnormalised_hadamard(n):
+    return _had(n) * math.sqrt(n)
+
+
+def _rotate_at_entry_index(ckv, cscore, ape, g, f, r, ov, eps, hadamard=False, store_bf16=False):
+    # rotate entries at s instead of r*s: undo r*s rotation then rotate at s
+    e = _comp(ckv, cscore, ape, g, f, r, ov, eps, hadamard=False, store_bf16=False)
+    N = e.shape[1]
+    e = O.rope_rotate(O.rope_derotate(e, (r * np.arange(N))[None, :], f), np.arange(N)[None, :], f)
+    if hadamard:
+        e = e @ _had(e.shape[-1]).T
+    return O.maybe_bf16(e, store_bf16)
+
+
+MUTATIONS = [
+    ("rope_rotate", _flip_sign, P.test_rope_is_complex_multiplication),
+    ("sparse_mqa", _inflated_scale, P.test_softmax_scale_is_head_dim_power),
+    ("topk_select", _ties_high, P.test_topk_matches_brute_force_sort),
+    ("pooling_weights", _no_ape, P.test_ape_row_order_is_chronological),
+    ("window_range", _window_off_by_one, P.test_hca_equals_dense_masked_sdpa),
+    ("hadamard_matrix", _unnormalised_hadamard, P.test_indexer_scores_invariant_under_hadamard),
+    ("compress", _rotate_at_entry_index, P.test_constant_score_gives_mean_of_members),
+]
+
+
+@pytest.mark.parametrize("name,mutant,pin", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pin_catches_planted_mistake(monkeypatch, name, mutant, pin):
+    monkeypatch.setattr(O, name, mutant)
+    with pytest.raises(AssertionError):
+        pin()
