@@ -1,0 +1,491 @@
+#!/usr/bin/env python
+"""Throughput of the DeepSeek-V4-Flash compressed attention forward on GB300.
+
+One step = one CSA layer forward plus one HCA layer forward (the repeating
+pair of the Flash stack), B=1, S=16384, 64 heads, 512-d latent, bf16, inputs
+resident in HBM (q and o alone are 1 GiB each per layer, far above the 129 MB
+L2, so no flush is needed).  value = tokens through the pair per second, over
+all ranks; each rank runs its own sequence (weak scaling, no collective on the
+data path).
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "attention-layer fwd tokens/s at S=16K (CSA & HCA)"
+WORKLOAD = ("DeepSeek-V4-Flash attention layer pair fwd: CSA (ratio 4 overlapped, indexer 64x128 "
+            "fp32 scoring, top-512, window 128) + HCA (ratio 128, window 128), B=1, S=16384, "
+            "H=64, D=512, R=64, bf16")
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic work (causal-exact) of one layer
+# ---------------------------------------------------------------------------
+def n_visible(t, r):
+    return (t + 1) // r if r > 0 else 0
+
+
+def attention_keys_total(S, r, K, W):
+    t = np.arange(S, dtype=np.int64)
+    nv = (t + 1) // r if r > 0 else np.zeros(S, dtype=np.int64)
+    ne = np.minimum(nv, K) if K > 0 else nv
+    nw = np.minimum(t + 1, W) if W >= 0 else t + 1
+    return int((ne + nw).sum())
+
+
+def layer_work(p):
+    B, S, H, D, r, K, W = p["B"], p["S"], p["H"], p["D"], p["ratio"], p["K"], p["W"]
+    keys = attention_keys_total(S, r, K, W)
+    attn_flops = 4.0 * B * H * D * keys
+    attn_bytes = 2.0 * B * S * H * D * 2            # q read + o written (bf16)
+    t = np.arange(S, dtype=np.int64)
+    idx_pairs = int(((t + 1) // r).sum()) if (r > 0 and K > 0) else 0
+    idx_flops = 2.0 * B * p["Hi"] * p["Di"] * idx_pairs
+    return dict(attn_flops=attn_flops, attn_bytes=attn_bytes, attn_keys=keys * B,
+                idx_flops=idx_flops, idx_pairs=idx_pairs * B)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d["bf16_tflops_sustained"]), src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, src="fallback")
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        self.file.flush()
+        rows = []
+        for line in open(self.file.name):
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts + frac, float(parts[2]), float(parts[3]), parts[6:10]))
+            except Exception:
+                continue
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        use = inside if inside else sorted(rows, key=lambda r: abs(r[0] - (t0 + t1) / 2))[:3]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i in range(4) if r[3][i].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use), "samples_inside_timed_region": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# Distributed helpers (one process per GPU; timing protocol only)
+# ---------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def smi_index(local):
+    """nvidia-smi index of this rank's GPU (honours CUDA_VISIBLE_DEVICES)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [v.strip() for v in vis.split(",") if v.strip()]
+    if local < len(ids):
+        return ids[local]
+    return str(local)
+
+
+def max_over_ranks(value, device=None):
+    """Max of a float over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value, device=None):
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+def make_layer(name, S, device, seed):
+    import torch
+
+    import seeded_inputs as SI
+    import sparse_compressed_attention_gb300 as V
+    p = SI.preset(name, S=S)
+    x = SI.make_layer_inputs(p, device, seed=seed)
+    yarn = p["yarn"]
+    f = V.v4_rope_inv_freq(p["theta"], p["R"], yarn, SI.YARN_ORIGINAL_LEN if yarn > 1 else 0,
+                           SI.YARN_BETA_FAST, SI.YARN_BETA_SLOW).to(device)
+    x["inv_freq"] = f
+    cfg = V.config_from_preset(p)
+    B, H = p["B"], p["H"]
+    outs = {"o": torch.empty_like(x["q"]), "lse": torch.empty(B, S, H, device=device)}
+    if p["K"] > 0:
+        outs["idx"] = torch.empty(B, S, p["K"], dtype=torch.int32, device=device)
+    ws = V.alloc_workspace(cfg, device)
+    return dict(name=name, p=p, x=x, outs=outs, cfg=cfg, ws=ws)
+
+
+def run_layer(L, stream=None):
+    import sparse_compressed_attention_gb300 as V
+    V.v4_attn_layer_fwd(L["cfg"], L["x"], L["outs"], L["ws"], stream)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import sparse_compressed_attention_gb300 as V
+    from sparse_compressed_attention_gb300 import build as B
+    ws_, rank, local = dist_env()
+    if ws_ > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or local == 0:
+        B.build()
+    barrier()
+    V.lib()
+    S = args.seq
+    layers = [make_layer("csa_bf16_16k", S, dev, seed=1000 + 2 * rank),
+              make_layer("hca_bf16_16k", S, dev, seed=1001 + 2 * rank)]
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        for L in layers:
+            run_layer(L)
+    torch.cuda.synchronize(dev)
+
+    clk = ClockSampler(smi_index(local))
+    clk.start()
+    # keep the GPU busy briefly so the sampler sees load before the timed region
+    t_pre = time.time()
+    while time.time() - t_pre < 0.3:
+        for L in layers:
+            run_layer(L)
+        torch.cuda.synchronize(dev)
+    V.v4_profile_enable(True)
+    launches0 = V.v4_launch_count()
+    marks = []
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        for L in layers:
+            run_layer(L)
+            marks.append((L["name"], V.v4_profile_count()))
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    barrier()
+    launches = V.v4_launch_count() - launches0
+    V.v4_profile_enable(False)
+    clk.stop()
+    clocks = clk.summary(t0, t1)
+    ms_local = ev0.elapsed_time(ev1)
+    ms = max_over_ranks(ms_local, dev)
+    status = V.v4_get_device_status()
+
+    # per-kernel durations from the live event records of the timed region
+    recs = V.v4_profile_records()
+    per = {}
+    start = 0
+    for name, end in marks:
+        for kind, t in recs[start:end]:
+            per.setdefault((name, kind), []).append(t)
+        start = end
+    kern = {"%s/%s" % k: {"launches": len(v), "avg_ms": sum(v) / len(v), "total_ms": sum(v)}
+            for k, v in per.items()}
+
+    tokens_rank = sum(L["p"]["B"] * L["p"]["S"] for L in layers[:1])   # tokens through the pair
+    tokens = sum_over_ranks(tokens_rank * args.steps, dev)
+    value = tokens / (ms / 1e3)
+
+    peaks = load_peaks()
+    work = {L["name"]: layer_work(L["p"]) for L in layers}
+    csa_attn = per.get(("csa_bf16_16k", "attention"), [])
+    hca_attn = per.get(("hca_bf16_16k", "attention"), [])
+    roof = None
+    if csa_attn:
+        a_ms = sum(csa_attn) / len(csa_attn)
+        achieved = work["csa_bf16_16k"]["attn_flops"] / (a_ms / 1e3) / 1e12
+        roof = {"kernel": "csa attention (sparse MQA, 64 heads x 512, top-512 + window 128)",
+                "bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4), "traffic": None,
+                "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % peaks["src"],
+                "flops_per_launch": work["csa_bf16_16k"]["attn_flops"], "avg_launch_ms": round(a_ms, 4)}
+    extra_roofs = []
+    if hca_attn:
+        a_ms = sum(hca_attn) / len(hca_attn)
+        gbs = work["hca_bf16_16k"]["attn_bytes"] / (a_ms / 1e3) / 1e9
+        extra_roofs.append({"kernel": "hca attention", "bound": "hbm", "achieved": round(gbs, 1),
+                            "peak": peaks["hbm"], "unit": "GB/s", "frac": round(gbs / peaks["hbm"], 4),
+                            "bytes_per_launch": work["hca_bf16_16k"]["attn_bytes"],
+                            "avg_launch_ms": round(a_ms, 4)})
+    isc = per.get(("csa_bf16_16k", "indexer_scores"), [])
+    if isc:
+        a_ms = sum(isc) / len(isc)
+        tf = work["csa_bf16_16k"]["idx_flops"] / (a_ms / 1e3) / 1e12
+        extra_roofs.append({"kernel": "csa indexer scores", "bound": "tensor", "achieved": round(tf, 2),
+                            "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": round(tf / peaks["bf16"], 4),
+                            "flops_per_launch": work["csa_bf16_16k"]["idx_flops"],
+                            "avg_launch_ms": round(a_ms, 4)})
+
+    e2e = run_e2e(args, layers, dev) if args.e2e_steps > 0 else None
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws_,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; activations unit-RMS N(0,1), q from a random rank-1024 path)",
+        "config": {"workload": WORKLOAD, "global_batch": ws_, "seq_len": S, "layers_per_step": 2,
+                   "parallelism": "replicas" if ws_ > 1 else "single",
+                   "l2": "no flush: inputs larger than L2 (q and o 1 GiB per layer)"},
+        "clocks": clocks, "gpu_launches": launches, "device_status": status,
+        "roofline": roof, "roofline_other": extra_roofs, "kernels": kern,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args, layers)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws_ > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, layers, dev):
+    """Same step through the C ABI with inputs in pinned host memory: every
+    step copies its inputs host->device and the outputs o device->host."""
+    import torch
+    hosts = []
+    h2d = d2h = 0
+    for L in layers:
+        hx = {k: (v.to("cpu").pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in L["x"].items()}
+        ho = L["outs"]["o"].to("cpu").pin_memory()
+        hosts.append((hx, ho))
+        h2d += sum(v.numel() * v.element_size() for v in hx.values() if isinstance(v, torch.Tensor))
+        d2h += ho.numel() * ho.element_size()
+    n = args.e2e_steps
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        for L, (hx, ho) in zip(layers, hosts):
+            for k, v in hx.items():
+                if isinstance(v, torch.Tensor):
+                    L["x"][k].copy_(v, non_blocking=True)
+            run_layer(L)
+            ho.copy_(L["outs"]["o"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    tokens = sum_over_ranks(layers[0]["p"]["B"] * layers[0]["p"]["S"] * n, dev)
+    return {"value": round(tokens / (ms / 1e3), 1), "unit": "tokens/s", "steps": n,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample (rank 0 only)
+# ---------------------------------------------------------------------------
+def oracle_sample(inputs_by_layer, rows_per_layer):
+    """Time the oracle on: the full compressors of both layers, plus indexer
+    and attention for `rows_per_layer` evenly spaced query rows per layer.
+    Returns (seconds extrapolated to all S rows of both layers, seconds spent)."""
+    from oracle import v4_oracle as O
+    total_est = 0.0
+    spent = 0.0
+    for name, (p, x) in inputs_by_layer.items():
+        S = p["S"]
+        rows = np.linspace(0, S - 1, rows_per_layer).round().astype(np.int64)
+        ta = time.perf_counter()
+        ent = O.compress(x["ckv"], x["cscore"], x["ape"], x["norm_w"], x["inv_freq"], p["ratio"],
+                         p["overlap"], 1e-6, store_bf16=True)
+        ikey = None
+        if p["K"] > 0:
+            ikey = O.compress(x["ickv"], x["icscore"], x["iape"], x["inorm_w"], x["inv_freq"],
+                              p["ratio"], p["overlap"], 1e-6, hadamard=True, store_bf16=True)
+        tb = time.perf_counter()
+        idx_rows = None
+        if p["K"] > 0:
+            sel = O.indexer_topk(x["iq_rows"], ikey, x["w_rows"], x["inv_freq"], p["ratio"], p["K"],
+                                 store_bf16=True, rows=rows, rows_only=True)
+            idx_rows = sel["idx"]
+        O.sparse_mqa(x["q_rows"], x["kv"], ent, idx_rows, None, x["inv_freq"], p["ratio"], p["W"],
+                     store_bf16=True, rows=rows, rows_only=True)
+        tc = time.perf_counter()
+        total_est += (tb - ta) + (tc - tb) * S / len(rows)
+        spent += tc - ta
+    return total_est, spent
+
+
+def gather_oracle_inputs(layers, rows_per_layer):
+    import torch
+    out = {}
+    for L in layers:
+        p, x = L["p"], L["x"]
+        S = p["S"]
+        rows = torch.from_numpy(np.linspace(0, S - 1, rows_per_layer).round().astype(np.int64))
+        d = {k: x[k].detach().double().cpu().numpy() for k in
+             ("kv", "ckv", "cscore", "ape", "norm_w") if x.get(k) is not None}
+        d["inv_freq"] = x["inv_freq"].cpu().numpy()
+        d["q_rows"] = x["q"][:, rows.to(x["q"].device)].double().cpu().numpy()
+        if p["K"] > 0:
+            for k in ("ickv", "icscore", "iape", "inorm_w"):
+                d[k] = x[k].detach().double().cpu().numpy()
+            d["iq_rows"] = x["iq"][:, rows.to(x["iq"].device)].double().cpu().numpy()
+            d["w_rows"] = x["w"][:, rows.to(x["w"].device)].double().cpu().numpy()
+        out[L["name"]] = (p, d)
+    return out
+
+
+def cpu_baseline(args, layers):
+    inputs = gather_oracle_inputs(layers, args.cpu_rows)
+    est, spent = oracle_sample(inputs, args.cpu_rows)
+    S = layers[0]["p"]["S"]
+    return {"value": round(S / est, 2), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": "numpy float64 oracle: full compressors of both layers + indexer/attention for "
+                      "%d evenly spaced query rows per layer, extrapolated to S=%d (%.1f s of CPU work)"
+                      % (args.cpu_rows, S, spent)}
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the CPU oracle as the comparison program
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    import torch
+
+    import seeded_inputs as SI
+    from oracle import v4_oracle as O
+    ws_, rank, _ = dist_env()
+    if rank != 0:
+        return
+    S = args.seq
+    layers = []
+    for name, seed in (("csa_bf16_16k", 1000), ("hca_bf16_16k", 1001)):
+        p = SI.preset(name, S=S)
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        x = SI.make_layer_inputs(p, dev, seed=seed)
+        x["inv_freq"] = torch.from_numpy(O.make_inv_freq(p["theta"], p["R"], p["yarn"],
+                                                         SI.YARN_ORIGINAL_LEN if p["yarn"] > 1 else 0))
+        layers.append(dict(name=name, p=p, x=x))
+    inputs = gather_oracle_inputs(layers, args.ref_rows)
+    for _ in range(args.warmup):
+        oracle_sample(inputs, args.ref_rows)
+    ests = []
+    spent = 0.0
+    for _ in range(args.steps):
+        e, s = oracle_sample(inputs, args.ref_rows)
+        ests.append(e)
+        spent += s
+    est = sum(ests) / len(ests)
+    value = S / est
+    cb = {"value": round(value, 2), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+          "sample": "numpy float64 oracle per step: full compressors + indexer/attention for %d query "
+                    "rows per layer, extrapolated to S=%d" % (args.ref_rows, S)}
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
+            "n_gpus": ws_, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(est * 1e3, 1), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": S, "layers_per_step": 2},
+            "cpu_baseline": cb,
+            "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seq", type=int, default=16384)
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-rows", type=int, default=24)
+    ap.add_argument("--ref-rows", type=int, default=6)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,267 @@
+/*
+ * v4attn.h - C ABI of the DeepSeek-V4-Flash compressed attention forward
+ * (compressor, CSA lightning indexer with top-k, sparse/dense multi-query
+ * attention with sliding window and de-rotated output) on one GB300 GPU.
+ *
+ * Sources of the operations:
+ *   [PR]   Primus PR #930 "fix(deepseek-v4): correct V4-Flash attention math,
+ *          wire the MoE balance loss", Part 1 (items 1-6, 8).
+ *   [BLOG] "Enabling DeepSeek-V4-Flash Training on AMD Instinct MI355X GPUs
+ *          with Primus", sections "The DeepSeek-V4-Flash architecture",
+ *          "Three attention types, interleaved", "Kernel fusions".
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are dense, row-major, in device memory owned by the caller.
+ *     The library never allocates device memory; scratch space is the
+ *     caller's workspace (see v4_workspace_size).  Every device pointer must
+ *     be 16-byte aligned.
+ *   - "Storage dtype" (cfg->dtype) is the element type of q, kv, the pooling
+ *     projections, entries, indexer keys/queries and the output: V4_F32 or
+ *     V4_BF16.  ape, norm weights, indexer weights w, sink, inv_freq, lse
+ *     and iscore are always float32.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and runs asynchronously.  A non-V4_OK return means nothing was
+ *     enqueued; v4_last_error() gives the reason.  Arguments are validated on
+ *     the host before any launch.
+ *   - Problems found on the device (an out-of-range selected index, a timed
+ *     out wait) never trap: they set a sticky status word that
+ *     v4_get_device_status() reads.  Offending keys are skipped.
+ *   - Entry points may be called from several host threads; the error text
+ *     is per thread.
+ *
+ * Notation: B batch, S sequence length, H query heads, D latent (head) dim,
+ * R rotated dims (the last R of D), r compression ratio, ov overlap (0/1),
+ * N = S / r entries (floor), Hi / Di indexer heads / dim, K top-k, W window.
+ */
+#ifndef V4ATTN_H
+#define V4ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  V4_OK = 0,
+  V4_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or combination */
+  V4_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. forced path) */
+  V4_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
+  V4_ERR_CUDA = 4,          /* a CUDA runtime call failed */
+  V4_ERR_TIMEOUT = 5,       /* device status: a bounded wait gave up */
+  V4_ERR_BAD_INDEX = 6      /* device status: a selected index was not visible */
+} v4_status;
+
+typedef enum { V4_F32 = 0, V4_BF16 = 1 } v4_dtype;
+
+/* Kernel family selection (cfg->path). AUTO picks the tensor-core kernels
+ * when the shapes and dtype allow it, otherwise the CUDA-core kernels. */
+typedef enum { V4_PATH_AUTO = 0, V4_PATH_SIMT = 1, V4_PATH_TC = 2 } v4_path;
+
+typedef struct v4_config {
+  int32_t batch;          /* B >= 1 */
+  int32_t seqlen;         /* S >= 1 */
+  int32_t n_heads;        /* H >= 1 (Flash: 64) */
+  int32_t head_dim;       /* D, multiple of 32, 32..1024 (Flash: 512) */
+  int32_t rope_dim;       /* R, multiple of 8, <= D (Flash: 64) */
+  int32_t ratio;          /* r: 0 = window-only layer, 4 = CSA, 128 = HCA; any r >= 1 */
+  int32_t overlap;        /* ov: 1 = each entry also pools the previous r tokens (CSA) */
+  int32_t window;         /* W: tokens [t-W+1, t]; 0 = no window; -1 = all tokens <= t */
+  int32_t topk;           /* K: 0 = attend to every visible entry (HCA); > 0 = CSA selection */
+  int32_t idx_heads;      /* Hi (Flash: 64) */
+  int32_t idx_dim;        /* Di, power of two, 8..256, >= R (Flash: 128) */
+  int32_t o_groups;       /* grouped output projection: groups (Flash: 8) */
+  int32_t o_rank;         /* grouped output projection: rank per group (Flash: 1024) */
+  float softmax_scale;    /* <= 0 selects D^-0.5, the only value [PR] item 1 allows */
+  float rms_eps;          /* entry RMSNorm epsilon (1e-6) */
+  int32_t dtype;          /* v4_dtype: storage dtype */
+  int32_t path;           /* v4_path */
+} v4_config;
+
+/* ----------------------------------------------------------------------
+ * RoPE inverse-frequency table (host function, no GPU).
+ * [PR] items 2 and 8: compressed layers rotate with base 40000 paired with a
+ * YaRN factor (16) acting on the inverse frequencies.  Base table
+ * theta^(-2j/R); YaRN "NTK-by-parts" (Peng et al. 2023, section 3.2) with
+ * ramp bounds beta_slow..beta_fast applies when yarn_factor > 1 and
+ * original_len > 0.  inv_freq: host array of R/2 floats, written.
+ * --------------------------------------------------------------------*/
+v4_status v4_rope_inv_freq(float theta, int32_t rope_dim, float yarn_factor,
+                           int32_t original_len, float beta_fast, float beta_slow,
+                           float* inv_freq);
+
+/* Bytes of workspace that every entry point below needs for `cfg` (the
+ * largest of their needs, so one buffer serves them all). */
+v4_status v4_workspace_size(const v4_config* cfg, size_t* bytes);
+
+/* ----------------------------------------------------------------------
+ * Compressor (one learned pooling operator for CSA and HCA).
+ * [BLOG] "Three attention types, interleaved" (softmax over the group biased
+ * by a learnable per-position term; CSA groups overlap: own r tokens plus
+ * the previous r) and "Kernel fusions", row "Compressor pooling";
+ * [PR] item 1 (entries are RMSNormed), item 2 (entry s rotated at r*s),
+ * item 6e (indexer keys: RoPE then normalised Hadamard).
+ *
+ *   ckv, cscore : [B, S, 1+ov, dim] storage dtype. Half 0 is the token's
+ *                 projection for its own group, half 1 for the next group
+ *                 (used as "previous" members).
+ *   ape         : [(1+ov)*r, dim] fp32. Rows are chronological: with
+ *                 overlap rows 0..r-1 bias the previous group's tokens,
+ *                 rows r..2r-1 the own tokens.
+ *   norm_w      : [dim] fp32 RMSNorm weight, NULL = ones.
+ *   inv_freq    : [R/2] fp32 device array.
+ *   dim         : channel count (D for the attention entries, Di for the
+ *                 indexer keys); R <= dim.
+ *   hadamard    : 1 = apply the normalised Sylvester Hadamard (dim must be a
+ *                 power of two) after the rotation.
+ *   out         : [B, N, dim] storage dtype, N = S / r.
+ * Per entry s and channel c: pooled = sum_m softmax_m(cscore + ape) * ckv over
+ * the members m (entry 0 has no previous group; absent members are left out),
+ * then e = pooled / sqrt(mean_c pooled^2 + eps) * g, rotated at position r*s.
+ * --------------------------------------------------------------------*/
+v4_status v4_compress(const v4_config* cfg, const void* ckv, const void* cscore,
+                      const float* ape, const float* norm_w, const float* inv_freq,
+                      int32_t dim, int32_t hadamard, void* out, void* stream);
+
+/* ----------------------------------------------------------------------
+ * Indexer query preparation.  [PR] item 6e: queries rotated at their own
+ * position t (partial RoPE at the compressed base), then the normalised
+ * Hadamard.  iq: [B, S, Hi, Di] -> iq_prep: [B, S, Hi, Di], storage dtype.
+ * --------------------------------------------------------------------*/
+v4_status v4_indexer_prep(const v4_config* cfg, const void* iq, const float* inv_freq,
+                          void* iq_prep, void* stream);
+
+/* ----------------------------------------------------------------------
+ * Lightning indexer scores and top-k selection (CSA).
+ * [PR] item 6a (per-head weights scaled by Hi^-1/2 * Di^-1/2), item 4 (the
+ * QK stays in high precision: bf16 operands, fp32 accumulation, fp32
+ * scoring and selection); [BLOG] "Kernel fusions", row "Indexer scoring tail"
+ * (ReLU, per-head weight, head sum, inline causal mask) and "Three attention
+ * types" (keep the best 512).
+ *
+ *   I[t,s] = sum_h w[t,h] * (Hi*Di)^-1/2 * max(0, iq~[t,h] . ikey[s]),
+ *   defined for s < n_vis(t) = (t+1)/r; the best min(K, n_vis(t)) are kept,
+ *   equal scores going to the lower index.
+ *
+ *   iq          : [B, S, Hi, Di]; un-rotated (iq_prepared = 0) or already
+ *                 prepared by v4_indexer_prep (iq_prepared = 1).
+ *   ikey        : [B, N, Di] from v4_compress(dim = Di, hadamard = 1).
+ *   w           : [B, S, Hi] fp32 per-head weights (unscaled).
+ *   idx         : [B, S, K] int32 out. The selected entries of row t in
+ *                 ascending index order, then -1 padding.
+ *   iscore      : [B, S, K] fp32 out, nullable: I[t, idx] (-inf on padding).
+ *   workspace   : at least v4_workspace_size bytes.
+ * --------------------------------------------------------------------*/
+v4_status v4_indexer_topk(const v4_config* cfg, const void* iq, int32_t iq_prepared,
+                          const void* ikey, const float* w, const float* inv_freq,
+                          int32_t* idx, float* iscore, void* workspace,
+                          size_t ws_bytes, void* stream);
+
+/* ----------------------------------------------------------------------
+ * Sparse / dense multi-query attention with sliding window, sink and
+ * de-rotated output.
+ * [BLOG] "The DeepSeek-V4-Flash architecture" (64 heads read one 512-d latent
+ * that is both key and value), "Three attention types" (selected entries or
+ * all HCA entries, plus the 128-token window), "Kernel fusions", row
+ * "SWA / CSA / HCA attention" (window and softmax sink in one kernel);
+ * [PR] item 1 (scale exactly D^-0.5), item 3 (output de-rotated at -t).
+ *
+ * For query t and head h: keys J(t) = idx[t] (K > 0), or every visible entry
+ * s < n_vis(t) (K = 0, r > 0), or none (r = 0); plus window tokens u in
+ * [max(0,t-W+1), t] rotated at u.  logits = scale * rot(q[t,h], t) . key;
+ * softmax over J(t) with the optional sink logit sink[h] in the
+ * denominator; o = sum p * key (V = K); o's last R dims rotated at -t.
+ *
+ *   q    : [B, S, H, D] un-rotated.           kv   : [B, S, D] un-rotated.
+ *   ent  : [B, N, D] rotated entries (v4_compress); NULL iff r == 0.
+ *   idx  : [B, S, K] int32; -1 = unused slot; NULL = all visible entries.
+ *          Values >= n_vis(t) or < -1 are skipped and flagged
+ *          (V4_ERR_BAD_INDEX in the device status).
+ *   sink : [H] fp32, nullable.
+ *   o    : [B, S, H, D] out.   lse : [B, S, H] fp32 out (natural log), nullable.
+ * An empty key set without a sink yields o = 0 and lse = -inf.
+ * --------------------------------------------------------------------*/
+v4_status v4_sparse_mqa_fwd(const v4_config* cfg, const void* q, const void* kv,
+                            const void* ent, const int32_t* idx, const float* sink,
+                            const float* inv_freq, void* o, float* lse,
+                            void* workspace, size_t ws_bytes, void* stream);
+
+/* ----------------------------------------------------------------------
+ * Grouped low-rank output projection.  [BLOG] "The DeepSeek-V4-Flash
+ * architecture": the 64 x 512 output splits into o_groups groups, each
+ * through an o_rank bottleneck.  Group g holds heads g*H/G .. (g+1)*H/G-1
+ * concatenated along D.
+ *   o    : [B, S, H, D];  wo_a : [G, (H/G)*D, o_rank];  y : [B, S, G*o_rank].
+ * bf16 storage only.
+ * --------------------------------------------------------------------*/
+v4_status v4_grouped_o_proj(const v4_config* cfg, const void* o, const void* wo_a,
+                            void* y, void* stream);
+
+/* Pointers of one layer call. Nullable fields are marked. */
+typedef struct v4_layer_inputs {
+  const void* q;         /* [B,S,H,D] */
+  const void* kv;        /* [B,S,D] window latent */
+  const void* ckv;       /* [B,S,1+ov,D]     (r > 0) */
+  const void* cscore;    /* [B,S,1+ov,D]     (r > 0) */
+  const float* ape;      /* [(1+ov)r, D]     (r > 0) */
+  const float* norm_w;   /* [D], nullable */
+  const void* ickv;      /* [B,S,1+ov,Di]    (K > 0) */
+  const void* icscore;   /* [B,S,1+ov,Di]    (K > 0) */
+  const float* iape;     /* [(1+ov)r, Di]    (K > 0) */
+  const float* inorm_w;  /* [Di], nullable */
+  const void* iq;        /* [B,S,Hi,Di] un-rotated (K > 0) */
+  const float* w;        /* [B,S,Hi]         (K > 0) */
+  const float* sink;     /* [H], nullable */
+  const float* inv_freq; /* [R/2] */
+  const void* wo_a;      /* [G,(H/G)D,o_rank], nullable = no projection */
+} v4_layer_inputs;
+
+typedef struct v4_layer_outputs {
+  void* o;               /* [B,S,H,D] */
+  float* lse;            /* [B,S,H], nullable */
+  void* ent;             /* [B,N,D], nullable (kept in the workspace) */
+  void* ikey;            /* [B,N,Di], nullable (kept in the workspace) */
+  int32_t* idx;          /* [B,S,K], nullable (kept in the workspace) */
+  float* iscore;         /* [B,S,K], nullable */
+  void* y;               /* [B,S,G*o_rank], required iff wo_a != NULL */
+} v4_layer_outputs;
+
+/* ----------------------------------------------------------------------
+ * One attention layer: compressor (r > 0), indexer keys + query prep +
+ * scores + top-k (K > 0), attention with window and de-rotation, optional
+ * grouped output projection; all on `stream`, no host synchronisation.
+ * [PR] Part 1 as a whole; [BLOG] "Three attention types, interleaved".
+ * --------------------------------------------------------------------*/
+v4_status v4_attn_layer_fwd(const v4_config* cfg, const v4_layer_inputs* in,
+                            v4_layer_outputs* out, void* workspace, size_t ws_bytes,
+                            void* stream);
+
+/* Text of the last non-OK status returned on this host thread ("" if none). */
+const char* v4_last_error(void);
+
+/* Copy the sticky device status word (a v4_status value, 0 = clean) after
+ * synchronising `stream`.  v4_reset_device_status clears it (async). */
+v4_status v4_get_device_status(void* stream, int32_t* status);
+v4_status v4_reset_device_status(void* stream);
+
+/* Number of kernels this library has launched since it was loaded. */
+uint64_t v4_launch_count(void);
+
+/* ----------------------------------------------------------------------
+ * Per-stage timing.  While enabled, every stage launch is bracketed by two
+ * CUDA events recorded on the stage's stream, so the timing sees exactly the
+ * stage's kernels in stream order.  v4_profile_enable(1) discards earlier
+ * records and starts recording; v4_profile_enable(0) stops.  Record i
+ * (launch order, 0-based) is read with v4_profile_get, which waits for its
+ * stop event.  kind: 0 compressor, 1 window-key rotation, 2 indexer query
+ * prep, 3 indexer scores, 4 top-k, 5 attention, 6 output projection.
+ * --------------------------------------------------------------------*/
+v4_status v4_profile_enable(int32_t on);
+int32_t v4_profile_count(void);
+v4_status v4_profile_get(int32_t i, int32_t* kind, float* ms);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* V4ATTN_H */

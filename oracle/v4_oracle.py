@@ -243,23 +243,25 @@ def indexer_scale(idx_heads, idx_dim):
     return 1.0 / math.sqrt(idx_heads) / math.sqrt(idx_dim)
 
 
-def indexer_query_prep(iq, inv_freq, store_bf16=False):
+def indexer_query_prep(iq, inv_freq, store_bf16=False, positions=None):
     """Queries rotated at their own positions t, then the normalised Hadamard.
 
-    iq: [B, S, Hi, Di] -> same shape.
+    iq: [B, T, Hi, Di] -> same shape; row i sits at position positions[i]
+    (default: positions 0..T-1).
     """
     iq = np.asarray(iq, dtype=F64)
-    S = iq.shape[1]
-    x = rope_rotate(iq, np.arange(S)[None, :, None], inv_freq)
+    pos = np.arange(iq.shape[1]) if positions is None else np.asarray(positions)
+    x = rope_rotate(iq, pos[None, :, None], inv_freq)
     x = x @ hadamard_matrix(iq.shape[-1]).T
     return maybe_bf16(x, store_bf16)
 
 
-def indexer_scores(iq_prep, ikey, w, ratio, rows=None):
+def indexer_scores(iq_prep, ikey, w, ratio, rows=None, rows_only=False):
     """I[b, t, s] = sum_h w[b,t,h] * (Hi*Di)^-1/2 * max(0, q~[b,t,h] . k[b,s]).
 
     Defined for s < n_visible(t); other entries are -inf.  ``rows`` selects the
-    query positions (default: all).  Returns [B, len(rows), N].
+    query positions (default: all); with ``rows_only`` the query and weight
+    arrays hold just those rows, in order.  Returns [B, len(rows), N].
     """
     iq_prep = np.asarray(iq_prep, dtype=F64)
     ikey = np.asarray(ikey, dtype=F64)
@@ -274,8 +276,9 @@ def indexer_scores(iq_prep, ikey, w, ratio, rows=None):
             nv = min(n_visible(int(t), ratio), N)
             if nv == 0:
                 continue
-            dots = iq_prep[b, t] @ ikey[b, :nv].T          # [Hi, nv]
-            out[b, i, :nv] = (w[b, t] * c) @ np.maximum(dots, 0.0)
+            r = i if rows_only else t
+            dots = iq_prep[b, r] @ ikey[b, :nv].T          # [Hi, nv]
+            out[b, i, :nv] = (w[b, r] * c) @ np.maximum(dots, 0.0)
     return out
 
 
@@ -299,16 +302,21 @@ def topk_select(score_row, nvis, k):
 
 
 def indexer_topk(iq, ikey, w, inv_freq, ratio, k, store_bf16=False, rows=None,
-                 prepared=False):
+                 prepared=False, rows_only=False):
     """Indexer from un-rotated queries (or prepared ones) to top-k index sets.
 
+    With ``rows_only`` the iq and w arrays hold just the listed rows.
     Returns dict(idx [B,T,k] int32, iscore [B,T,k], scores [B,T,N]).
     """
-    qp = np.asarray(iq, dtype=F64) if prepared else indexer_query_prep(iq, inv_freq, store_bf16)
-    sc = indexer_scores(qp, ikey, w, ratio, rows)
-    B, T, N = sc.shape
-    S = qp.shape[1]
+    S = np.asarray(iq).shape[1]
     rows_ = np.arange(S) if rows is None else np.asarray(rows)
+    if not rows_only and rows is not None:
+        iq = np.asarray(iq)[:, rows_]
+        w = np.asarray(w)[:, rows_]
+    qp = np.asarray(iq, dtype=F64) if prepared else indexer_query_prep(iq, inv_freq, store_bf16,
+                                                                       positions=rows_)
+    sc = indexer_scores(qp, ikey, w, ratio, rows_, rows_only=True)
+    B, T, N = sc.shape
     idx = np.full((B, T, k), -1, dtype=np.int32)
     isc = np.full((B, T, k), -np.inf, dtype=F64)
     for b in range(B):
@@ -324,13 +332,17 @@ def indexer_topk(iq, ikey, w, inv_freq, ratio, k, store_bf16=False, rows=None,
 # fusions", row "SWA / CSA / HCA attention": window and sink in one softmax;
 # [PR] item 1: scale head_dim ** -0.5; item 3: de-rotate the output at -t)
 # ---------------------------------------------------------------------------
-def attention_keys(b, t, kv, ent, idx, inv_freq, ratio, window):
-    """Keys (= values) of query t: the chosen entries, then the window tokens."""
+def attention_keys(b, i, kv, ent, idx, inv_freq, ratio, window, t=None):
+    """Keys (= values) of query t: the chosen entries, then the window tokens.
+
+    idx row i of batch b lists query t's selection (t defaults to i).
+    """
+    t = i if t is None else t
     parts = []
     if ratio > 0 and ent is not None:
         nv = min(n_visible(t, ratio), ent.shape[1])
         if idx is not None:
-            sel = np.asarray(idx[b, t])
+            sel = np.asarray(idx[b, i])
             sel = sel[sel >= 0]
             if np.any(sel >= nv):
                 raise ValueError("selected entry is not causally visible")
@@ -347,7 +359,7 @@ def attention_keys(b, t, kv, ent, idx, inv_freq, ratio, window):
 
 
 def sparse_mqa(q, kv, ent, idx, sink, inv_freq, ratio, window, scale=None,
-               store_bf16=False, rows=None):
+               store_bf16=False, rows=None, rows_only=False):
     """Attention of every head of query t over its keys, de-rotated at -t.
 
     q [B,S,H,D] (un-rotated), kv [B,S,D] (un-rotated window latent),
@@ -355,7 +367,8 @@ def sparse_mqa(q, kv, ent, idx, sink, inv_freq, ratio, window, scale=None,
     sink [H] or None.  Returns (o [B,T,H,D], lse [B,T,H]) for the ``rows``.
     logits = scale * rot(q_h, t) . key; m = max(logits, sink);
     o = sum_j exp(l_j - m) key_j / (sum_j exp(l_j - m) + exp(sink - m)).
-    An empty key set without a sink gives o = 0, lse = -inf.
+    An empty key set without a sink gives o = 0, lse = -inf.  With
+    ``rows_only`` q and idx hold just the listed rows, in order.
     """
     q = np.asarray(q, dtype=F64)
     B, S, H, D = q.shape
@@ -367,8 +380,11 @@ def sparse_mqa(q, kv, ent, idx, sink, inv_freq, ratio, window, scale=None,
     for b in range(B):
         for i, t in enumerate(rows):
             t = int(t)
-            keys = attention_keys(b, t, kv, ent, idx, inv_freq, ratio, window)
-            qr = rope_rotate(q[b, t], t, inv_freq)               # [H, D]
+            r = i if rows_only else t
+            sel = None if idx is None else np.asarray(idx)[b:b + 1, r:r + 1]
+            keys = attention_keys(0, 0, kv[b:b + 1], None if ent is None else ent[b:b + 1], sel,
+                                  inv_freq, ratio, window, t=t)
+            qr = rope_rotate(q[b, r], t, inv_freq)               # [H, D]
             logits = scale * (qr @ keys.T)                       # [H, nk]
             if keys.shape[0] == 0 and z is None:
                 continue

@@ -89,12 +89,15 @@ def make_layer_inputs(p, device="cpu", seed=0, sink=False, wo_a=False):
     w ~ N(0,1); norm weights are ones.  With q_mode "lowrank" the queries come
     from the rank-1024 path: qlat = unit-RMS N(0,1) [B,S,1024], q = per-head
     unit-RMS(qlat @ Wq), iq = qlat @ Wiq with Wq, Wiq ~ N(0, 0.02).
-    Returns a dict of tensors; activations in the preset's storage dtype,
-    parameters (ape, norm weights, w, sink) in float32.
+    Tensors a layer does not use (pooling inputs without compression, indexer
+    inputs without selection) are not drawn.  Returns a dict of tensors;
+    activations in the preset's storage dtype, parameters (ape, norm weights,
+    w, sink) in float32.
     """
     B, S, H, D = p["B"], p["S"], p["H"], p["D"]
     Hi, Di, r, ov = p["Hi"], p["Di"], p["ratio"], p["overlap"]
     dt = torch_dtype(p)
+    sel = p["K"] > 0 and r > 0
     g = torch.Generator(device=device)
     g.manual_seed(seed)
     x = {}
@@ -104,23 +107,28 @@ def make_layer_inputs(p, device="cpu", seed=0, sink=False, wo_a=False):
         q = (qlat @ wq).view(B, S, H, D)
         x["q"] = _unit_rms(q).to(dt)
         del q, wq
-        wiq = _normal((Q_RANK, Hi * Di), g, device, 0.02)
-        x["iq"] = (qlat @ wiq).view(B, S, Hi, Di).to(dt)
-        del wiq, qlat
+        if sel:
+            wiq = _normal((Q_RANK, Hi * Di), g, device, 0.02)
+            x["iq"] = (qlat @ wiq).view(B, S, Hi, Di).to(dt)
+            del wiq
+        del qlat
     else:
         x["q"] = _unit_rms(_normal((B, S, H, D), g, device)).to(dt)
-        x["iq"] = _unit_rms(_normal((B, S, Hi, Di), g, device)).to(dt)
+        if sel:
+            x["iq"] = _unit_rms(_normal((B, S, Hi, Di), g, device)).to(dt)
     x["kv"] = _unit_rms(_normal((B, S, D), g, device)).to(dt)
-    x["ckv"] = _unit_rms(_normal((B, S, 1 + ov, D), g, device)).to(dt)
-    x["cscore"] = _unit_rms(_normal((B, S, 1 + ov, D), g, device)).to(dt)
-    x["ickv"] = _unit_rms(_normal((B, S, 1 + ov, Di), g, device)).to(dt)
-    x["icscore"] = _unit_rms(_normal((B, S, 1 + ov, Di), g, device)).to(dt)
     G = max(1, (1 + ov) * max(r, 1))
-    x["ape"] = _normal((G, D), g, device, p["ape_std"])
-    x["iape"] = _normal((G, Di), g, device, p["ape_std"])
-    x["w"] = _normal((B, S, Hi), g, device)
-    x["norm_w"] = torch.ones(D, device=device)
-    x["inorm_w"] = torch.ones(Di, device=device)
+    if r > 0:
+        x["ckv"] = _unit_rms(_normal((B, S, 1 + ov, D), g, device)).to(dt)
+        x["cscore"] = _unit_rms(_normal((B, S, 1 + ov, D), g, device)).to(dt)
+        x["ape"] = _normal((G, D), g, device, p["ape_std"])
+        x["norm_w"] = torch.ones(D, device=device)
+    if sel:
+        x["ickv"] = _unit_rms(_normal((B, S, 1 + ov, Di), g, device)).to(dt)
+        x["icscore"] = _unit_rms(_normal((B, S, 1 + ov, Di), g, device)).to(dt)
+        x["iape"] = _normal((G, Di), g, device, p["ape_std"])
+        x["w"] = _normal((B, S, Hi), g, device)
+        x["inorm_w"] = torch.ones(Di, device=device)
     x["sink"] = _normal((H,), g, device) if sink else None
     if wo_a:
         x["wo_a"] = _normal((O_GROUPS, (H // O_GROUPS) * D, O_RANK), g, device, 0.02).to(dt)

@@ -1,0 +1,298 @@
+// Compressor (learned softmax pooling of the shared latent into entries),
+// window-key rotation and indexer query preparation.
+//
+// Compressor: "Enabling DeepSeek-V4-Flash Training on AMD Instinct MI355X
+// GPUs with Primus", section "Three attention types, interleaved" (softmax
+// over the group with a learnable per-position bias; CSA groups overlap) and
+// section "Kernel fusions", row "Compressor pooling" (bias add, softmax over
+// the window of 8 or 128, weighted reduce, all in fp32, one kernel).  Entry
+// RMSNorm and the rotation at r*s follow Primus PR #930 items 1 and 2; the
+// indexer-key Hadamard follows item 6e.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace v4 {
+
+namespace {
+
+constexpr int kCompThreads = 256;
+
+// One block per (entry s, batch b).  Thread tid works on channel vector
+// cv = tid % ncv (8 channels) and member slice ms = tid / ncv; it runs an
+// online softmax over the members m with m % nms == ms.  The nms partial
+// states of a channel are merged in shared memory, then the block finishes
+// the entry: RMSNorm, weight, RoPE at r*s, optional Hadamard, store.
+template <typename T>
+__global__ void __launch_bounds__(kCompThreads)
+compress_kernel(const T* __restrict__ ckv, const T* __restrict__ cscore,
+                const float* __restrict__ ape, const float* __restrict__ norm_w,
+                const float* __restrict__ inv_freq, T* __restrict__ out,
+                int S, int N, int dim, int R, int ratio, int overlap, float eps,
+                int hadamard) {
+  extern __shared__ float sm[];
+  const int ncv = dim / 8;
+  const int nms = kCompThreads / ncv;        // >= 1 because dim <= 2048
+  float* s_m = sm;                           // [nms][dim]
+  float* s_l = s_m + nms * dim;              // [nms][dim]
+  float* s_a = s_l + nms * dim;              // [nms][dim]
+  float* s_e = s_a + nms * dim;              // [dim] finished entry
+  __shared__ float s_red[32];
+
+  const int s = blockIdx.x;
+  const int b = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int cv = tid % ncv;
+  const int ms = tid / ncv;
+  const int P = 1 + overlap;
+  const int G = (overlap && s >= 1) ? 2 * ratio : ratio;  // members present
+  const int first_row = (overlap && s >= 1) ? 0 : overlap * ratio;
+
+  if (ms < nms) {
+    float m[8], l[8], acc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) { m[k] = -INFINITY; l[k] = 0.f; acc[k] = 0.f; }
+    for (int mi = ms; mi < G; mi += nms) {
+      // member mi in chronological order: ape row first_row + mi
+      const int row = first_row + mi;
+      int tok, half;
+      if (overlap && row < ratio) { tok = ratio * (s - 1) + row; half = 1; }
+      else { tok = ratio * s + (row - overlap * ratio); half = 0; }
+      const size_t off = (((size_t)b * S + tok) * P + half) * dim + cv * 8;
+      float sc[8], x[8], a[8];
+      load8(cscore + off, sc);
+      load8(ckv + off, x);
+      load8(ape + (size_t)row * dim + cv * 8, a);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float lam = sc[k] + a[k];
+        if (lam > m[k]) {
+          float f = expf(m[k] - lam);
+          l[k] = l[k] * f + 1.f;
+          acc[k] = acc[k] * f + x[k];
+          m[k] = lam;
+        } else {
+          float e = expf(lam - m[k]);
+          l[k] += e;
+          acc[k] += e * x[k];
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      s_m[ms * dim + cv * 8 + k] = m[k];
+      s_l[ms * dim + cv * 8 + k] = l[k];
+      s_a[ms * dim + cv * 8 + k] = acc[k];
+    }
+  }
+  __syncthreads();
+
+  // merge the member slices, accumulate the sum of squares
+  float ss = 0.f;
+  for (int c = tid; c < dim; c += kCompThreads) {
+    float mm = -INFINITY;
+    for (int j = 0; j < nms; ++j) mm = fmaxf(mm, s_m[j * dim + c]);
+    float ll = 0.f, aa = 0.f;
+    for (int j = 0; j < nms; ++j) {
+      float mj = s_m[j * dim + c];
+      if (mj == -INFINITY) continue;
+      float f = expf(mj - mm);
+      ll += s_l[j * dim + c] * f;
+      aa += s_a[j * dim + c] * f;
+    }
+    float v = aa / ll;
+    s_e[c] = v;
+    ss += v * v;
+  }
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((tid & 31) == 0) s_red[tid >> 5] = ss;
+  __syncthreads();
+  if (tid < 32) {
+    float v = tid < kCompThreads / 32 ? s_red[tid] : 0.f;
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (tid == 0) s_red[0] = v;
+  }
+  __syncthreads();
+  const float rinv = 1.0f / sqrtf(s_red[0] / (float)dim + eps);
+  for (int c = tid; c < dim; c += kCompThreads)
+    s_e[c] = s_e[c] * rinv * (norm_w ? norm_w[c] : 1.f);
+  __syncthreads();
+  // RoPE on interleaved pairs of the last R channels, position r*s
+  const long long pos = (long long)ratio * s;
+  for (int j = tid; j < R / 2; j += kCompThreads) {
+    float cs, sn;
+    rope_cos_sin(pos, inv_freq[j], &cs, &sn);
+    const int c0 = dim - R + 2 * j;
+    float a = s_e[c0], bb = s_e[c0 + 1];
+    rot_pair(a, bb, cs, sn);
+    s_e[c0] = a;
+    s_e[c0 + 1] = bb;
+  }
+  __syncthreads();
+  if (hadamard) {
+    for (int h = 1; h < dim; h <<= 1) {
+      for (int i = tid; i < dim / 2; i += kCompThreads) {
+        const int lo = (i / h) * 2 * h + (i % h);
+        float a = s_e[lo], bb = s_e[lo + h];
+        s_e[lo] = a + bb;
+        s_e[lo + h] = a - bb;
+      }
+      __syncthreads();
+    }
+    const float hs = 1.0f / sqrtf((float)dim);
+    for (int c = tid; c < dim; c += kCompThreads) s_e[c] *= hs;
+    __syncthreads();
+  }
+  T* dst = out + ((size_t)b * N + s) * dim;
+  for (int c8 = tid; c8 < ncv; c8 += kCompThreads) store8(dst + c8 * 8, s_e + c8 * 8);
+}
+
+// Rotate every row of kv [rows, D] at its own position u = row % S (last R
+// dims), writing the storage dtype.  One thread per 8-element vector.
+template <typename T>
+__global__ void rotate_rows_kernel(const T* __restrict__ x, const float* __restrict__ inv_freq,
+                                   T* __restrict__ y, long long rows, int S, int D, int R) {
+  const int nv = D / 8;
+  const long long total = rows * nv;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long row = i / nv;
+    const int v = (int)(i % nv);
+    float e[8];
+    load8(x + row * D + v * 8, e);
+    const int c0 = v * 8;
+    if (c0 >= D - R) {
+      const long long u = row % S;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float cs, sn;
+        rope_cos_sin(u, inv_freq[(c0 - (D - R)) / 2 + k], &cs, &sn);
+        rot_pair(e[2 * k], e[2 * k + 1], cs, sn);
+      }
+    }
+    store8(y + row * D + v * 8, e);
+  }
+}
+
+// Indexer query prep: rows of Di elements (row = (b,t,h)), RoPE at t on the
+// last R dims, then the normalised Hadamard via butterflies: stages 1,2,4
+// inside a thread's 8 elements, larger stages across the Di/8 lanes of the
+// row with warp shuffles.  Requires Di/8 <= 32.
+template <typename T>
+__global__ void indexer_prep_kernel(const T* __restrict__ iq, const float* __restrict__ inv_freq,
+                                    T* __restrict__ out, long long rows, int S, int Hi, int Di,
+                                    int R) {
+  const int lanes = Di / 8;                                  // lanes per row (power of 2)
+  const long long gt = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const long long row = gt / lanes;
+  const int lane = (int)(gt % lanes);
+  const bool live = row < rows;
+  float e[8];
+  if (live) load8(iq + row * Di + lane * 8, e);
+  else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) e[k] = 0.f;
+  }
+  const int c0 = lane * 8;
+  if (live && c0 >= Di - R) {
+    const long long t = (row / Hi) % S;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float cs, sn;
+      rope_cos_sin(t, inv_freq[(c0 - (Di - R)) / 2 + k], &cs, &sn);
+      rot_pair(e[2 * k], e[2 * k + 1], cs, sn);
+    }
+  }
+  // in-thread butterflies (h = 1, 2, 4)
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if ((k & h) == 0) {
+        float a = e[k], b = e[k + h];
+        e[k] = a + b;
+        e[k + h] = a - b;
+      }
+    }
+  }
+  // cross-lane butterflies (h = 8 .. Di/2)
+  for (int hl = 1; hl < lanes; hl <<= 1) {
+    const bool upper = (lane & hl) != 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      float other = __shfl_xor_sync(0xffffffffu, e[k], hl);
+      e[k] = upper ? (other - e[k]) : (e[k] + other);
+    }
+  }
+  const float hs = 1.0f / sqrtf((float)Di);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) e[k] *= hs;
+  if (live) store8(out + row * Di + lane * 8, e);
+}
+
+template <typename T>
+cudaError_t compress_t(const v4_config& c, const void* ckv, const void* cscore, const float* ape,
+                       const float* norm_w, const float* inv_freq, int dim, int hadamard,
+                       void* out, cudaStream_t st) {
+  const int N = c.seqlen / c.ratio;
+  if (N == 0) return cudaSuccess;
+  const int ncv = dim / 8;
+  const int nms = kCompThreads / ncv;
+  const size_t smem = (size_t)(3 * nms * dim + dim) * sizeof(float);
+  auto kern = compress_kernel<T>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(N, c.batch);
+  kern<<<grid, kCompThreads, smem, st>>>((const T*)ckv, (const T*)cscore, ape, norm_w, inv_freq,
+                                         (T*)out, c.seqlen, N, dim, c.rope_dim, c.ratio,
+                                         c.overlap, c.rms_eps, hadamard);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_compress(const v4_config& c, const void* ckv, const void* cscore,
+                            const float* ape, const float* norm_w, const float* inv_freq,
+                            int dim, int hadamard, void* out, cudaStream_t st) {
+  if (c.dtype == V4_BF16)
+    return compress_t<bf16>(c, ckv, cscore, ape, norm_w, inv_freq, dim, hadamard, out, st);
+  return compress_t<float>(c, ckv, cscore, ape, norm_w, inv_freq, dim, hadamard, out, st);
+}
+
+cudaError_t launch_rotate_rows(const v4_config& c, const void* kv, const float* inv_freq,
+                               void* kv_rot, cudaStream_t st) {
+  const long long rows = (long long)c.batch * c.seqlen;
+  const long long total = rows * (c.head_dim / 8);
+  const int threads = 256;
+  long long blocks = (total + threads - 1) / threads;
+  if (blocks > 152LL * 16) blocks = 152LL * 16;
+  if (c.dtype == V4_BF16)
+    rotate_rows_kernel<bf16><<<(int)blocks, threads, 0, st>>>(
+        (const bf16*)kv, inv_freq, (bf16*)kv_rot, rows, c.seqlen, c.head_dim, c.rope_dim);
+  else
+    rotate_rows_kernel<float><<<(int)blocks, threads, 0, st>>>(
+        (const float*)kv, inv_freq, (float*)kv_rot, rows, c.seqlen, c.head_dim, c.rope_dim);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_indexer_prep(const v4_config& c, const void* iq, const float* inv_freq,
+                                void* iqp, cudaStream_t st) {
+  const long long rows = (long long)c.batch * c.seqlen * c.idx_heads;
+  const int lanes = c.idx_dim / 8;
+  const int threads = 256;
+  const long long blocks = (rows * lanes + threads - 1) / threads;
+  if (c.dtype == V4_BF16)
+    indexer_prep_kernel<bf16><<<(unsigned)blocks, threads, 0, st>>>(
+        (const bf16*)iq, inv_freq, (bf16*)iqp, rows, c.seqlen, c.idx_heads, c.idx_dim, c.rope_dim);
+  else
+    indexer_prep_kernel<float><<<(unsigned)blocks, threads, 0, st>>>(
+        (const float*)iq, inv_freq, (float*)iqp, rows, c.seqlen, c.idx_heads, c.idx_dim,
+        c.rope_dim);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace v4

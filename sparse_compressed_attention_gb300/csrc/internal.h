@@ -1,0 +1,50 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+// Every launcher enqueues on `stream` and returns the launch error (if any).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/v4attn.h"
+
+namespace v4 {
+
+// Counts kernel launches made by the library (reported by v4_launch_count).
+void note_launch(int n = 1);
+
+// Workspace carve-up for one configuration.  Offsets are 256-byte aligned.
+struct Workspace {
+  size_t kv_rot = 0, kv_rot_bytes = 0;     // rotated window keys [B,S,D]
+  size_t ent = 0, ent_bytes = 0;           // entries [B,N,D] (layer call)
+  size_t ikey = 0, ikey_bytes = 0;         // indexer keys [B,N,Di] (layer call)
+  size_t iqp = 0, iqp_bytes = 0;           // prepared indexer queries [B,S,Hi,Di]
+  size_t scores = 0, scores_bytes = 0;     // indexer scores [B,S,N] fp32
+  size_t idx = 0, idx_bytes = 0;           // selected entries [B,S,K] (layer call)
+  size_t knorm = 0, knorm_bytes = 0;       // key-row norms (tensor-core attention)
+  size_t total = 0;
+};
+Workspace plan_workspace(const v4_config& c);
+
+// ---- compressor and preparation kernels (compress.cu)
+cudaError_t launch_compress(const v4_config& c, const void* ckv, const void* cscore,
+                            const float* ape, const float* norm_w, const float* inv_freq,
+                            int dim, int hadamard, void* out, cudaStream_t st);
+cudaError_t launch_rotate_rows(const v4_config& c, const void* kv, const float* inv_freq,
+                               void* kv_rot, cudaStream_t st);
+cudaError_t launch_indexer_prep(const v4_config& c, const void* iq, const float* inv_freq,
+                                void* iqp, cudaStream_t st);
+
+// ---- indexer (indexer.cu)
+cudaError_t launch_indexer_scores_simt(const v4_config& c, const void* iqp, const void* ikey,
+                                       const float* w, float* scores, cudaStream_t st);
+cudaError_t launch_topk(const v4_config& c, const float* scores, int32_t* idx, float* iscore,
+                        cudaStream_t st);
+
+// ---- attention (mqa.cu)
+cudaError_t launch_mqa_simt(const v4_config& c, const void* q, const void* kv_rot,
+                            const void* ent, const int32_t* idx, const float* sink,
+                            const float* inv_freq, void* o, float* lse, int* status,
+                            cudaStream_t st);
+
+}  // namespace v4
