@@ -25,17 +25,29 @@ def rel_l2(a, b):
     return float(np.linalg.norm(a - b) / (den if den > 0 else 1.0))
 
 
-def assert_within_bf16_ulp(gpu, ref, ulps=1, frac_exact_min=None):
-    """Every element within `ulps` bf16 ulps of the oracle's bf16-rounded value."""
-    g = np64(gpu).ravel()
-    r = np.asarray(ref, dtype=np.float64).ravel()
+def assert_within_bf16_ulp(gpu, ref, ulps=1, frac_exact_min=None, row_terms=None):
+    """Every element within `ulps` bf16 ulps of the oracle's bf16-rounded value,
+    plus the fp32 forward-error allowance of the kernel's arithmetic.
+
+    The kernels compute in fp32 and round once to bf16.  An output that comes
+    out of a cancelling sum (the Hadamard, a rotation) carries an absolute fp32
+    error proportional to the magnitude of the row, not of the result, so
+    each element also gets row_terms * 2^-24 * max|row| (row = last axis).
+    """
+    g = np64(gpu)
+    r = np.asarray(ref, dtype=np.float64)
     m, e = np.frexp(np.abs(r))
     ulp = np.ldexp(1.0, e - 8)
     ulp = np.where(r == 0, 2.0 ** -133, ulp)
-    bad = np.abs(g - r) > ulps * ulp + 1e-30
-    assert not bad.any(), "%d of %d elements beyond %d bf16 ulp; worst at %d: gpu %r oracle %r" % (
-        bad.sum(), bad.size, ulps, int(np.argmax(np.abs(g - r) / ulp)), g[np.argmax(np.abs(g - r) / ulp)],
-        r[np.argmax(np.abs(g - r) / ulp)])
+    allow = ulps * ulp + 1e-30
+    if row_terms is not None:
+        allow = allow + row_terms * U32 * np.abs(r).max(axis=-1, keepdims=True)
+    err = np.abs(g - r)
+    bad = err > allow
+    if bad.any():
+        k = int(np.argmax((err / allow).ravel()))
+        raise AssertionError("%d of %d elements beyond tolerance; worst: gpu %r oracle %r allow %r" % (
+            bad.sum(), bad.size, g.ravel()[k], r.ravel()[k], allow.ravel()[k]))
     if frac_exact_min is not None:
         assert np.mean(g == r) >= frac_exact_min
 

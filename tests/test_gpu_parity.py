@@ -77,7 +77,8 @@ def test_compress(name, case, which):
     ref = O.compress(np64(x[src[0]]), np64(x[src[1]]), np64(x[src[2]]), np64(x[src[3]]), f,
                      p["ratio"], p["overlap"], 1e-6, hadamard=bool(had), store_bf16=bf)
     if bf:
-        assert_within_bf16_ulp(out, ref, ulps=1, frac_exact_min=0.99)
+        # allowance: Hadamard (log2 dim stages) and RMSNorm/rotation rounding
+        assert_within_bf16_ulp(out, ref, ulps=1, frac_exact_min=0.99, row_terms=4 * math.log2(dim) + 16)
     else:
         assert rel_l2(np64(out), ref) < FP32_TOL
 
@@ -94,7 +95,8 @@ def test_indexer_prep(name, p):
     torch.cuda.synchronize()
     ref = O.indexer_query_prep(np64(x["iq"]), f, store_bf16=p["dtype"] == "bf16")
     if p["dtype"] == "bf16":
-        assert_within_bf16_ulp(out, ref, ulps=1, frac_exact_min=0.99)
+        assert_within_bf16_ulp(out, ref, ulps=1, frac_exact_min=0.99,
+                               row_terms=4 * math.log2(p["Di"]) + 16)
     else:
         assert rel_l2(np64(out), ref) < FP32_TOL
 
