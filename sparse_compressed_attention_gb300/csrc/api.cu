@@ -120,6 +120,7 @@ Workspace plan_workspace(const v4_config& c) {
   take(w.scores, w.scores_bytes, sel ? B * S * N * 4 : 0);
   take(w.idx, w.idx_bytes, sel ? B * S * c.topk * 4 : 0);
   take(w.knorm, w.knorm_bytes, (B * S + B * N) * 4);
+  take(w.counters, w.counters_bytes, (2 + B * S) * 4);
   w.total = off;
   return w;
 }
@@ -212,6 +213,10 @@ static v4_status do_indexer(const v4_config& c, const void* iq, int prepared, co
   return V4_OK;
 }
 
+static bool use_tc_attention(const v4_config& c) {
+  return c.path != V4_PATH_SIMT && mqa_tc_supported(c);
+}
+
 static v4_status do_mqa(const v4_config& c, const void* q, const void* kv, const void* ent,
                         const int32_t* idx, const float* sink, const float* f, void* o,
                         float* lse, char* ws, cudaStream_t st) {
@@ -219,13 +224,33 @@ static v4_status do_mqa(const v4_config& c, const void* q, const void* kv, const
   int* status = status_ptr();
   if (!status) return fail(V4_ERR_CUDA, "device status word unavailable");
   void* kv_rot = ws + plan.kv_rot;
+  float* kv_norm = (float*)(ws + plan.knorm);
+  float* ent_norm = kv_norm + (size_t)c.batch * c.seqlen;
+  const bool tc = use_tc_attention(c);
   {
     ProfScope ps(K_ROTATE, st);
-    CU(launch_rotate_rows(c, kv, f, kv_rot, st), "window-key rotation kernel");
+    if (tc) {
+      CU(launch_key_prep(c, kv, ent, f, kv_rot, kv_norm, ent_norm, st), "key prep kernel");
+    } else {
+      CU(launch_rotate_rows(c, kv, f, kv_rot, st), "window-key rotation kernel");
+    }
+  }
+  if (tc) {
+    int* counters = (int*)(ws + plan.counters);
+    {
+      ProfScope ps(K_ATTN, st);
+      CU(launch_mqa_tc(c, q, kv_rot, ent, idx, sink, f, kv_norm, ent_norm, o, lse, counters, status, st),
+         "tensor-core attention kernel");
+    }
+    // queries whose bound-shifted softmax kept too little mass are recomputed
+    // with the running-max kernel (normally none)
+    CU(launch_mqa_simt(c, q, kv_rot, ent, idx, sink, f, o, lse, status, counters + 1, st),
+       "attention fix-up kernel");
+    return V4_OK;
   }
   {
     ProfScope ps(K_ATTN, st);
-    CU(launch_mqa_simt(c, q, kv_rot, ent, idx, sink, f, o, lse, status, st), "attention kernel");
+    CU(launch_mqa_simt(c, q, kv_rot, ent, idx, sink, f, o, lse, status, nullptr, st), "attention kernel");
   }
   return V4_OK;
 }
@@ -328,7 +353,8 @@ v4_status v4_sparse_mqa_fwd(const v4_config* cfg, const void* q, const void* kv,
   OPT(sink, "sink");
   OPT(lse, "lse");
   if (cfg->rope_dim > 0) REQ(inv_freq, "inv_freq");
-  if (cfg->path == V4_PATH_TC) return fail(V4_ERR_UNSUPPORTED, "tensor-core attention path not built");
+  if (cfg->path == V4_PATH_TC && !mqa_tc_supported(*cfg))
+    return fail(V4_ERR_UNSUPPORTED, "tensor-core attention needs bf16, H=64, D=512, R=64, 1 <= W <= 128, K <= 512");
   s = check_ws(*cfg, workspace, ws_bytes);
   if (s != V4_OK) return s;
   return do_mqa(*cfg, q, kv, ent, cfg->topk > 0 ? idx : nullptr, sink, inv_freq, o, lse,
@@ -378,7 +404,8 @@ v4_status v4_attn_layer_fwd(const v4_config* cfg, const v4_layer_inputs* in, v4_
     }
   }
   if (in->wo_a) return fail(V4_ERR_UNSUPPORTED, "grouped output projection not built yet");
-  if (c.path == V4_PATH_TC) return fail(V4_ERR_UNSUPPORTED, "tensor-core attention path not built");
+  if (c.path == V4_PATH_TC && !mqa_tc_supported(c))
+    return fail(V4_ERR_UNSUPPORTED, "tensor-core attention needs bf16, H=64, D=512, R=64, 1 <= W <= 128, K <= 512");
   s = check_ws(c, workspace, ws_bytes);
   if (s != V4_OK) return s;
   char* ws = (char*)workspace;

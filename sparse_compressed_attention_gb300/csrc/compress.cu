@@ -175,6 +175,50 @@ __global__ void rotate_rows_kernel(const T* __restrict__ x, const float* __restr
   }
 }
 
+// Key prep: one warp per stored key row.  Rows [0, B*S) are window tokens:
+// rotated at their position u (last R dims), stored in the storage dtype,
+// and their norm taken from the stored (rounded) values.  Rows
+// [B*S, B*S + B*N) are entries (already rotated): only their norm.
+template <typename T>
+__global__ void key_prep_kernel(const T* __restrict__ kv, const T* __restrict__ ent,
+                                const float* __restrict__ inv_freq, T* __restrict__ kv_rot,
+                                float* __restrict__ kv_norm, float* __restrict__ ent_norm,
+                                long long kv_rows, long long ent_rows, int S, int D, int R) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long row = blockIdx.x * (long long)(blockDim.x >> 5) + (threadIdx.x >> 5);
+       row < kv_rows + ent_rows; row += warps) {
+    const bool is_kv = row < kv_rows;
+    const T* src = is_kv ? kv + row * D : ent + (row - kv_rows) * D;
+    float ss = 0.f;
+    for (int v = lane; v < D / 8; v += 32) {
+      float e[8];
+      load8(src + v * 8, e);
+      const int c0 = v * 8;
+      if (is_kv) {
+        if (c0 >= D - R) {
+          const long long u = row % S;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float cs, sn;
+            rope_cos_sin(u, inv_freq[(c0 - (D - R)) / 2 + k], &cs, &sn);
+            rot_pair(e[2 * k], e[2 * k + 1], cs, sn);
+          }
+        }
+        store8(kv_rot + row * D + c0, e);
+        load8(kv_rot + row * D + c0, e);         // norm of the stored values
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ss = fmaf(e[k], e[k], ss);
+    }
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) {
+      if (is_kv) kv_norm[row] = sqrtf(ss);
+      else ent_norm[row - kv_rows] = sqrtf(ss);
+    }
+  }
+}
+
 // Indexer query prep: rows of Di elements (row = (b,t,h)), RoPE at t on the
 // last R dims, then the normalised Hadamard via butterflies: stages 1,2,4
 // inside a thread's 8 elements, larger stages across the Di/8 lanes of the
@@ -274,6 +318,27 @@ cudaError_t launch_rotate_rows(const v4_config& c, const void* kv, const float* 
   else
     rotate_rows_kernel<float><<<(int)blocks, threads, 0, st>>>(
         (const float*)kv, inv_freq, (float*)kv_rot, rows, c.seqlen, c.head_dim, c.rope_dim);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_key_prep(const v4_config& c, const void* kv, const void* ent, const float* inv_freq,
+                            void* kv_rot, float* kv_norm, float* ent_norm, cudaStream_t st) {
+  const long long kv_rows = (long long)c.batch * c.seqlen;
+  const int N = c.ratio > 0 ? c.seqlen / c.ratio : 0;
+  const long long ent_rows = ent != nullptr ? (long long)c.batch * N : 0;
+  const int threads = 256;
+  long long blocks = (kv_rows + ent_rows + 7) / 8;
+  if (blocks > 152LL * 16) blocks = 152LL * 16;
+  if (blocks < 1) blocks = 1;
+  if (c.dtype == V4_BF16)
+    key_prep_kernel<bf16><<<(int)blocks, threads, 0, st>>>((const bf16*)kv, (const bf16*)ent, inv_freq,
+                                                            (bf16*)kv_rot, kv_norm, ent_norm, kv_rows,
+                                                            ent_rows, c.seqlen, c.head_dim, c.rope_dim);
+  else
+    key_prep_kernel<float><<<(int)blocks, threads, 0, st>>>((const float*)kv, (const float*)ent, inv_freq,
+                                                             (float*)kv_rot, kv_norm, ent_norm, kv_rows,
+                                                             ent_rows, c.seqlen, c.head_dim, c.rope_dim);
   note_launch();
   return cudaGetLastError();
 }

@@ -2,6 +2,7 @@
 // Every launcher enqueues on `stream` and returns the launch error (if any).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -21,7 +22,8 @@ struct Workspace {
   size_t iqp = 0, iqp_bytes = 0;           // prepared indexer queries [B,S,Hi,Di]
   size_t scores = 0, scores_bytes = 0;     // indexer scores [B,S,N] fp32
   size_t idx = 0, idx_bytes = 0;           // selected entries [B,S,K] (layer call)
-  size_t knorm = 0, knorm_bytes = 0;       // key-row norms (tensor-core attention)
+  size_t knorm = 0, knorm_bytes = 0;       // key-row norms [B*S + B*N] (tensor-core attention)
+  size_t counters = 0, counters_bytes = 0; // work counter, redo count, redo list [2 + B*S]
   size_t total = 0;
 };
 Workspace plan_workspace(const v4_config& c);
@@ -32,6 +34,14 @@ cudaError_t launch_compress(const v4_config& c, const void* ckv, const void* csc
                             int dim, int hadamard, void* out, cudaStream_t st);
 cudaError_t launch_rotate_rows(const v4_config& c, const void* kv, const float* inv_freq,
                                void* kv_rot, cudaStream_t st);
+// Rotated window keys plus the Euclidean norm of every stored key row
+// (window rows then entry rows), as the tensor-core attention needs them.
+cudaError_t launch_key_prep(const v4_config& c, const void* kv, const void* ent, const float* inv_freq,
+                            void* kv_rot, float* kv_norm, float* ent_norm, cudaStream_t st);
+
+// ---- TMA descriptors (tma_host.cu); returns 0 on success
+int make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                      uint32_t box_rows, bool swizzle128);
 cudaError_t launch_indexer_prep(const v4_config& c, const void* iq, const float* inv_freq,
                                 void* iqp, cudaStream_t st);
 
@@ -42,9 +52,16 @@ cudaError_t launch_topk(const v4_config& c, const float* scores, int32_t* idx, f
                         cudaStream_t st);
 
 // ---- attention (mqa.cu)
+// `list` (nullable): list[0] = number of queries, list[1..] = b*S + t of each;
+// when given, only those queries are computed.
 cudaError_t launch_mqa_simt(const v4_config& c, const void* q, const void* kv_rot,
                             const void* ent, const int32_t* idx, const float* sink,
                             const float* inv_freq, void* o, float* lse, int* status,
-                            cudaStream_t st);
+                            const int* list, cudaStream_t st);
+bool mqa_tc_supported(const v4_config& c);
+cudaError_t launch_mqa_tc(const v4_config& c, const void* q, const void* kv_rot, const void* ent,
+                          const int32_t* idx, const float* sink, const float* inv_freq,
+                          const float* kv_norm, const float* ent_norm, void* o, float* lse,
+                          int* counters, int* status, cudaStream_t st);
 
 }  // namespace v4

@@ -36,8 +36,8 @@ __global__ void __launch_bounds__(kMqaThreads)
 mqa_simt_kernel(const T* __restrict__ q, const T* __restrict__ kv_rot, const T* __restrict__ ent,
                 const int32_t* __restrict__ idx, const float* __restrict__ sink,
                 const float* __restrict__ inv_freq, T* __restrict__ o, float* __restrict__ lse,
-                int* __restrict__ status, int S, int H, int D, int R, int N, int ratio,
-                int window, int K, float scale) {
+                int* __restrict__ status, const int* __restrict__ list, int S, int H, int D, int R,
+                int N, int ratio, int window, int K, float scale) {
   extern __shared__ float sm[];
   const int ldk = D + 1;                      // padded key rows: conflict-free columns
   float* s_q = sm;                            // [kHG][D] rotated query rows
@@ -46,12 +46,25 @@ mqa_simt_kernel(const T* __restrict__ q, const T* __restrict__ kv_rot, const T* 
   __shared__ const T* s_ptr[kKT];
   __shared__ float s_cs[2][512];
 
-  const int t = blockIdx.x;
   const int h0 = blockIdx.y * kHG;
-  const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = h0 + warp;
   const bool head_live = h < H;
+  // without a list: query t = blockIdx.x of batch blockIdx.z; with a list:
+  // the listed queries, strided over blockIdx.x
+  for (int item = blockIdx.x;; item += gridDim.x) {
+  int t, b;
+  if (list != nullptr) {
+    if (item >= list[0]) break;
+    const int bt = list[1 + item];
+    b = bt / S;
+    t = bt % S;
+  } else {
+    if (item >= S) break;
+    t = item;
+    b = blockIdx.z;
+  }
+  __syncthreads();
 
   // RoPE angles of position t (shared by all heads)
   for (int j = threadIdx.x; j < R / 2; j += kMqaThreads) {
@@ -158,7 +171,7 @@ mqa_simt_kernel(const T* __restrict__ q, const T* __restrict__ kv_rot, const T* 
     }
   }
 
-  if (!head_live) return;
+  if (head_live) {
   const float inv_l = l > 0.f ? 1.f / l : 0.f;
   T* orow = o + (((size_t)b * S + t) * H + h) * D;
 #pragma unroll
@@ -177,12 +190,14 @@ mqa_simt_kernel(const T* __restrict__ q, const T* __restrict__ kv_rot, const T* 
     }
   }
   if (lse && lane == 0) lse[((size_t)b * S + t) * H + h] = l > 0.f ? m + logf(l) : -INFINITY;
+  }
+  }
 }
 
 template <typename T>
 cudaError_t mqa_t(const v4_config& c, const void* q, const void* kv_rot, const void* ent,
                   const int32_t* idx, const float* sink, const float* inv_freq, void* o,
-                  float* lse, int* status, cudaStream_t st) {
+                  float* lse, int* status, const int* list, cudaStream_t st) {
   const int D = c.head_dim;
   const size_t smem = (size_t)(kHG * D + kKT * (D + 1) + kHG * kKT) * sizeof(float);
   auto kern = mqa_simt_kernel<T>;
@@ -191,8 +206,9 @@ cudaError_t mqa_t(const v4_config& c, const void* q, const void* kv_rot, const v
   const int N = c.ratio > 0 ? c.seqlen / c.ratio : 0;
   const float scale = c.softmax_scale > 0.f ? c.softmax_scale : 1.0f / sqrtf((float)D);
   dim3 grid(c.seqlen, (c.n_heads + kHG - 1) / kHG, c.batch);
+  if (list != nullptr) grid = dim3(256, (c.n_heads + kHG - 1) / kHG, 1);
   kern<<<grid, kMqaThreads, smem, st>>>((const T*)q, (const T*)kv_rot, (const T*)ent, idx, sink,
-                                        inv_freq, (T*)o, lse, status, c.seqlen, c.n_heads, D,
+                                        inv_freq, (T*)o, lse, status, list, c.seqlen, c.n_heads, D,
                                         c.rope_dim, N, c.ratio, c.window, c.topk, scale);
   note_launch();
   return cudaGetLastError();
@@ -203,10 +219,10 @@ cudaError_t mqa_t(const v4_config& c, const void* q, const void* kv_rot, const v
 cudaError_t launch_mqa_simt(const v4_config& c, const void* q, const void* kv_rot,
                             const void* ent, const int32_t* idx, const float* sink,
                             const float* inv_freq, void* o, float* lse, int* status,
-                            cudaStream_t st) {
+                            const int* list, cudaStream_t st) {
   if (c.dtype == V4_BF16)
-    return mqa_t<bf16>(c, q, kv_rot, ent, idx, sink, inv_freq, o, lse, status, st);
-  return mqa_t<float>(c, q, kv_rot, ent, idx, sink, inv_freq, o, lse, status, st);
+    return mqa_t<bf16>(c, q, kv_rot, ent, idx, sink, inv_freq, o, lse, status, list, st);
+  return mqa_t<float>(c, q, kv_rot, ent, idx, sink, inv_freq, o, lse, status, list, st);
 }
 
 }  // namespace v4

@@ -1,0 +1,545 @@
+// Sparse / dense multi-query attention on the 5th-generation tensor cores
+// (tcgen05, TMEM accumulators, TMA) for the DeepSeek-V4-Flash shapes:
+// 64 query heads sharing one 512-d latent that is both key and value, the
+// last 64 dims rotated, bf16 storage, window <= 128.
+//
+// Method: "Enabling DeepSeek-V4-Flash Training on AMD Instinct MI355X GPUs
+// with Primus", sections "The DeepSeek-V4-Flash architecture", "Three
+// attention types, interleaved" and "Kernel fusions" (row "SWA / CSA / HCA
+// attention": in-kernel gather of the selected entries, window branch and
+// sink in one softmax); Primus PR #930 item 1 (scale D^-1/2) and item 3
+// (output de-rotated at -t).  The page's "fixed max via shift invariance"
+// idea (section "Attention kernels for the three layer types") is used with
+// a provable bound: m_h = scale * |q_h| * max_k |k| >= every logit, so the
+// softmax needs no running max and no rescaling; partial sums simply add.
+//
+// Layout per query t (one CTA, persistent over queries):
+//   S^T[key, head] = K_tile[128 keys x 512] . Q^T          (M=128 keys, N=64)
+//   P^T = exp(S^T * scale - m) in bf16 (one thread per key row)
+//   O^T[dim, head] += K_tile^T[512 x 128 keys] . P^T     (4 x M=128 dims, N=64)
+// The key tile in shared memory (8 K-blocks of [128 keys x 64 dims], 128-byte
+// swizzle) is the K-major A operand of the first product and, read as
+// MN-major, the A operand of the second.  TMEM: S^T double buffer (2 x 64
+// columns) and O^T (256 columns).
+//
+// Warp roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer (and TMEM
+// owner), warps 2-5 softmax + epilogue (one TMEM lane quarter each).
+#include <cuda.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sm100.cuh"
+
+namespace v4 {
+
+using namespace sm100;
+
+namespace {
+
+constexpr int kH = 64, kD = 512, kR = 64;
+constexpr int kThreads = 192;
+constexpr int kTileKeys = 128;
+constexpr int kSlots = 8;                         // one tile: 8 K-blocks of 64 dims
+constexpr uint32_t kSlotBytes = 128 * 128;        // 128 keys x 64 dims x 2 B
+constexpr uint32_t kQBlockBytes = 64 * 128;       // 64 heads x 64 dims x 2 B
+constexpr uint32_t kPBytes = 128 * 64 * 2;        // 128 keys x 64 heads x 2 B
+constexpr int kMaxSel = 512;
+
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_SLOT = OFF_Q + 8 * kQBlockBytes;           // 65536
+constexpr uint32_t OFF_P = OFF_SLOT + kSlots * kSlotBytes;        // 196608
+constexpr uint32_t OFF_LIST = OFF_P + 2 * kPBytes;                // 229376
+constexpr uint32_t OFF_CTL = OFF_LIST + kMaxSel * 4;              // 231424
+
+struct QInfo {
+  int b, t, n_ent, ent_tiles, tiles, w_lo, done;
+  float kmax;
+};
+
+struct Ctl {
+  uint64_t full[kSlots], empty[kSlots];
+  uint64_t q_full, q_ready, q_empty;
+  uint64_t s_full[2], p_ready[2];
+  uint64_t o_full, o_empty;
+  uint64_t info_full[2], info_empty[2];
+  uint64_t fin;
+  QInfo info[2];
+  float mlog2[kH];
+  float inv_l[kH];
+  uint32_t tmem_base;
+  int abort;
+  int decision;
+  int redo;
+};
+
+constexpr uint32_t kSmemBytes = OFF_CTL + sizeof(Ctl);
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct Params {
+  const int32_t* idx;          // [B,S,K] or null
+  const float* sink;           // [64] or null
+  const float* inv_freq;       // [32]
+  const float* kv_norm;        // [B*S]
+  const float* ent_norm;       // [B*N]
+  float* lse;                  // [B,S,64] or null
+  int* status;
+  int* counters;               // [0] work item, [1] redo count, [2..] redo list
+  int B, S, N, ratio, window, K;
+  float scale;
+};
+
+__device__ __forceinline__ bool wait_ok(uint64_t* bar, uint32_t parity, Ctl* c, int* status) {
+  return mbar_wait(bar, parity, &c->abort, status);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
+              const __grid_constant__ CUtensorMap map_ent, const __grid_constant__ CUtensorMap map_ent_g,
+              const __grid_constant__ CUtensorMap map_o, const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Ctl* c = reinterpret_cast<Ctl*>(smem + OFF_CTL);
+  int* list = reinterpret_cast<int*>(smem + OFF_LIST);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if ((smem_u32(smem) & 1023u) != 0) {          // swizzled operands need 1 KB alignment
+    if (threadIdx.x == 0) set_status(p.status, V4_ERR_UNSUPPORTED);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kSlots; ++i) { mbar_init(&c->full[i], 1); mbar_init(&c->empty[i], 1); }
+    mbar_init(&c->q_full, 1);
+    mbar_init(&c->q_ready, 128);
+    mbar_init(&c->q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&c->s_full[i], 1);
+      mbar_init(&c->p_ready[i], 128);
+      mbar_init(&c->info_full[i], 1);
+      mbar_init(&c->info_empty[i], 129);
+    }
+    mbar_init(&c->o_full, 1);
+    mbar_init(&c->o_empty, 128);
+    mbar_init(&c->fin, 1);
+    c->abort = 0;
+    c->redo = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&map_q);
+    prefetch_tmap(&map_kv);
+    prefetch_tmap(&map_ent);
+    prefetch_tmap(&map_ent_g);
+    prefetch_tmap(&map_o);
+  }
+  if (warp == 1) {
+    tmem_alloc(&c->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = c->tmem_base;
+  const int total = p.B * p.S;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int qc = 0, g = 0;
+    while (true) {
+      int item = 0;
+      if (lane == 0) item = atomicAdd(&p.counters[0], 1);
+      item = __shfl_sync(0xffffffffu, item, 0);
+      QInfo inf;
+      inf.done = item >= total ? 1 : 0;
+      int b = 0, t = 0;
+      if (!inf.done) {
+        b = item % p.B;
+        t = p.S - 1 - item / p.B;
+      }
+      inf.b = b;
+      inf.t = t;
+      float kmax = 0.f;
+      int n_ent = 0;
+      if (!inf.done) {
+        const int nv = p.ratio > 0 ? min((t + 1) / p.ratio, p.N) : 0;
+        if (p.ratio > 0 && p.idx != nullptr) {
+          // compact the valid selected entries into the list (order is free)
+          const int32_t* row = p.idx + ((size_t)b * p.S + t) * p.K;
+          int base = 0;
+          for (int j0 = 0; j0 < p.K; j0 += 32) {
+            const int j = j0 + lane;
+            int s = j < p.K ? row[j] : -1;
+            if (s < -1 || s >= nv) {
+              set_status(p.status, kStatusBadIndex);
+              s = -1;
+            }
+            const bool ok = s >= 0;
+            const unsigned m = __ballot_sync(0xffffffffu, ok);
+            if (ok) {
+              list[base + __popc(m & ((1u << lane) - 1u))] = s;
+              kmax = fmaxf(kmax, p.ent_norm[(size_t)b * p.N + s]);
+            }
+            base += __popc(m);
+          }
+          n_ent = base;
+        } else if (p.ratio > 0) {
+          n_ent = nv;
+          for (int s = lane; s < nv; s += 32) kmax = fmaxf(kmax, p.ent_norm[(size_t)b * p.N + s]);
+        }
+        inf.w_lo = max(0, t - p.window + 1);
+        for (int u = inf.w_lo + lane; u <= t; u += 32) kmax = fmaxf(kmax, p.kv_norm[(size_t)b * p.S + u]);
+        for (int o = 16; o > 0; o >>= 1) kmax = fmaxf(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+        __syncwarp();
+      }
+      inf.n_ent = n_ent;
+      inf.ent_tiles = (n_ent + kTileKeys - 1) / kTileKeys;
+      inf.tiles = inf.ent_tiles + 1;            // + the window tile
+      inf.kmax = kmax;
+      // publish the query
+      const int is = qc & 1;
+      bool ok = true;
+      if (lane == 0) {
+        if (qc >= 2) ok = wait_ok(&c->info_empty[is], ((qc >> 1) - 1) & 1, c, p.status);
+        c->info[is] = inf;
+        mbar_arrive(&c->info_full[is]);
+      }
+      ok = __shfl_sync(0xffffffffu, (int)ok, 0);
+      if (inf.done || !ok) break;
+      // queries: the 64 head rows of (b, t)
+      if (lane == 0) {
+        if (qc >= 1) ok = wait_ok(&c->q_empty, (qc - 1) & 1, c, p.status);
+        if (ok) {
+          mbar_expect_tx(&c->q_full, 8 * kQBlockBytes);
+          for (int kb = 0; kb < 8; ++kb)
+            tma_load_2d(smem + OFF_Q + kb * kQBlockBytes, &map_q, 64 * kb, (b * p.S + t) * kH, &c->q_full);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, (int)ok, 0);
+      if (!ok) break;
+      // key tiles
+      for (int j = 0; j < inf.tiles && ok; ++j) {
+        const bool window_tile = j == inf.ent_tiles;
+        for (int kb = 0; kb < kSlots; ++kb) {
+          if (lane == 0) {
+            if (g >= 1) ok = wait_ok(&c->empty[kb], (g - 1) & 1, c, p.status);
+            if (ok) mbar_expect_tx(&c->full[kb], kSlotBytes);
+          }
+          ok = __shfl_sync(0xffffffffu, (int)ok, 0);
+          if (!ok) break;
+          __syncwarp();
+          uint8_t* dst = smem + OFF_SLOT + kb * kSlotBytes;
+          if (window_tile) {
+            if (lane == 0) tma_load_2d(dst, &map_kv, 64 * kb, b * p.S + t - (kTileKeys - 1), &c->full[kb]);
+          } else if (p.idx != nullptr) {
+            // lane l gathers keys 4l..4l+3 of the tile
+            const int k0 = j * kTileKeys + 4 * lane;
+            int r[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) r[i] = b * p.N + (k0 + i < n_ent ? list[k0 + i] : 0);
+            tma_gather4(dst + 4 * lane * 128, &map_ent_g, 64 * kb, r[0], r[1], r[2], r[3], &c->full[kb]);
+          } else {
+            if (lane == 0) tma_load_2d(dst, &map_ent, 64 * kb, b * p.N + j * kTileKeys, &c->full[kb]);
+          }
+        }
+        ++g;
+      }
+      if (!ok) break;
+      ++qc;
+      __syncwarp();
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id1 = idesc_bf16_f32(128, 64, 0, 0);
+      const uint32_t id2 = idesc_bf16_f32(128, 64, 1, 1);
+      int qc = 0, g = 0;
+      bool ok = true;
+      while (ok) {
+        const int is = qc & 1;
+        ok = wait_ok(&c->info_full[is], (qc >> 1) & 1, c, p.status);
+        if (!ok) break;
+        const QInfo inf = c->info[is];
+        mbar_arrive(&c->info_empty[is]);
+        if (inf.done) break;
+        ok = wait_ok(&c->q_ready, qc & 1, c, p.status);
+        tc_fence_after();
+        for (int j = 0; j < inf.tiles && ok; ++j) {
+          const int sb = g & 1;
+          const uint32_t s_tmem = tmem + 64 * sb;
+          for (int kb = 0; kb < kSlots && ok; ++kb) {
+            ok = wait_ok(&c->full[kb], g & 1, c, p.status);
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(smem + OFF_SLOT + kb * kSlotBytes);
+            const uint32_t b0 = smem_u32(smem + OFF_Q + kb * kQBlockBytes);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              umma_f16_ss(s_tmem, smem_desc(a0 + 32 * ks, 16, 1024, kLayoutSW128),
+                          smem_desc(b0 + 32 * ks, 16, 1024, kLayoutSW128), id1, (kb | ks) != 0);
+          }
+          umma_commit(&c->s_full[sb]);
+          if (j == inf.tiles - 1) umma_commit(&c->q_empty);
+          if (!ok) break;
+          ok = wait_ok(&c->p_ready[sb], (g >> 1) & 1, c, p.status);
+          if (ok && j == 0 && qc >= 1) ok = wait_ok(&c->o_empty, (qc - 1) & 1, c, p.status);
+          tc_fence_after();
+          const uint32_t pb = smem_u32(smem + OFF_P + sb * kPBytes);
+          for (int m = 0; m < 4; ++m) {
+            const uint32_t a0 = smem_u32(smem + OFF_SLOT + (2 * m) * kSlotBytes);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+              umma_f16_ss(tmem + 128 + 64 * m, smem_desc(a0 + 2048 * ks, kSlotBytes, 1024, kLayoutSW128),
+                          smem_desc(pb + 256 * ks, 128, 2048, kLayoutNone), id2, (j > 0 || ks > 0) ? 1u : 0u);
+            umma_commit(&c->empty[2 * m]);
+            umma_commit(&c->empty[2 * m + 1]);
+          }
+          ++g;
+        }
+        umma_commit(&c->o_full);
+        ++qc;
+      }
+      // every issued MMA completes before TMEM is released
+      umma_commit(&c->fin);
+      mbar_wait(&c->fin, 0, &c->abort, p.status, 200000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int ts = threadIdx.x - 64;          // 0..127
+    const int quarter = warp & 3;             // TMEM lane quarter of this warp
+    const int krow = 32 * quarter + lane;     // key row / dim row owned in TMEM
+    const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
+    const float log2e = 1.4426950408889634f;
+    const float c1 = p.scale * log2e;
+    int qc = 0, g = 0;
+    while (true) {
+      const int is = qc & 1;
+      wait_ok(&c->info_full[is], (qc >> 1) & 1, c, p.status);
+      const QInfo inf = c->info[is];
+      mbar_arrive(&c->info_empty[is]);
+      if (ts == 0) c->decision = (c->abort || inf.done) ? 1 : 0;
+      named_bar_sync(1, 128);
+      if (c->decision) break;
+      const int t = inf.t, b = inf.b;
+
+      // rotate the last 64 dims of each head at position t, then head norms
+      wait_ok(&c->q_full, qc & 1, c, p.status);
+      const int h = ts >> 1, half = ts & 1;
+      uint8_t* qrow = smem + OFF_Q + 7 * kQBlockBytes + h * 128;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const int ch = 4 * half + cc;                        // 16-byte chunk of dims 448..511
+        uint4* ptr = reinterpret_cast<uint4*>(qrow + ((ch ^ (h & 7)) * 16));
+        uint4 u = *ptr;
+        __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float2 f = __bfloat1622float2(hv[i]);
+          float cs, sn;
+          rope_cos_sin(t, p.inv_freq[ch * 4 + i], &cs, &sn);
+          rot_pair(f.x, f.y, cs, sn);
+          hv[i] = __floats2bfloat162_rn(f.x, f.y);
+        }
+        *ptr = u;
+      }
+      float ss = 0.f;
+      for (int kb = 4 * half; kb < 4 * half + 4; ++kb) {
+        const uint4* r = reinterpret_cast<const uint4*>(smem + OFF_Q + kb * kQBlockBytes + h * 128);
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          uint4 u = r[cc];
+          const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float2 f = __bfloat1622float2(hv[i]);
+            ss = fmaf(f.x, f.x, ss);
+            ss = fmaf(f.y, f.y, ss);
+          }
+        }
+      }
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      if (half == 0) {
+        float m = p.scale * sqrtf(ss) * inf.kmax;
+        m = m * (1.0f + 1e-5f) + 1e-6f;                     // covers rounding of the bound itself
+        if (p.sink != nullptr) m = fmaxf(m, p.sink[h]);
+        c->mlog2[h] = m * log2e;
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      mbar_arrive(&c->q_ready);
+
+      float lsum[kH];
+#pragma unroll
+      for (int i = 0; i < kH; ++i) lsum[i] = 0.f;
+      const int nk_total = inf.n_ent + (t - inf.w_lo + 1);
+      for (int j = 0; j < inf.tiles; ++j) {
+        const int sb = g & 1;
+        bool valid;
+        if (j < inf.ent_tiles) {
+          valid = j * kTileKeys + krow < inf.n_ent;
+        } else {
+          const int u = t - (kTileKeys - 1) + krow;
+          valid = u >= inf.w_lo && u <= t;
+        }
+        wait_ok(&c->s_full[sb], (g >> 1) & 1, c, p.status);
+        tc_fence_after();
+        float v[kH];
+        tmem_ld32(tmem + lane_base + 64 * sb, v);
+        tmem_ld32(tmem + lane_base + 64 * sb + 32, v + 32);
+        tmem_wait_ld();
+        uint32_t pk[kH / 2];
+#pragma unroll
+        for (int i = 0; i < kH / 2; ++i) {
+          float x0 = valid ? ex2_approx(fmaf(v[2 * i], c1, -c->mlog2[2 * i])) : 0.f;
+          float x1 = valid ? ex2_approx(fmaf(v[2 * i + 1], c1, -c->mlog2[2 * i + 1])) : 0.f;
+          pk[i] = pack_bf16x2(x0, x1);
+          lsum[2 * i] += __uint_as_float(pk[i] << 16);
+          lsum[2 * i + 1] += __uint_as_float(pk[i] & 0xFFFF0000u);
+        }
+        uint8_t* prow = smem + OFF_P + sb * kPBytes + krow * 16;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          *reinterpret_cast<uint4*>(prow + cc * 2048) =
+              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&c->p_ready[sb]);
+        ++g;
+      }
+
+      // ---- epilogue: denominators, lse, O^T / l, de-rotation, TMA store
+      wait_ok(&c->o_full, qc & 1, c, p.status);
+      tc_fence_after();
+      float* red = reinterpret_cast<float*>(smem + OFF_P);     // both P buffers are idle now
+#pragma unroll
+      for (int i = 0; i < kH; ++i) {
+        float x = lsum[i];
+        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        if (lane == 0) red[quarter * kH + i] = x;
+      }
+      named_bar_sync(1, 128);
+      if (ts < kH) {
+        float l = red[ts] + red[kH + ts] + red[2 * kH + ts] + red[3 * kH + ts];
+        const float m = c->mlog2[ts] / log2e;
+        if (p.sink != nullptr) l += expf(p.sink[ts] - m);
+        // too little mass under the bound: exp underflow may have lost keys
+        const bool bad = !(l >= (float)nk_total * 1.0e-26f) || !(l < INFINITY);
+        if (bad) atomicOr(&c->redo, 1);
+        c->inv_l[ts] = 1.0f / l;
+        if (p.lse) p.lse[((size_t)b * p.S + t) * kH + ts] = m + logf(l);
+      }
+      named_bar_sync(1, 128);
+      if (ts == 0 && c->redo) {
+        const int slot = atomicAdd(&p.counters[1], 1);
+        p.counters[2 + slot] = b * p.S + t;
+        c->redo = 0;
+      }
+      // de-rotation angle of this thread's dim pair (M-block 3 holds dims 384..511)
+      float dc = 1.f, ds = 0.f;
+      const int dim3 = 384 + krow;
+      if (dim3 >= kD - kR) rope_cos_sin(t, p.inv_freq[(dim3 - (kD - kR)) >> 1], &dc, &ds);
+      for (int m = 0; m < 4; ++m) {
+        uint8_t* stage = smem + OFF_P + (m & 1) * kPBytes;
+        if (m >= 2) {
+          if (ts == 0) tma_store_wait_read<1>();
+          named_bar_sync(1, 128);
+        }
+        float v[kH];
+        tmem_ld32(tmem + lane_base + 128 + 64 * m, v);
+        tmem_ld32(tmem + lane_base + 128 + 64 * m + 32, v + 32);
+        tmem_wait_ld();
+        if (m == 3) {
+          tc_fence_before();
+          mbar_arrive(&c->o_empty);
+        }
+#pragma unroll
+        for (int i = 0; i < kH; ++i) v[i] *= c->inv_l[i];
+        if (m == 3) {
+          const bool odd = lane & 1;
+#pragma unroll
+          for (int i = 0; i < kH; ++i) {
+            const float other = __shfl_xor_sync(0xffffffffu, v[i], 1);
+            if (dim3 >= kD - kR) v[i] = odd ? (-other * ds + v[i] * dc) : (v[i] * dc + other * ds);
+          }
+        }
+        __nv_bfloat16* srow = reinterpret_cast<__nv_bfloat16*>(stage) + krow;
+#pragma unroll
+        for (int i = 0; i < kH; ++i) srow[i * 128] = __float2bfloat16_rn(v[i]);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (ts == 0) {
+          tma_store_2d(&map_o, 128 * m, (b * p.S + t) * kH, stage);
+          tma_store_commit();
+        }
+      }
+      if (ts == 0) tma_store_wait_read<0>();
+      named_bar_sync(1, 128);
+      ++qc;
+    }
+    if (ts == 0) tma_store_wait_all<0>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side: tensor maps and launch
+// ---------------------------------------------------------------------------
+}  // namespace
+
+cudaError_t launch_mqa_tc(const v4_config& cfg, const void* q, const void* kv_rot, const void* ent,
+                          const int32_t* idx, const float* sink, const float* inv_freq,
+                          const float* kv_norm, const float* ent_norm, void* o, float* lse,
+                          int* counters, int* status, cudaStream_t st) {
+  const int B = cfg.batch, S = cfg.seqlen;
+  const int N = cfg.ratio > 0 ? S / cfg.ratio : 0;
+  CUtensorMap mq, mkv, ment, mentg, mo;
+  const uint64_t qrows = (uint64_t)B * S * kH;
+  int e = 0;
+  e |= make_tmap_bf16_2d(&mq, q, kD, qrows, 64, 64, true);
+  e |= make_tmap_bf16_2d(&mkv, kv_rot, kD, (uint64_t)B * S, 64, kTileKeys, true);
+  const void* ent_base = (ent != nullptr && N > 0) ? ent : kv_rot;      // unused when there are no entries
+  const uint64_t ent_rows = (ent != nullptr && N > 0) ? (uint64_t)B * N : (uint64_t)B * S;
+  e |= make_tmap_bf16_2d(&ment, ent_base, kD, ent_rows, 64, kTileKeys, true);
+  e |= make_tmap_bf16_2d(&mentg, ent_base, kD, ent_rows, 64, 1, true);
+  e |= make_tmap_bf16_2d(&mo, o, kD, qrows, 128, 64, false);
+  if (e) return cudaErrorInvalidValue;
+  Params prm;
+  prm.idx = idx;
+  prm.sink = sink;
+  prm.inv_freq = inv_freq;
+  prm.kv_norm = kv_norm;
+  prm.ent_norm = ent_norm;
+  prm.lse = lse;
+  prm.status = status;
+  prm.counters = counters;
+  prm.B = B;
+  prm.S = S;
+  prm.N = N;
+  prm.ratio = cfg.ratio;
+  prm.window = cfg.window;
+  prm.K = cfg.topk;
+  prm.scale = cfg.softmax_scale > 0.f ? cfg.softmax_scale : 1.0f / sqrtf((float)kD);
+  cudaError_t err = cudaFuncSetAttribute(mqa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+  if (err != cudaSuccess) return err;
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int total = B * S;
+  const int grid = total < sms ? total : sms;
+  err = cudaMemsetAsync(counters, 0, 2 * sizeof(int), st);
+  if (err != cudaSuccess) return err;
+  mqa_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mq, mkv, ment, mentg, mo, prm);
+  note_launch();
+  return cudaGetLastError();
+}
+
+bool mqa_tc_supported(const v4_config& c) {
+  return c.dtype == V4_BF16 && c.n_heads == kH && c.head_dim == kD && c.rope_dim == kR &&
+         c.window >= 1 && c.window <= kTileKeys && c.topk <= kMaxSel && (c.ratio == 0 || c.ratio >= 1);
+}
+
+}  // namespace v4

@@ -188,7 +188,10 @@ def test_sparse_mqa(name, base, over, mode, sink):
     assert rel_l2(o, ro) < tol
     fin = np.isfinite(rl)
     assert np.array_equal(fin, np.isfinite(lse))
-    assert np.max(np.abs(lse[fin] - rl[fin])) < (1e-5 if p["dtype"] == "f32" else 2e-2)
+    if p["dtype"] == "f32":
+        assert np.max(np.abs(lse[fin] - rl[fin])) < 1e-5
+    else:
+        assert np.all(np.abs(lse[fin] - rl[fin]) < 2e-2 + 4e-3 * np.abs(rl[fin]))
     # per-row relative error stays small too (no row may be wrong)
     B, S, H, D = o.shape
     num = np.linalg.norm((o - ro).reshape(B * S, -1), axis=1)

@@ -1,0 +1,172 @@
+"""Tensor-core attention (tcgen05 / TMA) against the oracle.
+
+Forced tensor-core path at the Flash shapes (64 heads, 512-d latent, 64 rotated
+dims, bf16): CSA selections, HCA dense entries, window-only, ragged lengths,
+batches, sink, top-512 over several entry tiles, inputs whose large norms push
+the softmax bound far above the logits (those queries go through the
+running-max fix-up), and the full S=16384 layers of the benchmark checked on
+sampled rows.  Tolerance: 1e-2 relative L2 (bf16 storage, fp32 accumulation).
+"""
+import numpy as np
+import pytest
+import torch
+
+import seeded_inputs as SI
+import sparse_compressed_attention_gb300 as V
+from oracle import v4_oracle as O
+from tests.helpers import check_topk_rows, inv_freq_for, np64, rel_l2, to_dev
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from sparse_compressed_attention_gb300 import build
+    build.build()
+    V.lib()
+
+
+def _run(p, mode, sink, path, seed=0, q_scale=1.0, idx_seed=7):
+    x = SI.make_layer_inputs(p, "cpu", seed=seed, sink=sink)
+    if q_scale != 1.0:
+        x["q"] = (x["q"].float() * q_scale).to(x["q"].dtype)
+    f = inv_freq_for(p)
+    xd = to_dev(x)
+    fd = torch.from_numpy(f).cuda()
+    B, S, H, r = p["B"], p["S"], p["H"], p["ratio"]
+    ent = ent_d = idx = idx_d = None
+    if r > 0:
+        ent = O.compress(np64(x["ckv"]), np64(x["cscore"]), np64(x["ape"]), None, f, r, p["overlap"],
+                         1e-6, store_bf16=True)
+        ent_d = torch.from_numpy(ent).to(torch.bfloat16).cuda()
+    K = p["K"] if mode == "csa" else 0
+    if mode == "csa":
+        idx_d = SI.random_topk_indices(B, S, r, K, "cpu", seed=idx_seed)
+        idx = idx_d.numpy()
+        idx_d = idx_d.cuda()
+    cfg = V.config_from_preset(p, K=K, path=path)
+    o = torch.empty_like(xd["q"])
+    lse = torch.empty(B, S, H, dtype=torch.float32, device="cuda")
+    ws = V.alloc_workspace(cfg)
+    V.v4_reset_device_status()
+    V.v4_sparse_mqa_fwd(cfg, xd["q"], xd["kv"], ent_d, idx_d, xd["sink"], fd, o, lse, ws)
+    assert V.v4_get_device_status() == 0
+    ro, rl = O.sparse_mqa(np64(x["q"]), np64(x["kv"]), ent, idx, np64(x["sink"]), f, r, p["W"],
+                          store_bf16=True)
+    return np64(o), np64(lse), ro, rl
+
+
+def _check(o, lse, ro, rl, tol=TOL):
+    assert rel_l2(o, ro) < tol
+    B, S, H, D = o.shape
+    num = np.linalg.norm((o - ro).reshape(B * S, -1), axis=1)
+    den = np.linalg.norm(ro.reshape(B * S, -1), axis=1) + 1e-30
+    assert np.max(num / den) < 5 * tol, "worst row %d: %.3e" % (np.argmax(num / den), np.max(num / den))
+    fin = np.isfinite(rl)
+    assert np.array_equal(fin, np.isfinite(lse))
+    # the kernel feeds the tensor cores bf16 copies of the rotated query and
+    # window keys: a relative 2^-8 on the rotated part of each logit
+    assert np.all(np.abs(lse[fin] - rl[fin]) < 2e-2 + 4e-3 * np.abs(rl[fin]))
+
+
+CASES = [
+    # name, preset, overrides, mode, sink
+    ("csa_k64_s700", "csa_bf16_4k", dict(S=700, K=64), "csa", False),
+    ("csa_k512_s2100", "csa_bf16_4k", dict(S=2100), "csa", False),
+    ("csa_k32_b2_sink", "csa_bf16_4k", dict(S=300, B=2, K=32), "csa", True),
+    ("csa_s1", "csa_bf16_4k", dict(S=1, K=16), "csa", False),
+    ("hca_s1000_sink", "hca_bf16_16k", dict(S=1000), "hca", True),
+    ("hca_two_tiles", "hca_bf16_16k", dict(S=260, ratio=2), "hca", False),
+    ("hca_b2_ragged", "hca_bf16_16k", dict(S=777, B=2, ratio=16), "hca", False),
+    ("swa_s300", "swa_bf16_16k", dict(S=300), "swa", False),
+    ("swa_w7_b2", "swa_bf16_16k", dict(S=100, B=2, W=7), "swa", True),
+]
+
+
+@pytest.mark.parametrize("name,base,over,mode,sink", CASES, ids=[c[0] for c in CASES])
+def test_tc_attention_matches_oracle(name, base, over, mode, sink):
+    p = SI.preset(base, q_mode="direct", **over)
+    o, lse, ro, rl = _run(p, mode, sink, V.V4_PATH_TC)
+    _check(o, lse, ro, rl)
+
+
+def test_tc_and_simt_agree():
+    p = SI.preset("csa_bf16_4k", q_mode="direct", S=900, K=128)
+    o1, l1, ro, rl = _run(p, "csa", True, V.V4_PATH_TC)
+    o2, l2, _, _ = _run(p, "csa", True, V.V4_PATH_SIMT)
+    assert rel_l2(o1, o2) < TOL
+    _check(o2, l2, ro, rl)
+
+
+def test_large_norms_take_the_fixup_path():
+    # q scaled by 16: the Cauchy-Schwarz bound (about 362) sits far above the
+    # logits, exp() underflows for every key, and the fix-up kernel recomputes
+    # those queries with a running max.
+    p = SI.preset("hca_bf16_16k", q_mode="direct", S=400, ratio=16)
+    o, lse, ro, rl = _run(p, "hca", False, V.V4_PATH_TC, q_scale=16.0)
+    _check(o, lse, ro, rl)
+
+
+def test_forced_tc_path_rejects_other_shapes():
+    p = SI.preset("tiny_csa_f32", ratio=0, overlap=0, K=0)
+    cfg = V.config_from_preset(p, path=V.V4_PATH_TC)
+    x = SI.make_layer_inputs(p, "cuda")
+    with pytest.raises(V.V4Error) as e:
+        V.v4_sparse_mqa_fwd(cfg, x["q"], x["kv"], None, None, None,
+                            torch.from_numpy(inv_freq_for(p)).cuda(), torch.empty_like(x["q"]), None,
+                            V.alloc_workspace(cfg))
+    assert e.value.status == 2
+
+
+@pytest.mark.parametrize("name", ["csa_bf16_16k", "hca_bf16_16k"])
+def test_full_size_layer_sampled_rows(name):
+    """The bench's layers (B=1, S=16384, rank-1024 queries) through
+    v4_attn_layer_fwd, checked on 40 sampled query rows (and, for CSA, the
+    top-512 sets of those rows)."""
+    p = SI.preset(name)
+    x = SI.make_layer_inputs(p, "cuda", seed=11)
+    f = inv_freq_for(p)
+    xd = dict(x, inv_freq=torch.from_numpy(f).cuda())
+    cfg = V.config_from_preset(p)
+    B, S, H, K = p["B"], p["S"], p["H"], p["K"]
+    outs = {"o": torch.empty_like(x["q"]), "lse": torch.empty(B, S, H, device="cuda")}
+    if K:
+        outs["idx"] = torch.empty(B, S, K, dtype=torch.int32, device="cuda")
+        outs["ikey"] = torch.empty(B, S // p["ratio"], p["Di"], dtype=torch.bfloat16, device="cuda")
+    outs["ent"] = torch.empty(B, S // p["ratio"], p["D"], dtype=torch.bfloat16, device="cuda")
+    ws = V.alloc_workspace(cfg)
+    V.v4_reset_device_status()
+    V.v4_attn_layer_fwd(cfg, xd, outs, ws)
+    torch.cuda.synchronize()
+    assert V.v4_get_device_status() == 0
+    rows = np.unique(np.concatenate([np.linspace(0, S - 1, 32).round().astype(int),
+                                     [0, 1, 127, 128, 511, 512, 2047, S - 1]]))
+    ent = O.compress(np64(x["ckv"]), np64(x["cscore"]), np64(x["ape"]), None, f, p["ratio"], p["overlap"],
+                     1e-6, store_bf16=True)
+    assert rel_l2(np64(outs["ent"]), ent) < 1e-3
+    idx_rows = None
+    if K:
+        ikey = O.compress(np64(x["ickv"]), np64(x["icscore"]), np64(x["iape"]), None, f, p["ratio"],
+                          p["overlap"], 1e-6, hadamard=True, store_bf16=True)
+        iq_rows = np64(x["iq"][:, torch.from_numpy(rows).cuda()])
+        w_rows = np64(x["w"][:, torch.from_numpy(rows).cuda()])
+        sel = O.indexer_topk(iq_rows, ikey, w_rows, f, p["ratio"], K, store_bf16=True, rows=rows,
+                             rows_only=True)
+        gi = outs["idx"][0, torch.from_numpy(rows).cuda()].cpu().numpy()
+        agree = total = 0
+        for i in range(len(rows)):
+            a = set(gi[i][gi[i] >= 0].tolist())
+            r = set(sel["idx"][0, i][sel["idx"][0, i] >= 0].tolist())
+            assert len(a) == len(r)
+            agree += len(a & r)
+            total += len(r)
+        assert agree >= 0.99 * total, (agree, total)
+        idx_rows = sel["idx"]
+    q_rows = np64(x["q"][:, torch.from_numpy(rows).cuda()])
+    # the oracle attends with its own entries and its own selection
+    ro, rl = O.sparse_mqa(q_rows, np64(x["kv"]), ent, idx_rows, None, f, p["ratio"], p["W"],
+                          store_bf16=True, rows=rows, rows_only=True)
+    go = np64(outs["o"][:, torch.from_numpy(rows).cuda()])
+    gl = np64(outs["lse"][:, torch.from_numpy(rows).cuda()])
+    _check(go, gl, ro, rl)
