@@ -121,6 +121,7 @@ Workspace plan_workspace(const v4_config& c) {
   take(w.idx, w.idx_bytes, sel ? B * S * c.topk * 4 : 0);
   take(w.knorm, w.knorm_bytes, (B * S + B * N) * 4);
   take(w.counters, w.counters_bytes, (2 + B * S) * 4);
+  take(w.rope, w.rope_bytes, S * (size_t)(c.rope_dim / 2) * 8);
   w.total = off;
   return w;
 }
@@ -191,20 +192,37 @@ static v4_status do_compress(const v4_config& c, const void* ckv, const void* cs
   return V4_OK;
 }
 
+// cos/sin table of every position (kept in the workspace for the call)
+static v4_status do_rope_table(const v4_config& c, const float* f, char* ws, cudaStream_t st) {
+  const Workspace plan = plan_workspace(c);
+  CU(launch_rope_table(c, f, (float2*)(ws + plan.rope), st), "rope table kernel");
+  return V4_OK;
+}
+
 static v4_status do_indexer(const v4_config& c, const void* iq, int prepared, const void* ikey,
                             const float* w, const float* f, int32_t* idx, float* iscore,
-                            char* ws, cudaStream_t st) {
+                            char* ws, cudaStream_t st, bool table_ready) {
   const Workspace plan = plan_workspace(c);
   const void* iqp = iq;
   if (!prepared) {
+    if (!table_ready) {
+      v4_status s = do_rope_table(c, f, ws, st);
+      if (s != V4_OK) return s;
+    }
     ProfScope ps(K_IDX_PREP, st);
-    CU(launch_indexer_prep(c, iq, f, ws + plan.iqp, st), "indexer prep kernel");
+    CU(launch_indexer_prep(c, iq, (const float2*)(ws + plan.rope), f, ws + plan.iqp, st), "indexer prep kernel");
     iqp = ws + plan.iqp;
   }
   float* scores = (float*)(ws + plan.scores);
   {
     ProfScope ps(K_IDX_SCORE, st);
-    CU(launch_indexer_scores_simt(c, iqp, ikey, w, scores, st), "indexer score kernel");
+    if (c.path != V4_PATH_SIMT && indexer_tc_supported(c)) {
+      int* status = status_ptr();
+      if (!status) return fail(V4_ERR_CUDA, "device status word unavailable");
+      CU(launch_indexer_scores_tc(c, iqp, ikey, w, scores, status, st), "tensor-core indexer kernel");
+    } else {
+      CU(launch_indexer_scores_simt(c, iqp, ikey, w, scores, st), "indexer score kernel");
+    }
   }
   {
     ProfScope ps(K_TOPK, st);
@@ -219,8 +237,9 @@ static bool use_tc_attention(const v4_config& c) {
 
 static v4_status do_mqa(const v4_config& c, const void* q, const void* kv, const void* ent,
                         const int32_t* idx, const float* sink, const float* f, void* o,
-                        float* lse, char* ws, cudaStream_t st) {
+                        float* lse, char* ws, cudaStream_t st, bool table_ready) {
   const Workspace plan = plan_workspace(c);
+  const float2* table = (const float2*)(ws + plan.rope);
   int* status = status_ptr();
   if (!status) return fail(V4_ERR_CUDA, "device status word unavailable");
   void* kv_rot = ws + plan.kv_rot;
@@ -230,7 +249,11 @@ static v4_status do_mqa(const v4_config& c, const void* q, const void* kv, const
   {
     ProfScope ps(K_ROTATE, st);
     if (tc) {
-      CU(launch_key_prep(c, kv, ent, f, kv_rot, kv_norm, ent_norm, st), "key prep kernel");
+      if (!table_ready) {
+        v4_status s = do_rope_table(c, f, ws, st);
+        if (s != V4_OK) return s;
+      }
+      CU(launch_key_prep(c, kv, ent, table, kv_rot, kv_norm, ent_norm, st), "key prep kernel");
     } else {
       CU(launch_rotate_rows(c, kv, f, kv_rot, st), "window-key rotation kernel");
     }
@@ -239,7 +262,7 @@ static v4_status do_mqa(const v4_config& c, const void* q, const void* kv, const
     int* counters = (int*)(ws + plan.counters);
     {
       ProfScope ps(K_ATTN, st);
-      CU(launch_mqa_tc(c, q, kv_rot, ent, idx, sink, f, kv_norm, ent_norm, o, lse, counters, status, st),
+      CU(launch_mqa_tc(c, q, kv_rot, ent, idx, sink, table, kv_norm, ent_norm, o, lse, counters, status, st),
          "tensor-core attention kernel");
     }
     // queries whose bound-shifted softmax kept too little mass are recomputed
@@ -318,7 +341,7 @@ v4_status v4_indexer_prep(const v4_config* cfg, const void* iq, const float* inv
   REQ(iq, "iq");
   REQ(iq_prep, "iq_prep");
   if (cfg->rope_dim > 0) REQ(inv_freq, "inv_freq");
-  CU(launch_indexer_prep(*cfg, iq, inv_freq, iq_prep, (cudaStream_t)stream), "indexer prep kernel");
+  CU(launch_indexer_prep(*cfg, iq, nullptr, inv_freq, iq_prep, (cudaStream_t)stream), "indexer prep kernel");
   return V4_OK;
 }
 
@@ -334,10 +357,12 @@ v4_status v4_indexer_topk(const v4_config* cfg, const void* iq, int32_t iq_prepa
   OPT(iscore, "iscore");
   if (cfg->seqlen / cfg->ratio > 0) REQ(ikey, "ikey");
   if (!iq_prepared && cfg->rope_dim > 0) REQ(inv_freq, "inv_freq");
+  if (cfg->path == V4_PATH_TC && !indexer_tc_supported(*cfg))
+    return fail(V4_ERR_UNSUPPORTED, "tensor-core indexer needs bf16, idx_heads 64, idx_dim 128");
   s = check_ws(*cfg, workspace, ws_bytes);
   if (s != V4_OK) return s;
   return do_indexer(*cfg, iq, iq_prepared ? 1 : 0, ikey, w, inv_freq, idx, iscore, (char*)workspace,
-                    (cudaStream_t)stream);
+                    (cudaStream_t)stream, false);
 }
 
 v4_status v4_sparse_mqa_fwd(const v4_config* cfg, const void* q, const void* kv, const void* ent,
@@ -358,7 +383,7 @@ v4_status v4_sparse_mqa_fwd(const v4_config* cfg, const void* q, const void* kv,
   s = check_ws(*cfg, workspace, ws_bytes);
   if (s != V4_OK) return s;
   return do_mqa(*cfg, q, kv, ent, cfg->topk > 0 ? idx : nullptr, sink, inv_freq, o, lse,
-                (char*)workspace, (cudaStream_t)stream);
+                (char*)workspace, (cudaStream_t)stream, false);
 }
 
 v4_status v4_grouped_o_proj(const v4_config* cfg, const void* o, const void* wo_a, void* y,
@@ -414,6 +439,8 @@ v4_status v4_attn_layer_fwd(const v4_config* cfg, const v4_layer_inputs* in, v4_
   void* ent = out->ent ? out->ent : (void*)(ws + plan.ent);
   void* ikey = out->ikey ? out->ikey : (void*)(ws + plan.ikey);
   int32_t* idx = out->idx ? out->idx : (int32_t*)(ws + plan.idx);
+  s = do_rope_table(c, in->inv_freq, ws, st);
+  if (s != V4_OK) return s;
   if (comp) {
     s = do_compress(c, in->ckv, in->cscore, in->ape, in->norm_w, in->inv_freq, c.head_dim, 0, ent, st);
     if (s != V4_OK) return s;
@@ -424,11 +451,11 @@ v4_status v4_attn_layer_fwd(const v4_config* cfg, const v4_layer_inputs* in, v4_
                       ikey, st);
       if (s != V4_OK) return s;
     }
-    s = do_indexer(c, in->iq, 0, ikey, in->w, in->inv_freq, idx, out->iscore, ws, st);
+    s = do_indexer(c, in->iq, 0, ikey, in->w, in->inv_freq, idx, out->iscore, ws, st, true);
     if (s != V4_OK) return s;
   }
   return do_mqa(c, in->q, in->kv, comp ? ent : nullptr, sel ? idx : nullptr, in->sink, in->inv_freq,
-                out->o, out->lse, ws, st);
+                out->o, out->lse, ws, st, true);
 }
 
 const char* v4_last_error(void) { return g_err.c_str(); }

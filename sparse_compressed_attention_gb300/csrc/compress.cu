@@ -175,13 +175,26 @@ __global__ void rotate_rows_kernel(const T* __restrict__ x, const float* __restr
   }
 }
 
+// cos/sin of pos * inv_freq[j] for every position pos < S and pair j, one
+// thread per entry: the table all position-dependent rotations read.
+__global__ void rope_table_kernel(const float* __restrict__ inv_freq, float2* __restrict__ table,
+                                  long long S, int half_r) {
+  const long long total = S * half_r;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    float cs, sn;
+    rope_cos_sin(i / half_r, inv_freq[i % half_r], &cs, &sn);
+    table[i] = make_float2(cs, sn);
+  }
+}
+
 // Key prep: one warp per stored key row.  Rows [0, B*S) are window tokens:
 // rotated at their position u (last R dims), stored in the storage dtype,
 // and their norm taken from the stored (rounded) values.  Rows
 // [B*S, B*S + B*N) are entries (already rotated): only their norm.
 template <typename T>
 __global__ void key_prep_kernel(const T* __restrict__ kv, const T* __restrict__ ent,
-                                const float* __restrict__ inv_freq, T* __restrict__ kv_rot,
+                                const float2* __restrict__ cs_table, T* __restrict__ kv_rot,
                                 float* __restrict__ kv_norm, float* __restrict__ ent_norm,
                                 long long kv_rows, long long ent_rows, int S, int D, int R) {
   const int lane = threadIdx.x & 31;
@@ -197,13 +210,9 @@ __global__ void key_prep_kernel(const T* __restrict__ kv, const T* __restrict__ 
       const int c0 = v * 8;
       if (is_kv) {
         if (c0 >= D - R) {
-          const long long u = row % S;
+          const float2* cs = cs_table + (row % S) * (R / 2) + (c0 - (D - R)) / 2;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            float cs, sn;
-            rope_cos_sin(u, inv_freq[(c0 - (D - R)) / 2 + k], &cs, &sn);
-            rot_pair(e[2 * k], e[2 * k + 1], cs, sn);
-          }
+          for (int k = 0; k < 4; ++k) rot_pair(e[2 * k], e[2 * k + 1], cs[k].x, cs[k].y);
         }
         store8(kv_rot + row * D + c0, e);
         load8(kv_rot + row * D + c0, e);         // norm of the stored values
@@ -224,9 +233,9 @@ __global__ void key_prep_kernel(const T* __restrict__ kv, const T* __restrict__ 
 // inside a thread's 8 elements, larger stages across the Di/8 lanes of the
 // row with warp shuffles.  Requires Di/8 <= 32.
 template <typename T>
-__global__ void indexer_prep_kernel(const T* __restrict__ iq, const float* __restrict__ inv_freq,
-                                    T* __restrict__ out, long long rows, int S, int Hi, int Di,
-                                    int R) {
+__global__ void indexer_prep_kernel(const T* __restrict__ iq, const float2* __restrict__ cs_table,
+                                    const float* __restrict__ inv_freq, T* __restrict__ out,
+                                    long long rows, int S, int Hi, int Di, int R) {
   const int lanes = Di / 8;                                  // lanes per row (power of 2)
   const long long gt = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   const long long row = gt / lanes;
@@ -241,10 +250,17 @@ __global__ void indexer_prep_kernel(const T* __restrict__ iq, const float* __res
   const int c0 = lane * 8;
   if (live && c0 >= Di - R) {
     const long long t = (row / Hi) % S;
+    const int j0 = (c0 - (Di - R)) / 2;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       float cs, sn;
-      rope_cos_sin(t, inv_freq[(c0 - (Di - R)) / 2 + k], &cs, &sn);
+      if (cs_table) {
+        const float2 v = cs_table[t * (R / 2) + j0 + k];
+        cs = v.x;
+        sn = v.y;
+      } else {
+        rope_cos_sin(t, inv_freq[j0 + k], &cs, &sn);
+      }
       rot_pair(e[2 * k], e[2 * k + 1], cs, sn);
     }
   }
@@ -322,7 +338,17 @@ cudaError_t launch_rotate_rows(const v4_config& c, const void* kv, const float* 
   return cudaGetLastError();
 }
 
-cudaError_t launch_key_prep(const v4_config& c, const void* kv, const void* ent, const float* inv_freq,
+cudaError_t launch_rope_table(const v4_config& c, const float* inv_freq, float2* table, cudaStream_t st) {
+  const long long total = (long long)c.seqlen * (c.rope_dim / 2);
+  if (total == 0) return cudaSuccess;
+  long long blocks = (total + 255) / 256;
+  if (blocks > 152LL * 8) blocks = 152LL * 8;
+  rope_table_kernel<<<(int)blocks, 256, 0, st>>>(inv_freq, table, c.seqlen, c.rope_dim / 2);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_key_prep(const v4_config& c, const void* kv, const void* ent, const float2* cs_table,
                             void* kv_rot, float* kv_norm, float* ent_norm, cudaStream_t st) {
   const long long kv_rows = (long long)c.batch * c.seqlen;
   const int N = c.ratio > 0 ? c.seqlen / c.ratio : 0;
@@ -332,29 +358,29 @@ cudaError_t launch_key_prep(const v4_config& c, const void* kv, const void* ent,
   if (blocks > 152LL * 16) blocks = 152LL * 16;
   if (blocks < 1) blocks = 1;
   if (c.dtype == V4_BF16)
-    key_prep_kernel<bf16><<<(int)blocks, threads, 0, st>>>((const bf16*)kv, (const bf16*)ent, inv_freq,
+    key_prep_kernel<bf16><<<(int)blocks, threads, 0, st>>>((const bf16*)kv, (const bf16*)ent, cs_table,
                                                             (bf16*)kv_rot, kv_norm, ent_norm, kv_rows,
                                                             ent_rows, c.seqlen, c.head_dim, c.rope_dim);
   else
-    key_prep_kernel<float><<<(int)blocks, threads, 0, st>>>((const float*)kv, (const float*)ent, inv_freq,
+    key_prep_kernel<float><<<(int)blocks, threads, 0, st>>>((const float*)kv, (const float*)ent, cs_table,
                                                              (float*)kv_rot, kv_norm, ent_norm, kv_rows,
                                                              ent_rows, c.seqlen, c.head_dim, c.rope_dim);
   note_launch();
   return cudaGetLastError();
 }
 
-cudaError_t launch_indexer_prep(const v4_config& c, const void* iq, const float* inv_freq,
-                                void* iqp, cudaStream_t st) {
+cudaError_t launch_indexer_prep(const v4_config& c, const void* iq, const float2* cs_table,
+                                const float* inv_freq, void* iqp, cudaStream_t st) {
   const long long rows = (long long)c.batch * c.seqlen * c.idx_heads;
   const int lanes = c.idx_dim / 8;
   const int threads = 256;
   const long long blocks = (rows * lanes + threads - 1) / threads;
   if (c.dtype == V4_BF16)
     indexer_prep_kernel<bf16><<<(unsigned)blocks, threads, 0, st>>>(
-        (const bf16*)iq, inv_freq, (bf16*)iqp, rows, c.seqlen, c.idx_heads, c.idx_dim, c.rope_dim);
+        (const bf16*)iq, cs_table, inv_freq, (bf16*)iqp, rows, c.seqlen, c.idx_heads, c.idx_dim, c.rope_dim);
   else
     indexer_prep_kernel<float><<<(unsigned)blocks, threads, 0, st>>>(
-        (const float*)iq, inv_freq, (float*)iqp, rows, c.seqlen, c.idx_heads, c.idx_dim,
+        (const float*)iq, cs_table, inv_freq, (float*)iqp, rows, c.seqlen, c.idx_heads, c.idx_dim,
         c.rope_dim);
   note_launch();
   return cudaGetLastError();

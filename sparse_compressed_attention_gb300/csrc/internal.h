@@ -7,7 +7,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/v4attn.h"
+#include "v4attn.h"
 
 namespace v4 {
 
@@ -24,6 +24,7 @@ struct Workspace {
   size_t idx = 0, idx_bytes = 0;           // selected entries [B,S,K] (layer call)
   size_t knorm = 0, knorm_bytes = 0;       // key-row norms [B*S + B*N] (tensor-core attention)
   size_t counters = 0, counters_bytes = 0; // work counter, redo count, redo list [2 + B*S]
+  size_t rope = 0, rope_bytes = 0;         // cos/sin table [S][R/2] float2
   size_t total = 0;
 };
 Workspace plan_workspace(const v4_config& c);
@@ -36,18 +37,24 @@ cudaError_t launch_rotate_rows(const v4_config& c, const void* kv, const float* 
                                void* kv_rot, cudaStream_t st);
 // Rotated window keys plus the Euclidean norm of every stored key row
 // (window rows then entry rows), as the tensor-core attention needs them.
-cudaError_t launch_key_prep(const v4_config& c, const void* kv, const void* ent, const float* inv_freq,
+cudaError_t launch_key_prep(const v4_config& c, const void* kv, const void* ent, const float2* cs_table,
                             void* kv_rot, float* kv_norm, float* ent_norm, cudaStream_t st);
+// cos/sin of every (position < S, rotated pair): table[pos * R/2 + j].
+cudaError_t launch_rope_table(const v4_config& c, const float* inv_freq, float2* table, cudaStream_t st);
 
 // ---- TMA descriptors (tma_host.cu); returns 0 on success
 int make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
                       uint32_t box_rows, bool swizzle128);
-cudaError_t launch_indexer_prep(const v4_config& c, const void* iq, const float* inv_freq,
-                                void* iqp, cudaStream_t st);
+// cs_table may be null (angles are then computed in the kernel from inv_freq)
+cudaError_t launch_indexer_prep(const v4_config& c, const void* iq, const float2* cs_table,
+                                const float* inv_freq, void* iqp, cudaStream_t st);
 
 // ---- indexer (indexer.cu)
 cudaError_t launch_indexer_scores_simt(const v4_config& c, const void* iqp, const void* ikey,
                                        const float* w, float* scores, cudaStream_t st);
+bool indexer_tc_supported(const v4_config& c);
+cudaError_t launch_indexer_scores_tc(const v4_config& c, const void* iqp, const void* ikey, const float* w,
+                                     float* scores, int* status, cudaStream_t st);
 cudaError_t launch_topk(const v4_config& c, const float* scores, int32_t* idx, float* iscore,
                         cudaStream_t st);
 
@@ -60,7 +67,7 @@ cudaError_t launch_mqa_simt(const v4_config& c, const void* q, const void* kv_ro
                             const int* list, cudaStream_t st);
 bool mqa_tc_supported(const v4_config& c);
 cudaError_t launch_mqa_tc(const v4_config& c, const void* q, const void* kv_rot, const void* ent,
-                          const int32_t* idx, const float* sink, const float* inv_freq,
+                          const int32_t* idx, const float* sink, const float2* cs_table,
                           const float* kv_norm, const float* ent_norm, void* o, float* lse,
                           int* counters, int* status, cudaStream_t st);
 

@@ -20,10 +20,17 @@
 // The key tile in shared memory (8 K-blocks of [128 keys x 64 dims], 128-byte
 // swizzle) is the K-major A operand of the first product and, read as
 // MN-major, the A operand of the second.  TMEM: S^T double buffer (2 x 64
-// columns) and O^T (256 columns).
+// columns) and O^T (256 columns).  Contiguous key tiles (window rows, HCA
+// entries) and the query rows arrive by TMA boxes; selected entries are
+// gathered row by row with 16-byte cp.async (many small TMA gathers would
+// serialise in the TMA unit).  The output leaves through shared-memory
+// staging and coalesced 16-byte stores, so it never queues behind loads.
+// Rotations read a per-position cos/sin table built once per call.
 //
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer (and TMEM
-// owner), warps 2-5 softmax + epilogue (one TMEM lane quarter each).
+// Warp roles (256 threads): warp 0 producer (per-query selection list, query
+// rows and contiguous tiles by TMA, one third of the gathers), warp 1 MMA
+// issuer and TMEM owner, warps 2-3 gather the other two thirds, warps 4-7
+// softmax + epilogue (one TMEM lane quarter each).
 #include <cuda.h>
 #include <math.h>
 
@@ -38,7 +45,8 @@ using namespace sm100;
 namespace {
 
 constexpr int kH = 64, kD = 512, kR = 64;
-constexpr int kThreads = 192;
+constexpr int kThreads = 256;
+constexpr int kGatherLanes = 96;                  // warps 0, 2, 3
 constexpr int kTileKeys = 128;
 constexpr int kSlots = 8;                         // one tile: 8 K-blocks of 64 dims
 constexpr uint32_t kSlotBytes = 128 * 128;        // 128 keys x 64 dims x 2 B
@@ -58,15 +66,15 @@ struct QInfo {
 };
 
 struct Ctl {
-  uint64_t full[kSlots], empty[kSlots];
+  uint64_t full[kSlots], empty[kSlots];    // full: 96 gather-lane arrivals + TMA bytes
+  uint64_t list_free;                      // warps 2-3 have read the selection list
   uint64_t q_full, q_ready, q_empty;
   uint64_t s_full[2], p_ready[2];
   uint64_t o_full, o_empty;
   uint64_t info_full[2], info_empty[2];
   uint64_t fin;
   QInfo info[2];
-  float mlog2[kH];
-  float inv_l[kH];
+  float mlog2[2][kH];          // per-query shift (log2 units), double-buffered by query parity
   uint32_t tmem_base;
   int abort;
   int decision;
@@ -77,9 +85,12 @@ constexpr uint32_t kSmemBytes = OFF_CTL + sizeof(Ctl);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Params {
+  const bf16* q;               // [B,S,64,512] (L2 prefetch of upcoming queries)
+  const bf16* ent;             // [B,N,512] gathered entries
+  bf16* o;                     // [B,S,64,512]
   const int32_t* idx;          // [B,S,K] or null
   const float* sink;           // [64] or null
-  const float* inv_freq;       // [32]
+  const float2* rope_cs;       // [S][32] cos/sin
   const float* kv_norm;        // [B*S]
   const float* ent_norm;       // [B*N]
   float* lse;                  // [B,S,64] or null
@@ -93,10 +104,41 @@ __device__ __forceinline__ bool wait_ok(uint64_t* bar, uint32_t parity, Ctl* c, 
   return mbar_wait(bar, parity, &c->abort, status);
 }
 
+// Row groups (4 rows each) of a 128-key tile handled by gather warp gw:
+// groups gw, gw+3, ... (11, 11 and 10 groups).
+constexpr int kMaxGroups = 11;
+
+// Gather one K-block (64 dims) of the selected entries of a tile: lane
+// covers row 4*grp + lane/8, 16-byte chunk lane%8, written into the
+// 128-byte-swizzled K-major slot layout; one arrival when the copies land.
+__device__ __forceinline__ void gather_kblock(uint8_t* slot, const bf16* ent_b, const int* sidx, int gw, int lane,
+                                              int kb, uint64_t* full) {
+  const int chunk = lane & 7;
+  const bf16* src = ent_b + kb * 64 + chunk * 8;
+  const uint32_t d0 = smem_u32(slot);
+#pragma unroll
+  for (int i = 0; i < kMaxGroups; ++i) {
+    const int grp = gw + 3 * i;
+    if (grp < 32) {
+      const int row = 4 * grp + (lane >> 3);
+      cp_async_16(d0 + row * 128 + ((chunk ^ (row & 7)) << 4), src + (size_t)sidx[i] * kD);
+    }
+  }
+  cp_async_mbar_arrive(full);
+}
+
+// Selection-list rows of tile j for gather warp gw (row 0 pads short tiles).
+__device__ __forceinline__ void load_rows(const int* list, int n_ent, int j, int gw, int lane, int* sidx) {
+#pragma unroll
+  for (int i = 0; i < kMaxGroups; ++i) {
+    const int k = j * 128 + 4 * (gw + 3 * i) + (lane >> 3);
+    sidx[i] = (gw + 3 * i < 32 && k < n_ent) ? list[k] : 0;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
-              const __grid_constant__ CUtensorMap map_ent, const __grid_constant__ CUtensorMap map_ent_g,
-              const __grid_constant__ CUtensorMap map_o, const Params p) {
+              const __grid_constant__ CUtensorMap map_ent, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Ctl* c = reinterpret_cast<Ctl*>(smem + OFF_CTL);
   int* list = reinterpret_cast<int*>(smem + OFF_LIST);
@@ -106,7 +148,8 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     return;
   }
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kSlots; ++i) { mbar_init(&c->full[i], 1); mbar_init(&c->empty[i], 1); }
+    for (int i = 0; i < kSlots; ++i) { mbar_init(&c->full[i], kGatherLanes); mbar_init(&c->empty[i], 1); }
+    mbar_init(&c->list_free, 64);
     mbar_init(&c->q_full, 1);
     mbar_init(&c->q_ready, 128);
     mbar_init(&c->q_empty, 1);
@@ -114,7 +157,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       mbar_init(&c->s_full[i], 1);
       mbar_init(&c->p_ready[i], 128);
       mbar_init(&c->info_full[i], 1);
-      mbar_init(&c->info_empty[i], 129);
+      mbar_init(&c->info_empty[i], 1 + 128 + 64);
     }
     mbar_init(&c->o_full, 1);
     mbar_init(&c->o_empty, 128);
@@ -127,8 +170,6 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     prefetch_tmap(&map_q);
     prefetch_tmap(&map_kv);
     prefetch_tmap(&map_ent);
-    prefetch_tmap(&map_ent_g);
-    prefetch_tmap(&map_o);
   }
   if (warp == 1) {
     tmem_alloc(&c->tmem_base, 512);
@@ -143,16 +184,26 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     int qc = 0, g = 0;
-    while (true) {
-      int item = 0;
-      if (lane == 0) item = atomicAdd(&p.counters[0], 1);
-      item = __shfl_sync(0xffffffffu, item, 0);
+    for (int item = blockIdx.x;; item += gridDim.x) {
       QInfo inf;
       inf.done = item >= total ? 1 : 0;
       int b = 0, t = 0;
       if (!inf.done) {
         b = item % p.B;
         t = p.S - 1 - item / p.B;
+        // warm L2 with the query rows and selection of this CTA's next query
+        const int nxt = item + gridDim.x;
+        if (lane == 0 && nxt < total) {
+          const int nb = nxt % p.B, nt = p.S - 1 - nxt / p.B;
+          const bf16* qn = p.q + ((size_t)nb * p.S + nt) * kH * kD;
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(qn), "r"(kH * kD * 2) : "memory");
+          if (p.idx != nullptr && p.K >= 4) {
+            const int32_t* rn = p.idx + ((size_t)nb * p.S + nt) * p.K;
+            const uint32_t bytes = (uint32_t)(p.K * 4) & ~15u;
+            if ((((uintptr_t)rn) & 15u) == 0 && bytes > 0)
+              asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(rn), "r"(bytes) : "memory");
+          }
+        }
       }
       inf.b = b;
       inf.t = t;
@@ -161,31 +212,54 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       if (!inf.done) {
         const int nv = p.ratio > 0 ? min((t + 1) / p.ratio, p.N) : 0;
         if (p.ratio > 0 && p.idx != nullptr) {
-          // compact the valid selected entries into the list (order is free)
+          // the helpers must have read the previous query's list
+          bool lok = true;
+          if (lane == 0 && qc >= 1) lok = wait_ok(&c->list_free, (qc - 1) & 1, c, p.status);
+          __syncwarp();
+          (void)lok;
+          // all selection slots first, then their norms: two dependent rounds
           const int32_t* row = p.idx + ((size_t)b * p.S + t) * p.K;
-          int base = 0;
-          for (int j0 = 0; j0 < p.K; j0 += 32) {
-            const int j = j0 + lane;
-            int s = j < p.K ? row[j] : -1;
-            if (s < -1 || s >= nv) {
+          int sv[kMaxSel / 32];
+#pragma unroll
+          for (int i = 0; i < kMaxSel / 32; ++i) {
+            const int j = lane + 32 * i;
+            sv[i] = j < p.K ? row[j] : -1;
+          }
+          float nrm[kMaxSel / 32];
+#pragma unroll
+          for (int i = 0; i < kMaxSel / 32; ++i) {
+            if (sv[i] < -1 || sv[i] >= nv) {
               set_status(p.status, kStatusBadIndex);
-              s = -1;
+              sv[i] = -1;
             }
-            const bool ok = s >= 0;
+            nrm[i] = sv[i] >= 0 ? p.ent_norm[(size_t)b * p.N + sv[i]] : 0.f;
+          }
+          int base = 0;
+#pragma unroll
+          for (int i = 0; i < kMaxSel / 32; ++i) {
+            const bool ok = sv[i] >= 0;
             const unsigned m = __ballot_sync(0xffffffffu, ok);
-            if (ok) {
-              list[base + __popc(m & ((1u << lane) - 1u))] = s;
-              kmax = fmaxf(kmax, p.ent_norm[(size_t)b * p.N + s]);
-            }
+            if (ok) list[base + __popc(m & ((1u << lane) - 1u))] = sv[i];
             base += __popc(m);
+            kmax = fmaxf(kmax, nrm[i]);
           }
           n_ent = base;
         } else if (p.ratio > 0) {
           n_ent = nv;
-          for (int s = lane; s < nv; s += 32) kmax = fmaxf(kmax, p.ent_norm[(size_t)b * p.N + s]);
+          for (int s0 = 0; s0 < nv; s0 += 128) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int s = s0 + lane + 32 * i;
+              if (s < nv) kmax = fmaxf(kmax, p.ent_norm[(size_t)b * p.N + s]);
+            }
+          }
         }
         inf.w_lo = max(0, t - p.window + 1);
-        for (int u = inf.w_lo + lane; u <= t; u += 32) kmax = fmaxf(kmax, p.kv_norm[(size_t)b * p.S + u]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int u = inf.w_lo + lane + 32 * i;
+          if (u <= t) kmax = fmaxf(kmax, p.kv_norm[(size_t)b * p.S + u]);
+        }
         for (int o = 16; o > 0; o >>= 1) kmax = fmaxf(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
         __syncwarp();
       }
@@ -217,26 +291,25 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       // key tiles
       for (int j = 0; j < inf.tiles && ok; ++j) {
         const bool window_tile = j == inf.ent_tiles;
+        int sidx[kMaxGroups];
+        if (!window_tile && p.idx != nullptr) load_rows(list, n_ent, j, 0, lane, sidx);
         for (int kb = 0; kb < kSlots; ++kb) {
-          if (lane == 0) {
-            if (g >= 1) ok = wait_ok(&c->empty[kb], (g - 1) & 1, c, p.status);
-            if (ok) mbar_expect_tx(&c->full[kb], kSlotBytes);
-          }
+          if (lane == 0 && g >= 1) ok = wait_ok(&c->empty[kb], (g - 1) & 1, c, p.status);
           ok = __shfl_sync(0xffffffffu, (int)ok, 0);
           if (!ok) break;
-          __syncwarp();
           uint8_t* dst = smem + OFF_SLOT + kb * kSlotBytes;
-          if (window_tile) {
-            if (lane == 0) tma_load_2d(dst, &map_kv, 64 * kb, b * p.S + t - (kTileKeys - 1), &c->full[kb]);
-          } else if (p.idx != nullptr) {
-            // lane l gathers keys 4l..4l+3 of the tile
-            const int k0 = j * kTileKeys + 4 * lane;
-            int r[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) r[i] = b * p.N + (k0 + i < n_ent ? list[k0 + i] : 0);
-            tma_gather4(dst + 4 * lane * 128, &map_ent_g, 64 * kb, r[0], r[1], r[2], r[3], &c->full[kb]);
+          if (window_tile || p.idx == nullptr) {
+            if (lane == 0) {
+              mbar_expect_tx(&c->full[kb], kSlotBytes);
+              if (window_tile)
+                tma_load_2d(dst, &map_kv, 64 * kb, b * p.S + t - (kTileKeys - 1), &c->full[kb]);
+              else
+                tma_load_2d(dst, &map_ent, 64 * kb, b * p.N + j * kTileKeys, &c->full[kb]);
+            } else {
+              mbar_arrive(&c->full[kb]);
+            }
           } else {
-            if (lane == 0) tma_load_2d(dst, &map_ent, 64 * kb, b * p.N + j * kTileKeys, &c->full[kb]);
+            gather_kblock(dst, p.ent + (size_t)b * p.N * kD, sidx, 0, lane, kb, &c->full[kb]);
           }
         }
         ++g;
@@ -244,6 +317,43 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       if (!ok) break;
       ++qc;
       __syncwarp();
+    }
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------------------------ gather helpers
+    const int gw = warp - 1;                  // row groups gw, gw+3, ...
+    int qc = 0, g = 0;
+    bool ok = true;
+    while (ok) {
+      const int is = qc & 1;
+      QInfo inf;
+      ok = wait_ok(&c->info_full[is], (qc >> 1) & 1, c, p.status);    // every lane acquires
+      ok = __shfl_sync(0xffffffffu, (int)ok, 0);
+      inf = c->info[is];
+      __syncwarp();
+      mbar_arrive(&c->info_empty[is]);
+      if (inf.done || !ok) break;
+      const bool gathered = p.idx != nullptr;
+      if (!gathered || inf.ent_tiles == 0) mbar_arrive(&c->list_free);
+      const bf16* ent_b = p.ent + (size_t)inf.b * p.N * kD;
+      for (int j = 0; j < inf.tiles && ok; ++j) {
+        const bool window_tile = j == inf.ent_tiles;
+        int sidx[kMaxGroups];
+        if (!window_tile && gathered) {
+          load_rows(list, inf.n_ent, j, gw, lane, sidx);
+          if (j == inf.ent_tiles - 1) mbar_arrive(&c->list_free);
+        }
+        for (int kb = 0; kb < kSlots; ++kb) {
+          if (lane == 0 && g >= 1) ok = wait_ok(&c->empty[kb], (g - 1) & 1, c, p.status);
+          ok = __shfl_sync(0xffffffffu, (int)ok, 0);
+          if (!ok) break;
+          if (window_tile || !gathered)
+            mbar_arrive(&c->full[kb]);
+          else
+            gather_kblock(smem + OFF_SLOT + kb * kSlotBytes, ent_b, sidx, gw, lane, kb, &c->full[kb]);
+        }
+        ++g;
+      }
+      ++qc;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -266,6 +376,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           const uint32_t s_tmem = tmem + 64 * sb;
           for (int kb = 0; kb < kSlots && ok; ++kb) {
             ok = wait_ok(&c->full[kb], g & 1, c, p.status);
+            fence_proxy_async_smem();                 // cp.async writes -> tensor-core reads
             tc_fence_after();
             const uint32_t a0 = smem_u32(smem + OFF_SLOT + kb * kSlotBytes);
             const uint32_t b0 = smem_u32(smem + OFF_Q + kb * kQBlockBytes);
@@ -302,24 +413,28 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int ts = threadIdx.x - 64;          // 0..127
+    const int ts = threadIdx.x - 128;         // 0..127
     const int quarter = warp & 3;             // TMEM lane quarter of this warp
     const int krow = 32 * quarter + lane;     // key row / dim row owned in TMEM
     const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
     const float log2e = 1.4426950408889634f;
     const float c1 = p.scale * log2e;
-    int qc = 0, g = 0;
-    while (true) {
+
+    // Receive query qc's description; returns false when the work is over.
+    auto next_query = [&](int qc, QInfo& inf) -> bool {
       const int is = qc & 1;
       wait_ok(&c->info_full[is], (qc >> 1) & 1, c, p.status);
-      const QInfo inf = c->info[is];
+      inf = c->info[is];
       mbar_arrive(&c->info_empty[is]);
       if (ts == 0) c->decision = (c->abort || inf.done) ? 1 : 0;
       named_bar_sync(1, 128);
-      if (c->decision) break;
-      const int t = inf.t, b = inf.b;
-
-      // rotate the last 64 dims of each head at position t, then head norms
+      const bool more = c->decision == 0;
+      named_bar_sync(1, 128);
+      return more;
+    };
+    // Rotate the last 64 dims of each head of query qc at position t, take
+    // the head norms of the stored bf16 values and publish the shift table.
+    auto setup_query = [&](int qc, const QInfo& inf) {
       wait_ok(&c->q_full, qc & 1, c, p.status);
       const int h = ts >> 1, half = ts & 1;
       uint8_t* qrow = smem + OFF_Q + 7 * kQBlockBytes + h * 128;
@@ -329,22 +444,24 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         uint4* ptr = reinterpret_cast<uint4*>(qrow + ((ch ^ (h & 7)) * 16));
         uint4 u = *ptr;
         __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&u);
+        const float4* csp = reinterpret_cast<const float4*>(p.rope_cs + (size_t)inf.t * (kR / 2) + ch * 4);
+        const float4 cs01 = csp[0], cs23 = csp[1];
+        const float cs[8] = {cs01.x, cs01.y, cs01.z, cs01.w, cs23.x, cs23.y, cs23.z, cs23.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           float2 f = __bfloat1622float2(hv[i]);
-          float cs, sn;
-          rope_cos_sin(t, p.inv_freq[ch * 4 + i], &cs, &sn);
-          rot_pair(f.x, f.y, cs, sn);
+          rot_pair(f.x, f.y, cs[2 * i], cs[2 * i + 1]);
           hv[i] = __floats2bfloat162_rn(f.x, f.y);
         }
         *ptr = u;
       }
+      __syncwarp();
       float ss = 0.f;
       for (int kb = 4 * half; kb < 4 * half + 4; ++kb) {
         const uint4* r = reinterpret_cast<const uint4*>(smem + OFF_Q + kb * kQBlockBytes + h * 128);
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
-          uint4 u = r[cc];
+          uint4 u = r[cc ^ (h & 7)];            // spread the 16 heads of a warp over the banks
           const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -359,15 +476,23 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         float m = p.scale * sqrtf(ss) * inf.kmax;
         m = m * (1.0f + 1e-5f) + 1e-6f;                     // covers rounding of the bound itself
         if (p.sink != nullptr) m = fmaxf(m, p.sink[h]);
-        c->mlog2[h] = m * log2e;
+        c->mlog2[qc & 1][h] = m * log2e;
       }
       fence_proxy_async_smem();
       named_bar_sync(1, 128);
       mbar_arrive(&c->q_ready);
+    };
 
+    int qc = 0, g = 0;
+    QInfo inf;
+    bool more = next_query(0, inf);
+    if (more) setup_query(0, inf);
+    while (more) {
+      const float* mlog2 = c->mlog2[qc & 1];
       float lsum[kH];
 #pragma unroll
       for (int i = 0; i < kH; ++i) lsum[i] = 0.f;
+      const int t = inf.t, b = inf.b;
       const int nk_total = inf.n_ent + (t - inf.w_lo + 1);
       for (int j = 0; j < inf.tiles; ++j) {
         const int sb = g & 1;
@@ -387,8 +512,8 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         uint32_t pk[kH / 2];
 #pragma unroll
         for (int i = 0; i < kH / 2; ++i) {
-          float x0 = valid ? ex2_approx(fmaf(v[2 * i], c1, -c->mlog2[2 * i])) : 0.f;
-          float x1 = valid ? ex2_approx(fmaf(v[2 * i + 1], c1, -c->mlog2[2 * i + 1])) : 0.f;
+          float x0 = valid ? ex2_approx(fmaf(v[2 * i], c1, -mlog2[2 * i])) : 0.f;
+          float x1 = valid ? ex2_approx(fmaf(v[2 * i + 1], c1, -mlog2[2 * i + 1])) : 0.f;
           pk[i] = pack_bf16x2(x0, x1);
           lsum[2 * i] += __uint_as_float(pk[i] << 16);
           lsum[2 * i + 1] += __uint_as_float(pk[i] & 0xFFFF0000u);
@@ -404,7 +529,13 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         ++g;
       }
 
-      // ---- epilogue: denominators, lse, O^T / l, de-rotation, TMA store
+      // the next query's queries go first, so its first products overlap
+      // this query's epilogue
+      QInfo nxt;
+      more = next_query(qc + 1, nxt);
+      if (more) setup_query(qc + 1, nxt);
+
+      // ---- epilogue: denominators, lse, O^T / l, de-rotation, store
       wait_ok(&c->o_full, qc & 1, c, p.status);
       tc_fence_after();
       float* red = reinterpret_cast<float*>(smem + OFF_P);     // both P buffers are idle now
@@ -417,30 +548,41 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       named_bar_sync(1, 128);
       if (ts < kH) {
         float l = red[ts] + red[kH + ts] + red[2 * kH + ts] + red[3 * kH + ts];
-        const float m = c->mlog2[ts] / log2e;
+        const float m = mlog2[ts] * 0.6931471805599453f;
         if (p.sink != nullptr) l += expf(p.sink[ts] - m);
         // too little mass under the bound: exp underflow may have lost keys
         const bool bad = !(l >= (float)nk_total * 1.0e-26f) || !(l < INFINITY);
-        if (bad) atomicOr(&c->redo, 1);
-        c->inv_l[ts] = 1.0f / l;
+        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&c->redo, 1);
+        red[4 * kH + ts] = 1.0f / l;
         if (p.lse) p.lse[((size_t)b * p.S + t) * kH + ts] = m + logf(l);
       }
       named_bar_sync(1, 128);
+      float inv_l[kH];
+#pragma unroll
+      for (int i = 0; i < kH; i += 4) {
+        const float4 v4 = *reinterpret_cast<const float4*>(red + 4 * kH + i);
+        inv_l[i] = v4.x;
+        inv_l[i + 1] = v4.y;
+        inv_l[i + 2] = v4.z;
+        inv_l[i + 3] = v4.w;
+      }
       if (ts == 0 && c->redo) {
         const int slot = atomicAdd(&p.counters[1], 1);
         p.counters[2 + slot] = b * p.S + t;
         c->redo = 0;
       }
-      // de-rotation angle of this thread's dim pair (M-block 3 holds dims 384..511)
+      named_bar_sync(1, 128);                                   // red[] is overwritten below
+      // de-rotation of this thread's dim pair (M-block 3 holds dims 384..511)
       float dc = 1.f, ds = 0.f;
       const int dim3 = 384 + krow;
-      if (dim3 >= kD - kR) rope_cos_sin(t, p.inv_freq[(dim3 - (kD - kR)) >> 1], &dc, &ds);
+      if (dim3 >= kD - kR) {
+        const float2 cs = p.rope_cs[(size_t)t * (kR / 2) + ((dim3 - (kD - kR)) >> 1)];
+        dc = cs.x;
+        ds = cs.y;
+      }
+      bf16* orow = p.o + ((size_t)b * p.S + t) * kH * kD;
       for (int m = 0; m < 4; ++m) {
         uint8_t* stage = smem + OFF_P + (m & 1) * kPBytes;
-        if (m >= 2) {
-          if (ts == 0) tma_store_wait_read<1>();
-          named_bar_sync(1, 128);
-        }
         float v[kH];
         tmem_ld32(tmem + lane_base + 128 + 64 * m, v);
         tmem_ld32(tmem + lane_base + 128 + 64 * m + 32, v + 32);
@@ -450,7 +592,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           mbar_arrive(&c->o_empty);
         }
 #pragma unroll
-        for (int i = 0; i < kH; ++i) v[i] *= c->inv_l[i];
+        for (int i = 0; i < kH; ++i) v[i] *= inv_l[i];
         if (m == 3) {
           const bool odd = lane & 1;
 #pragma unroll
@@ -459,21 +601,23 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             if (dim3 >= kD - kR) v[i] = odd ? (-other * ds + v[i] * dc) : (v[i] * dc + other * ds);
           }
         }
+        // stage as [64 heads][128 dims] bf16, then 16-byte coalesced copies out
         __nv_bfloat16* srow = reinterpret_cast<__nv_bfloat16*>(stage) + krow;
 #pragma unroll
         for (int i = 0; i < kH; ++i) srow[i * 128] = __float2bfloat16_rn(v[i]);
-        fence_proxy_async_smem();
         named_bar_sync(1, 128);
-        if (ts == 0) {
-          tma_store_2d(&map_o, 128 * m, (b * p.S + t) * kH, stage);
-          tma_store_commit();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int cidx = ts + 128 * i;              // 1024 chunks of 16 B
+          const int hh = cidx >> 4, piece = cidx & 15;
+          const uint4 val = *reinterpret_cast<const uint4*>(stage + hh * 256 + piece * 16);
+          *reinterpret_cast<uint4*>(orow + (size_t)hh * kD + 128 * m + piece * 8) = val;
         }
       }
-      if (ts == 0) tma_store_wait_read<0>();
-      named_bar_sync(1, 128);
+      named_bar_sync(1, 128);                                   // staging free for the next P tiles
+      inf = nxt;
       ++qc;
     }
-    if (ts == 0) tma_store_wait_all<0>();
   }
 
   tc_fence_before();
@@ -490,12 +634,12 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
 }  // namespace
 
 cudaError_t launch_mqa_tc(const v4_config& cfg, const void* q, const void* kv_rot, const void* ent,
-                          const int32_t* idx, const float* sink, const float* inv_freq,
+                          const int32_t* idx, const float* sink, const float2* cs_table,
                           const float* kv_norm, const float* ent_norm, void* o, float* lse,
                           int* counters, int* status, cudaStream_t st) {
   const int B = cfg.batch, S = cfg.seqlen;
   const int N = cfg.ratio > 0 ? S / cfg.ratio : 0;
-  CUtensorMap mq, mkv, ment, mentg, mo;
+  CUtensorMap mq, mkv, ment;
   const uint64_t qrows = (uint64_t)B * S * kH;
   int e = 0;
   e |= make_tmap_bf16_2d(&mq, q, kD, qrows, 64, 64, true);
@@ -503,13 +647,14 @@ cudaError_t launch_mqa_tc(const v4_config& cfg, const void* q, const void* kv_ro
   const void* ent_base = (ent != nullptr && N > 0) ? ent : kv_rot;      // unused when there are no entries
   const uint64_t ent_rows = (ent != nullptr && N > 0) ? (uint64_t)B * N : (uint64_t)B * S;
   e |= make_tmap_bf16_2d(&ment, ent_base, kD, ent_rows, 64, kTileKeys, true);
-  e |= make_tmap_bf16_2d(&mentg, ent_base, kD, ent_rows, 64, 1, true);
-  e |= make_tmap_bf16_2d(&mo, o, kD, qrows, 128, 64, false);
   if (e) return cudaErrorInvalidValue;
   Params prm;
+  prm.q = (const bf16*)q;
+  prm.ent = (const bf16*)ent_base;
+  prm.o = (bf16*)o;
   prm.idx = idx;
   prm.sink = sink;
-  prm.inv_freq = inv_freq;
+  prm.rope_cs = cs_table;
   prm.kv_norm = kv_norm;
   prm.ent_norm = ent_norm;
   prm.lse = lse;
@@ -530,9 +675,9 @@ cudaError_t launch_mqa_tc(const v4_config& cfg, const void* q, const void* kv_ro
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int total = B * S;
   const int grid = total < sms ? total : sms;
-  err = cudaMemsetAsync(counters, 0, 2 * sizeof(int), st);
+  err = cudaMemsetAsync(counters + 1, 0, sizeof(int), st);
   if (err != cudaSuccess) return err;
-  mqa_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mq, mkv, ment, mentg, mo, prm);
+  mqa_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mq, mkv, ment, prm);
   note_launch();
   return cudaGetLastError();
 }

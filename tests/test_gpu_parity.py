@@ -101,12 +101,14 @@ def test_indexer_prep(name, p):
         assert rel_l2(np64(out), ref) < FP32_TOL
 
 
+@pytest.mark.parametrize("path", [V.V4_PATH_SIMT, V.V4_PATH_AUTO], ids=["simt", "auto"])
 @pytest.mark.parametrize("name,p", [
     ("tiny_f32", SI.preset("tiny_csa_f32")),
     ("flash_bf16_1k", SI.preset("csa_bf16_4k", S=1024, q_mode="direct")),
     ("flash_bf16_ragged_b2", SI.preset("csa_bf16_4k", S=777, B=2, K=64, q_mode="direct")),
+    ("flash_bf16_3k", SI.preset("csa_bf16_4k", S=3001, q_mode="direct")),
 ])
-def test_indexer_topk_prepared(name, p):
+def test_indexer_topk_prepared(name, p, path):
     # both sides score the same prepared queries and keys (made by the oracle)
     x, xd, f, fd = _setup(p)
     bf = p["dtype"] == "bf16"
@@ -114,7 +116,7 @@ def test_indexer_topk_prepared(name, p):
                       p["overlap"], 1e-6, hadamard=True, store_bf16=bf)
     iqp = O.indexer_query_prep(np64(x["iq"]), f, store_bf16=bf)
     dt = xd["iq"].dtype
-    cfg = V.config_from_preset(p)
+    cfg = V.config_from_preset(p, path=path)
     B, S, K = p["B"], p["S"], p["K"]
     idx = torch.empty(B, S, K, dtype=torch.int32, device="cuda")
     isc = torch.empty(B, S, K, dtype=torch.float32, device="cuda")
