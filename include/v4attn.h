@@ -188,6 +188,28 @@ v4_status v4_sparse_mqa_fwd(const v4_config* cfg, const void* q, const void* kv,
                             void* workspace, size_t ws_bytes, void* stream);
 
 /* ----------------------------------------------------------------------
+ * v4_sparse_mqa_fwd without a workspace: the method has no counterpart for
+ * this entry point; it exists for callers that cannot allocate device memory
+ * where they run the attention (a serving stack whose planner owns all
+ * device memory up front, a plugin that may not call cudaMalloc inside a
+ * host framework, a latency-critical path that cannot absorb an
+ * allocation).  Arguments and results are those of v4_sparse_mqa_fwd.
+ *
+ * Scratch comes from one library-owned device array of about 10 MiB, held by
+ * every GPU that loads the library until the process exits.  Limits:
+ * batch*seqlen <= 8192, batch*seqlen*head_dim*element size <= 8 MiB and
+ * seqlen*rope_dim <= 524288; larger problems return V4_ERR_INVALID_ARG with
+ * a message.  The call allocates nothing.  The first call on a device looks
+ * up the array's device address (cudaGetSymbolAddress, with that device
+ * current), so make that first call before any stream capture.  All calls
+ * share the array and it keeps the last call's contents: calls that overlap
+ * on the GPU (unordered streams, several host threads) race on it.
+ * --------------------------------------------------------------------*/
+v4_status v4_sparse_mqa_fwd_noalloc(const v4_config* cfg, const void* q, const void* kv,
+                                    const void* ent, const int32_t* idx, const float* sink,
+                                    const float* inv_freq, void* o, float* lse, void* stream);
+
+/* ----------------------------------------------------------------------
  * Grouped low-rank output projection.  [BLOG] "The DeepSeek-V4-Flash
  * architecture": the 64 x 512 output splits into o_groups groups, each
  * through an o_rank bottleneck.  Group g holds heads g*H/G .. (g+1)*H/G-1

@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "V4_OK", 1: "V4_ERR_INVALID_ARG", 2: "V4_ERR_UNSUPPORTED", 3:
 EXPORTS = ["v4_rope_inv_freq", "v4_workspace_size", "v4_compress", "v4_indexer_prep",
            "v4_indexer_topk", "v4_sparse_mqa_fwd", "v4_grouped_o_proj", "v4_attn_layer_fwd",
            "v4_last_error", "v4_get_device_status", "v4_reset_device_status", "v4_launch_count",
-           "v4_profile_enable", "v4_profile_count", "v4_profile_get"]
+           "v4_profile_enable", "v4_profile_count", "v4_profile_get", "v4_sparse_mqa_fwd_noalloc"]
 PROFILE_KINDS = {0: "compress", 1: "window_rotate", 2: "indexer_prep", 3: "indexer_scores", 4: "topk",
                  5: "attention", 6: "o_proj"}
 
@@ -76,6 +76,7 @@ def lib(path=None):
         "v4_indexer_prep": [cfgp, vp, vp, vp, vp],
         "v4_indexer_topk": [cfgp, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp],
         "v4_sparse_mqa_fwd": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
+        "v4_sparse_mqa_fwd_noalloc": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
         "v4_grouped_o_proj": [cfgp, vp, vp, vp, vp],
         "v4_attn_layer_fwd": [cfgp, C.POINTER(v4_layer_inputs), C.POINTER(v4_layer_outputs), vp, sz, vp],
         "v4_get_device_status": [vp, C.POINTER(i32)],
@@ -198,6 +199,19 @@ def v4_sparse_mqa_fwd(cfg, q, kv, ent, idx, sink, inv_freq, o, lse, workspace, s
                                    _ptr(o, "o", dt), _ptr(lse, "lse", torch.float32, optional=True),
                                    _ptr(workspace, "workspace", torch.uint8), workspace.numel(),
                                    _stream(stream)))
+    return o
+
+
+def v4_sparse_mqa_fwd_noalloc(cfg, q, kv, ent, idx, sink, inv_freq, o, lse, stream=None):
+    """v4_sparse_mqa_fwd with library-owned scratch (no workspace argument)."""
+    dt = _storage(cfg)
+    _check(lib().v4_sparse_mqa_fwd_noalloc(C.byref(cfg), _ptr(q, "q", dt), _ptr(kv, "kv", dt),
+                                           _ptr(ent, "ent", dt, optional=True),
+                                           _ptr(idx, "idx", torch.int32, optional=True),
+                                           _ptr(sink, "sink", torch.float32, optional=True),
+                                           _ptr(inv_freq, "inv_freq", torch.float32),
+                                           _ptr(o, "o", dt), _ptr(lse, "lse", torch.float32, optional=True),
+                                           _stream(stream)))
     return o
 
 

@@ -278,6 +278,11 @@ static v4_status do_mqa(const v4_config& c, const void* q, const void* kv, const
   return V4_OK;
 }
 
+// Accessors for other translation units of the library.
+v4_status validate_config(const v4_config* c) { return check_cfg(c); }
+v4_status set_error(v4_status st, const char* msg) { return fail(st, "%s", msg); }
+int* device_status_ptr() { return status_ptr(); }
+
 }  // namespace v4
 
 using namespace v4;

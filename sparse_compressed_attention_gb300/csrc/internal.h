@@ -14,6 +14,11 @@ namespace v4 {
 // Counts kernel launches made by the library (reported by v4_launch_count).
 void note_launch(int n = 1);
 
+// Argument checks, error text and the device status word (api.cu).
+v4_status validate_config(const v4_config* c);
+v4_status set_error(v4_status st, const char* msg);
+int* device_status_ptr();
+
 // Workspace carve-up for one configuration.  Offsets are 256-byte aligned.
 struct Workspace {
   size_t kv_rot = 0, kv_rot_bytes = 0;     // rotated window keys [B,S,D]
