@@ -63,6 +63,27 @@ def layer_work(p):
                 idx_flops=idx_flops, idx_pairs=idx_pairs * B)
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch at
+# S=16384, from the ncu capture summarised in profiles/dram_traffic_s16384.md.
+# A figure is reported only while its kernel source is unchanged (sha256).
+NCU_TRAFFIC = {
+    "csa_attention": ("mqa_tc.cu", "a689d0f5330de780b5295c7c0cbc27d98f723eb9be288966fa52f75131138ad0", 2162458880),
+    "hca_attention": ("mqa_tc.cu", "a689d0f5330de780b5295c7c0cbc27d98f723eb9be288966fa52f75131138ad0", 2120372992),
+    "csa_indexer": ("indexer_tc.cu", "1590624bd98a7b0e06ee2c59fbc95e8cbb3e7a448f92f6d5b9ee4cfc7c7f5f4e", 399407872),
+}
+
+
+def ncu_traffic(key, seq):
+    import hashlib
+    src, sha, val = NCU_TRAFFIC[key]
+    path = os.path.join(ROOT, "sparse_compressed_attention_gb300", "csrc", src)
+    try:
+        cur = hashlib.sha256(open(path, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return val if (cur == sha and seq == 16384) else None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -285,7 +306,8 @@ def run_ours(args):
         achieved = work["csa_bf16_16k"]["attn_flops"] / (a_ms / 1e3) / 1e12
         roof = {"kernel": "csa attention (sparse MQA, 64 heads x 512, top-512 + window 128)",
                 "bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16"],
-                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4), "traffic": None,
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4),
+                "traffic": ncu_traffic("csa_attention", S),
                 "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % peaks["src"],
                 "flops_per_launch": work["csa_bf16_16k"]["attn_flops"], "avg_launch_ms": round(a_ms, 4)}
     extra_roofs = []
@@ -294,6 +316,7 @@ def run_ours(args):
         gbs = work["hca_bf16_16k"]["attn_bytes"] / (a_ms / 1e3) / 1e9
         extra_roofs.append({"kernel": "hca attention", "bound": "hbm", "achieved": round(gbs, 1),
                             "peak": peaks["hbm"], "unit": "GB/s", "frac": round(gbs / peaks["hbm"], 4),
+                            "traffic": ncu_traffic("hca_attention", S),
                             "bytes_per_launch": work["hca_bf16_16k"]["attn_bytes"],
                             "avg_launch_ms": round(a_ms, 4)})
     isc = per.get(("csa_bf16_16k", "indexer_scores"), [])
@@ -302,6 +325,7 @@ def run_ours(args):
         tf = work["csa_bf16_16k"]["idx_flops"] / (a_ms / 1e3) / 1e12
         extra_roofs.append({"kernel": "csa indexer scores", "bound": "tensor", "achieved": round(tf, 2),
                             "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": round(tf / peaks["bf16"], 4),
+                            "traffic": ncu_traffic("csa_indexer", S),
                             "flops_per_launch": work["csa_bf16_16k"]["idx_flops"],
                             "avg_launch_ms": round(a_ms, 4)})
 
@@ -415,13 +439,20 @@ def gather_oracle_inputs(layers, rows_per_layer):
 
 
 def cpu_baseline(args, layers):
-    inputs = gather_oracle_inputs(layers, args.cpu_rows)
-    est, spent = oracle_sample(inputs, args.cpu_rows)
+    """Oracle time on a sample sized to roughly 10-30 s of CPU work: the row
+    count doubles until one sample takes at least --cpu-seconds."""
     S = layers[0]["p"]["S"]
+    rows = args.cpu_rows
+    while True:
+        inputs = gather_oracle_inputs(layers, rows)
+        est, spent = oracle_sample(inputs, rows)
+        if spent >= args.cpu_seconds or rows >= S:
+            break
+        rows = min(S, rows * 2)
     return {"value": round(S / est, 2), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": "numpy float64 oracle: full compressors of both layers + indexer/attention for "
                       "%d evenly spaced query rows per layer, extrapolated to S=%d (%.1f s of CPU work)"
-                      % (args.cpu_rows, S, spent)}
+                      % (rows, S, spent)}
 
 
 # ---------------------------------------------------------------------------
@@ -477,7 +508,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--seq", type=int, default=16384)
     ap.add_argument("--e2e-steps", type=int, default=3)
-    ap.add_argument("--cpu-rows", type=int, default=24)
+    ap.add_argument("--cpu-rows", type=int, default=64)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-rows", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -139,6 +139,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(128, 256, 0, 0);
+      const uint64_t dA0 = smem_desc(smem_u32(smem + OFF_A), 16, 1024, kLayoutSW128);
+      const uint64_t dB0 = smem_desc(smem_u32(smem + OFF_B), 16, 1024, kLayoutSW128);
       int gq = 0, st = 0, use = 0, tile_ct = 0;
       bool ok = true;
       for (int gi = blockIdx.x; gi < total && ok; gi += gridDim.x) {
@@ -153,14 +155,13 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           tc_fence_after();
           if (!ok) break;
           const uint32_t d = tmem + 256 * ab;
+          const uint64_t dA = dA0 + (uint64_t)((st * kAStage) >> 4);
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb) {
-            const uint32_t a0 = smem_u32(smem + OFF_A + st * kAStage + kb * kABlock);
-            const uint32_t b0 = smem_u32(smem + OFF_B + kb * kBBlock);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-              umma_f16_ss(d, smem_desc(a0 + 32 * ks, 16, 1024, kLayoutSW128),
-                          smem_desc(b0 + 32 * ks, 16, 1024, kLayoutSW128), idesc, (kb | ks) != 0);
+              umma_f16_ss(d, dA + (uint64_t)((kb * kABlock + 32 * ks) >> 4),
+                          dB0 + (uint64_t)((kb * kBBlock + 32 * ks) >> 4), idesc, (kb | ks) != 0);
           }
           umma_commit(&c->a_empty[st]);
           umma_commit(&c->acc_full[ab]);

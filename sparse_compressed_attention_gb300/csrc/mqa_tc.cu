@@ -104,21 +104,24 @@ __device__ __forceinline__ bool wait_ok(uint64_t* bar, uint32_t parity, Ctl* c, 
   return mbar_wait(bar, parity, &c->abort, status);
 }
 
-// Row groups (4 rows each) of a 128-key tile handled by gather warp gw:
-// groups gw, gw+3, ... (11, 11 and 10 groups).
+// Row groups (4 rows each) of a 128-key tile: with nw gathering warps, warp
+// gw takes groups gw, gw+nw, ... (three warps: at most 11 groups each).
+// Adding the softmax warps as gatherers did not speed the gather: with one
+// tile of slots per SM the rate is bounded by bytes in flight over the L2
+// latency, not by issue.
 constexpr int kMaxGroups = 11;
 
 // Gather one K-block (64 dims) of the selected entries of a tile: lane
 // covers row 4*grp + lane/8, 16-byte chunk lane%8, written into the
 // 128-byte-swizzled K-major slot layout; one arrival when the copies land.
-__device__ __forceinline__ void gather_kblock(uint8_t* slot, const bf16* ent_b, const int* sidx, int gw, int lane,
-                                              int kb, uint64_t* full) {
+__device__ __forceinline__ void gather_kblock(uint8_t* slot, const bf16* ent_b, const int* sidx, int gw, int nw,
+                                              int lane, int kb, uint64_t* full) {
   const int chunk = lane & 7;
   const bf16* src = ent_b + kb * 64 + chunk * 8;
   const uint32_t d0 = smem_u32(slot);
 #pragma unroll
   for (int i = 0; i < kMaxGroups; ++i) {
-    const int grp = gw + 3 * i;
+    const int grp = gw + nw * i;
     if (grp < 32) {
       const int row = 4 * grp + (lane >> 3);
       cp_async_16(d0 + row * 128 + ((chunk ^ (row & 7)) << 4), src + (size_t)sidx[i] * kD);
@@ -127,12 +130,13 @@ __device__ __forceinline__ void gather_kblock(uint8_t* slot, const bf16* ent_b, 
   cp_async_mbar_arrive(full);
 }
 
-// Selection-list rows of tile j for gather warp gw (row 0 pads short tiles).
-__device__ __forceinline__ void load_rows(const int* list, int n_ent, int j, int gw, int lane, int* sidx) {
+// Selection-list rows of tile j for gather warp gw of nw (row 0 pads short tiles).
+__device__ __forceinline__ void load_rows(const int* list, int n_ent, int j, int gw, int nw, int lane, int* sidx) {
 #pragma unroll
   for (int i = 0; i < kMaxGroups; ++i) {
-    const int k = j * 128 + 4 * (gw + 3 * i) + (lane >> 3);
-    sidx[i] = (gw + 3 * i < 32 && k < n_ent) ? list[k] : 0;
+    const int grp = gw + nw * i;
+    const int k = j * 128 + 4 * grp + (lane >> 3);
+    sidx[i] = (grp < 32 && k < n_ent) ? list[k] : 0;
   }
 }
 
@@ -292,7 +296,8 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       for (int j = 0; j < inf.tiles && ok; ++j) {
         const bool window_tile = j == inf.ent_tiles;
         int sidx[kMaxGroups];
-        if (!window_tile && p.idx != nullptr) load_rows(list, n_ent, j, 0, lane, sidx);
+        const int nw = 3;
+        if (!window_tile && p.idx != nullptr) load_rows(list, n_ent, j, 0, nw, lane, sidx);
         for (int kb = 0; kb < kSlots; ++kb) {
           if (lane == 0 && g >= 1) ok = wait_ok(&c->empty[kb], (g - 1) & 1, c, p.status);
           ok = __shfl_sync(0xffffffffu, (int)ok, 0);
@@ -309,7 +314,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
               mbar_arrive(&c->full[kb]);
             }
           } else {
-            gather_kblock(dst, p.ent + (size_t)b * p.N * kD, sidx, 0, lane, kb, &c->full[kb]);
+            gather_kblock(dst, p.ent + (size_t)b * p.N * kD, sidx, 0, nw, lane, kb, &c->full[kb]);
           }
         }
         ++g;
@@ -338,8 +343,9 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       for (int j = 0; j < inf.tiles && ok; ++j) {
         const bool window_tile = j == inf.ent_tiles;
         int sidx[kMaxGroups];
+        const int nw = 3;
         if (!window_tile && gathered) {
-          load_rows(list, inf.n_ent, j, gw, lane, sidx);
+          load_rows(list, inf.n_ent, j, gw, nw, lane, sidx);
           if (j == inf.ent_tiles - 1) mbar_arrive(&c->list_free);
         }
         for (int kb = 0; kb < kSlots; ++kb) {
@@ -349,7 +355,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           if (window_tile || !gathered)
             mbar_arrive(&c->full[kb]);
           else
-            gather_kblock(smem + OFF_SLOT + kb * kSlotBytes, ent_b, sidx, gw, lane, kb, &c->full[kb]);
+            gather_kblock(smem + OFF_SLOT + kb * kSlotBytes, ent_b, sidx, gw, nw, lane, kb, &c->full[kb]);
         }
         ++g;
       }
@@ -360,6 +366,12 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     if (lane == 0) {
       const uint32_t id1 = idesc_bf16_f32(128, 64, 0, 0);
       const uint32_t id2 = idesc_bf16_f32(128, 64, 1, 1);
+      // descriptors are affine in the start address (14-bit field, no carry
+      // below 256 KB): build the bases once, add byte offsets >> 4 per MMA
+      const uint64_t dA1 = smem_desc(smem_u32(smem + OFF_SLOT), 16, 1024, kLayoutSW128);
+      const uint64_t dQ = smem_desc(smem_u32(smem + OFF_Q), 16, 1024, kLayoutSW128);
+      const uint64_t dA2 = smem_desc(smem_u32(smem + OFF_SLOT), kSlotBytes, 1024, kLayoutSW128);
+      const uint64_t dP0 = smem_desc(smem_u32(smem + OFF_P), 128, 2048, kLayoutNone);
       int qc = 0, g = 0;
       bool ok = true;
       while (ok) {
@@ -374,16 +386,15 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         for (int j = 0; j < inf.tiles && ok; ++j) {
           const int sb = g & 1;
           const uint32_t s_tmem = tmem + 64 * sb;
-          for (int kb = 0; kb < kSlots && ok; ++kb) {
-            ok = wait_ok(&c->full[kb], g & 1, c, p.status);
+#pragma unroll
+          for (int kb = 0; kb < kSlots; ++kb) {
+            ok = ok && wait_ok(&c->full[kb], g & 1, c, p.status);
             fence_proxy_async_smem();                 // cp.async writes -> tensor-core reads
             tc_fence_after();
-            const uint32_t a0 = smem_u32(smem + OFF_SLOT + kb * kSlotBytes);
-            const uint32_t b0 = smem_u32(smem + OFF_Q + kb * kQBlockBytes);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-              umma_f16_ss(s_tmem, smem_desc(a0 + 32 * ks, 16, 1024, kLayoutSW128),
-                          smem_desc(b0 + 32 * ks, 16, 1024, kLayoutSW128), id1, (kb | ks) != 0);
+              umma_f16_ss(s_tmem, dA1 + (uint64_t)((kb * kSlotBytes + 32 * ks) >> 4),
+                          dQ + (uint64_t)((kb * kQBlockBytes + 32 * ks) >> 4), id1, (kb | ks) != 0);
           }
           umma_commit(&c->s_full[sb]);
           if (j == inf.tiles - 1) umma_commit(&c->q_empty);
@@ -391,13 +402,13 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           ok = wait_ok(&c->p_ready[sb], (g >> 1) & 1, c, p.status);
           if (ok && j == 0 && qc >= 1) ok = wait_ok(&c->o_empty, (qc - 1) & 1, c, p.status);
           tc_fence_after();
-          const uint32_t pb = smem_u32(smem + OFF_P + sb * kPBytes);
+          const uint64_t dP = dP0 + (uint64_t)((sb * kPBytes) >> 4);
+#pragma unroll
           for (int m = 0; m < 4; ++m) {
-            const uint32_t a0 = smem_u32(smem + OFF_SLOT + (2 * m) * kSlotBytes);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-              umma_f16_ss(tmem + 128 + 64 * m, smem_desc(a0 + 2048 * ks, kSlotBytes, 1024, kLayoutSW128),
-                          smem_desc(pb + 256 * ks, 128, 2048, kLayoutNone), id2, (j > 0 || ks > 0) ? 1u : 0u);
+              umma_f16_ss(tmem + 128 + 64 * m, dA2 + (uint64_t)((2 * m * kSlotBytes + 2048 * ks) >> 4),
+                          dP + (uint64_t)((256 * ks) >> 4), id2, (j > 0 || ks > 0) ? 1u : 0u);
             umma_commit(&c->empty[2 * m]);
             umma_commit(&c->empty[2 * m + 1]);
           }
