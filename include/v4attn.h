@@ -215,7 +215,8 @@ v4_status v4_sparse_mqa_fwd_noalloc(const v4_config* cfg, const void* q, const v
  * through an o_rank bottleneck.  Group g holds heads g*H/G .. (g+1)*H/G-1
  * concatenated along D.
  *   o    : [B, S, H, D];  wo_a : [G, (H/G)*D, o_rank];  y : [B, S, G*o_rank].
- * bf16 storage only.
+ * bf16 storage; (H/G)*D a multiple of 64 and o_rank a multiple of 256 (other
+ * shapes return V4_ERR_UNSUPPORTED).  fp32 accumulation, bf16 result.
  * --------------------------------------------------------------------*/
 v4_status v4_grouped_o_proj(const v4_config* cfg, const void* o, const void* wo_a,
                             void* y, void* stream);

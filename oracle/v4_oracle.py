@@ -414,8 +414,9 @@ def grouped_wo_a(o, wo_a, store_bf16=False):
     o = np.asarray(o, dtype=F64)
     B, T, H, D = o.shape
     G, gin, rank = wo_a.shape
-    x = o.reshape(B, T, G, gin)
-    y = np.einsum("btgi,gir->btgr", x, np.asarray(wo_a, dtype=F64))
+    x = o.reshape(B * T, G, gin)
+    w = np.asarray(wo_a, dtype=F64)
+    y = np.stack([x[:, g, :] @ w[g] for g in range(G)], axis=1)      # [B*T, G, rank]
     return maybe_bf16(y.reshape(B, T, G * rank), store_bf16)
 
 

@@ -391,12 +391,33 @@ v4_status v4_sparse_mqa_fwd(const v4_config* cfg, const void* q, const void* kv,
                 (char*)workspace, (cudaStream_t)stream, false);
 }
 
+static v4_status check_oproj(const v4_config& c) {
+  if (c.o_groups < 1 || c.n_heads % c.o_groups) return fail(V4_ERR_INVALID_ARG, "o_groups must divide n_heads");
+  if (c.o_rank < 1) return fail(V4_ERR_INVALID_ARG, "o_rank must be >= 1");
+  if (!oproj_tc_supported(c))
+    return fail(V4_ERR_UNSUPPORTED,
+                "grouped projection needs bf16, (n_heads/o_groups)*head_dim a multiple of 64, o_rank a multiple of 256");
+  return V4_OK;
+}
+
+static v4_status do_oproj(const v4_config& c, const void* o, const void* wo_a, void* y, cudaStream_t st) {
+  int* status = status_ptr();
+  if (!status) return fail(V4_ERR_CUDA, "device status word unavailable");
+  ProfScope ps(K_OPROJ, st);
+  CU(launch_oproj_tc(c, o, wo_a, y, status, st), "grouped projection kernel");
+  return V4_OK;
+}
+
 v4_status v4_grouped_o_proj(const v4_config* cfg, const void* o, const void* wo_a, void* y,
                             void* stream) {
   v4_status s = check_cfg(cfg);
   if (s != V4_OK) return s;
-  (void)o; (void)wo_a; (void)y; (void)stream;
-  return fail(V4_ERR_UNSUPPORTED, "grouped output projection not built yet");
+  s = check_oproj(*cfg);
+  if (s != V4_OK) return s;
+  REQ(o, "o");
+  REQ(wo_a, "wo_a");
+  REQ(y, "y");
+  return do_oproj(*cfg, o, wo_a, y, (cudaStream_t)stream);
 }
 
 v4_status v4_attn_layer_fwd(const v4_config* cfg, const v4_layer_inputs* in, v4_layer_outputs* out,
@@ -433,7 +454,12 @@ v4_status v4_attn_layer_fwd(const v4_config* cfg, const v4_layer_inputs* in, v4_
       OPT(out->ikey, "ikey");
     }
   }
-  if (in->wo_a) return fail(V4_ERR_UNSUPPORTED, "grouped output projection not built yet");
+  if (in->wo_a) {
+    REQ(in->wo_a, "wo_a");
+    REQ(out->y, "y");
+    s = check_oproj(c);
+    if (s != V4_OK) return s;
+  }
   if (c.path == V4_PATH_TC && !mqa_tc_supported(c))
     return fail(V4_ERR_UNSUPPORTED, "tensor-core attention needs bf16, H=64, D=512, R=64, 1 <= W <= 128, K <= 512");
   s = check_ws(c, workspace, ws_bytes);
@@ -459,8 +485,10 @@ v4_status v4_attn_layer_fwd(const v4_config* cfg, const v4_layer_inputs* in, v4_
     s = do_indexer(c, in->iq, 0, ikey, in->w, in->inv_freq, idx, out->iscore, ws, st, true);
     if (s != V4_OK) return s;
   }
-  return do_mqa(c, in->q, in->kv, comp ? ent : nullptr, sel ? idx : nullptr, in->sink, in->inv_freq,
-                out->o, out->lse, ws, st, true);
+  s = do_mqa(c, in->q, in->kv, comp ? ent : nullptr, sel ? idx : nullptr, in->sink, in->inv_freq, out->o,
+             out->lse, ws, st, true);
+  if (s != V4_OK || !in->wo_a) return s;
+  return do_oproj(c, out->o, in->wo_a, out->y, st);
 }
 
 const char* v4_last_error(void) { return g_err.c_str(); }

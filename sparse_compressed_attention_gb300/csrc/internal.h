@@ -71,6 +71,11 @@ cudaError_t launch_mqa_simt(const v4_config& c, const void* q, const void* kv_ro
                             const float* inv_freq, void* o, float* lse, int* status,
                             const int* list, cudaStream_t st);
 bool mqa_tc_supported(const v4_config& c);
+
+// ---- grouped output projection (oproj_tc.cu)
+bool oproj_tc_supported(const v4_config& c);
+cudaError_t launch_oproj_tc(const v4_config& c, const void* o, const void* wo_a, void* y, int* status,
+                            cudaStream_t st);
 cudaError_t launch_mqa_tc(const v4_config& c, const void* q, const void* kv_rot, const void* ent,
                           const int32_t* idx, const float* sink, const float2* cs_table,
                           const float* kv_norm, const float* ent_norm, void* o, float* lse,

@@ -20,7 +20,10 @@
 // The key tile in shared memory (8 K-blocks of [128 keys x 64 dims], 128-byte
 // swizzle) is the K-major A operand of the first product and, read as
 // MN-major, the A operand of the second.  TMEM: S^T double buffer (2 x 64
-// columns) and O^T (256 columns).  Contiguous key tiles (window rows, HCA
+// columns), O^T (256 columns) and the softmax denominators (64 columns:
+// l = ones[128 x keys] . P^T, an extra M=128 MMA whose A operand is one
+// 128-byte all-ones core matrix read with zero strides, so l sums exactly the
+// bf16 P the output uses).  Contiguous key tiles (window rows, HCA
 // entries) and the query rows arrive by TMA boxes; selected entries are
 // gathered row by row with 16-byte cp.async (many small TMA gathers would
 // serialise in the TMA unit).  The output leaves through shared-memory
@@ -81,7 +84,8 @@ struct Ctl {
   int redo;
 };
 
-constexpr uint32_t kSmemBytes = OFF_CTL + sizeof(Ctl);
+constexpr uint32_t OFF_ONES = (OFF_CTL + sizeof(Ctl) + 127) & ~127u;   // 8 x 8 bf16 ones
+constexpr uint32_t kSmemBytes = OFF_ONES + 128;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Params {
@@ -169,6 +173,11 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     c->abort = 0;
     c->redo = 0;
     fence_barrier_init();
+  }
+  if (threadIdx.x < 8) {
+    const uint32_t one2 = 0x3F803F80u;                  // two bf16 1.0
+    reinterpret_cast<uint4*>(smem + OFF_ONES)[threadIdx.x] = make_uint4(one2, one2, one2, one2);
+    fence_proxy_async_smem();
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&map_q);
@@ -372,6 +381,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       const uint64_t dQ = smem_desc(smem_u32(smem + OFF_Q), 16, 1024, kLayoutSW128);
       const uint64_t dA2 = smem_desc(smem_u32(smem + OFF_SLOT), kSlotBytes, 1024, kLayoutSW128);
       const uint64_t dP0 = smem_desc(smem_u32(smem + OFF_P), 128, 2048, kLayoutNone);
+      const uint64_t dOnes = smem_desc(smem_u32(smem + OFF_ONES), 0, 0, kLayoutNone);   // one core matrix, reused
       int qc = 0, g = 0;
       bool ok = true;
       while (ok) {
@@ -412,6 +422,10 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             umma_commit(&c->empty[2 * m]);
             umma_commit(&c->empty[2 * m + 1]);
           }
+          // denominators: every TMEM lane of columns 384..447 gets sum_k P^T[k, h]
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            umma_f16_ss(tmem + 384, dOnes, dP + (uint64_t)((256 * ks) >> 4), id2, (j > 0 || ks > 0) ? 1u : 0u);
           ++g;
         }
         umma_commit(&c->o_full);
@@ -467,8 +481,10 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         *ptr = u;
       }
       __syncwarp();
-      float ss = 0.f;
-      for (int kb = 4 * half; kb < 4 * half + 4; ++kb) {
+      float ss4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const int kb = 4 * half + kk;
         const uint4* r = reinterpret_cast<const uint4*>(smem + OFF_Q + kb * kQBlockBytes + h * 128);
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
@@ -477,11 +493,12 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             float2 f = __bfloat1622float2(hv[i]);
-            ss = fmaf(f.x, f.x, ss);
-            ss = fmaf(f.y, f.y, ss);
+            ss4[i] = fmaf(f.x, f.x, ss4[i]);
+            ss4[i] = fmaf(f.y, f.y, ss4[i]);
           }
         }
       }
+      float ss = (ss4[0] + ss4[1]) + (ss4[2] + ss4[3]);
       ss += __shfl_xor_sync(0xffffffffu, ss, 1);
       if (half == 0) {
         float m = p.scale * sqrtf(ss) * inf.kmax;
@@ -500,9 +517,6 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     if (more) setup_query(0, inf);
     while (more) {
       const float* mlog2 = c->mlog2[qc & 1];
-      float lsum[kH];
-#pragma unroll
-      for (int i = 0; i < kH; ++i) lsum[i] = 0.f;
       const int t = inf.t, b = inf.b;
       const int nk_total = inf.n_ent + (t - inf.w_lo + 1);
       for (int j = 0; j < inf.tiles; ++j) {
@@ -526,8 +540,6 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           float x0 = valid ? ex2_approx(fmaf(v[2 * i], c1, -mlog2[2 * i])) : 0.f;
           float x1 = valid ? ex2_approx(fmaf(v[2 * i + 1], c1, -mlog2[2 * i + 1])) : 0.f;
           pk[i] = pack_bf16x2(x0, x1);
-          lsum[2 * i] += __uint_as_float(pk[i] << 16);
-          lsum[2 * i + 1] += __uint_as_float(pk[i] & 0xFFFF0000u);
         }
         uint8_t* prow = smem + OFF_P + sb * kPBytes + krow * 16;
 #pragma unroll
@@ -547,42 +559,6 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       if (more) setup_query(qc + 1, nxt);
 
       // ---- epilogue: denominators, lse, O^T / l, de-rotation, store
-      wait_ok(&c->o_full, qc & 1, c, p.status);
-      tc_fence_after();
-      float* red = reinterpret_cast<float*>(smem + OFF_P);     // both P buffers are idle now
-#pragma unroll
-      for (int i = 0; i < kH; ++i) {
-        float x = lsum[i];
-        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-        if (lane == 0) red[quarter * kH + i] = x;
-      }
-      named_bar_sync(1, 128);
-      if (ts < kH) {
-        float l = red[ts] + red[kH + ts] + red[2 * kH + ts] + red[3 * kH + ts];
-        const float m = mlog2[ts] * 0.6931471805599453f;
-        if (p.sink != nullptr) l += expf(p.sink[ts] - m);
-        // too little mass under the bound: exp underflow may have lost keys
-        const bool bad = !(l >= (float)nk_total * 1.0e-26f) || !(l < INFINITY);
-        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&c->redo, 1);
-        red[4 * kH + ts] = 1.0f / l;
-        if (p.lse) p.lse[((size_t)b * p.S + t) * kH + ts] = m + logf(l);
-      }
-      named_bar_sync(1, 128);
-      float inv_l[kH];
-#pragma unroll
-      for (int i = 0; i < kH; i += 4) {
-        const float4 v4 = *reinterpret_cast<const float4*>(red + 4 * kH + i);
-        inv_l[i] = v4.x;
-        inv_l[i + 1] = v4.y;
-        inv_l[i + 2] = v4.z;
-        inv_l[i + 3] = v4.w;
-      }
-      if (ts == 0 && c->redo) {
-        const int slot = atomicAdd(&p.counters[1], 1);
-        p.counters[2 + slot] = b * p.S + t;
-        c->redo = 0;
-      }
-      named_bar_sync(1, 128);                                   // red[] is overwritten below
       // de-rotation of this thread's dim pair (M-block 3 holds dims 384..511)
       float dc = 1.f, ds = 0.f;
       const int dim3 = 384 + krow;
@@ -591,9 +567,59 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         dc = cs.x;
         ds = cs.y;
       }
-      bf16* orow = p.o + ((size_t)b * p.S + t) * kH * kD;
+      wait_ok(&c->o_full, qc & 1, c, p.status);
+      tc_fence_after();
+      // per-head scalars, one head per thread; the P buffers are idle here
+      float* hs = reinterpret_cast<float*>(smem + OFF_P);        // [0,64) l, [64,128) 1/l
+      if (ts < 32) {
+        float lv[32];
+        tmem_ld32(tmem + lane_base + 384, lv);                   // every lane holds l_h in column h
+        tmem_wait_ld();
+        if (ts == 0) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(hs + i) = make_float4(lv[i], lv[i + 1], lv[i + 2], lv[i + 3]);
+        }
+      } else if (ts < 64) {
+        float lv[32];
+        tmem_ld32(tmem + lane_base + 384 + 32, lv);
+        tmem_wait_ld();
+        if (ts == 32) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(hs + 32 + i) = make_float4(lv[i], lv[i + 1], lv[i + 2], lv[i + 3]);
+        }
+      }
+      named_bar_sync(1, 128);
+      if (ts < kH) {
+        float l = hs[ts];
+        const float m = mlog2[ts] * 0.6931471805599453f;
+        if (p.sink != nullptr) l += expf(p.sink[ts] - m);
+        // too little mass under the bound: exp underflow may have lost keys
+        const bool bad = !(l >= (float)nk_total * 1.0e-26f) || !(l < INFINITY);
+        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&c->redo, 1);
+        if (p.lse) p.lse[((size_t)b * p.S + t) * kH + ts] = m + logf(l);
+        hs[kH + ts] = 1.0f / l;
+      }
+      named_bar_sync(1, 128);
+      if (ts == 0 && c->redo) {                 // queue the query once for the running-max kernel
+        const int slot = atomicAdd(&p.counters[1], 1);
+        p.counters[2 + slot] = b * p.S + t;
+        c->redo = 0;
+      }
+      float inv_l[kH];
+#pragma unroll
+      for (int i = 0; i < kH; i += 4) {
+        const float4 v4 = *reinterpret_cast<const float4*>(hs + kH + i);
+        inv_l[i] = v4.x;
+        inv_l[i + 1] = v4.y;
+        inv_l[i + 2] = v4.z;
+        inv_l[i + 3] = v4.w;
+      }
+      // o[t, h, 128m + krow]: for each head the 32 lanes of a warp write 64
+      // contiguous bytes
+      bf16* obase = p.o + ((size_t)b * p.S + t) * kH * kD + krow;
       for (int m = 0; m < 4; ++m) {
-        uint8_t* stage = smem + OFF_P + (m & 1) * kPBytes;
         float v[kH];
         tmem_ld32(tmem + lane_base + 128 + 64 * m, v);
         tmem_ld32(tmem + lane_base + 128 + 64 * m + 32, v + 32);
@@ -612,20 +638,10 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             if (dim3 >= kD - kR) v[i] = odd ? (-other * ds + v[i] * dc) : (v[i] * dc + other * ds);
           }
         }
-        // stage as [64 heads][128 dims] bf16, then 16-byte coalesced copies out
-        __nv_bfloat16* srow = reinterpret_cast<__nv_bfloat16*>(stage) + krow;
 #pragma unroll
-        for (int i = 0; i < kH; ++i) srow[i * 128] = __float2bfloat16_rn(v[i]);
-        named_bar_sync(1, 128);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int cidx = ts + 128 * i;              // 1024 chunks of 16 B
-          const int hh = cidx >> 4, piece = cidx & 15;
-          const uint4 val = *reinterpret_cast<const uint4*>(stage + hh * 256 + piece * 16);
-          *reinterpret_cast<uint4*>(orow + (size_t)hh * kD + 128 * m + piece * 8) = val;
-        }
+        for (int i = 0; i < kH; ++i) obase[(size_t)i * kD + 128 * m] = __float2bfloat16_rn(v[i]);
       }
-      named_bar_sync(1, 128);                                   // staging free for the next P tiles
+      named_bar_sync(1, 128);                   // the scalars in the P buffer are read; P may be rewritten
       inf = nxt;
       ++qc;
     }
