@@ -75,102 +75,147 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
 
 constexpr int kTopkThreads = 256;
 
-// Block-wide exclusive scan of one int per thread; returns the prefix and
-// writes the block total.
-__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* total) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  int x = v;
-  for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) s_warp[wid] = x;
-  __syncthreads();
-  if (wid == 0) {
-    int wv = lane < kTopkThreads / 32 ? s_warp[lane] : 0;
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, wv, o);
-      if (lane >= o) wv += y;
-    }
-    if (lane < kTopkThreads / 32) s_warp[lane] = wv;
-  }
-  __syncthreads();
-  const int before = (wid > 0 ? s_warp[wid - 1] : 0) + x - v;
-  *total = s_warp[kTopkThreads / 32 - 1];
-  __syncthreads();
-  return before;
+// One block per (t, b): exact top-K of the row's n_vis scores.  The row is
+// loaded once into shared memory as order-preserving 32-bit keys; a 4-pass
+// MSB-first radix select (8 bits per pass) finds the K-th key: each pass
+// builds per-warp 256-bin histograms (lanes that hit the same bin combine
+// their increments first), sums them, and one warp locates the digit with a
+// suffix scan.  The compaction keeps every key above the K-th key plus the
+// lowest-index keys equal to it.  Output in ascending index
+// order, -1 padded.  Rows longer than the shared-memory capacity fall back to
+// reading the keys from global memory on every pass.
+constexpr int kTopkWarps = kTopkThreads / 32;
+
+__device__ __forceinline__ uint32_t row_key(const float* row, const uint32_t* skeys, bool in_smem, int s) {
+  return in_smem ? skeys[s] : ordered_key(row[s]);
 }
 
-// One block per (t, b): exact top-K of the row's n_vis scores by a 4-pass
-// MSB-first radix select on the ordered 32-bit keys (8 bits per pass), then
-// an index-ordered compaction: every key above the K-th key, plus the
-// lowest-index keys equal to it until K are taken.  Output in ascending
-// index order, -1 padded.
 __global__ void __launch_bounds__(kTopkThreads)
 topk_kernel(const float* __restrict__ scores, int32_t* __restrict__ idx, float* __restrict__ iscore,
-            int S, int N, int K, int ratio) {
-  __shared__ int s_hist[256];
-  __shared__ int s_warp[kTopkThreads / 32];
+            int S, int N, int K, int ratio, int smem_cap) {
+  extern __shared__ uint32_t skeys[];
+  __shared__ int s_hist[kTopkWarps][256];
   __shared__ uint32_t s_prefix, s_mask;
   __shared__ int s_krem;
   const int t = blockIdx.x, b = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int nv = min(n_visible(t, ratio), N);
   const float* row = scores + ((size_t)b * S + t) * N;
   int32_t* orow = idx + ((size_t)b * S + t) * K;
   float* srow = iscore ? iscore + ((size_t)b * S + t) * K : nullptr;
   if (nv <= K) {
-    for (int j = threadIdx.x; j < K; j += kTopkThreads) {
+    for (int j = tid; j < K; j += kTopkThreads) {
       orow[j] = j < nv ? j : -1;
       if (srow) srow[j] = j < nv ? row[j] : -INFINITY;
     }
     return;
   }
-  if (threadIdx.x == 0) { s_prefix = 0u; s_mask = 0u; s_krem = K; }
+  const bool in_smem = nv <= smem_cap;
+  if (in_smem)
+    for (int s = tid; s < nv; s += kTopkThreads) skeys[s] = ordered_key(row[s]);
+  if (tid == 0) { s_prefix = 0u; s_mask = 0u; s_krem = K; }
+  __syncthreads();
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += kTopkThreads) s_hist[i] = 0;
+    for (int i = tid; i < kTopkWarps * 256; i += kTopkThreads) (&s_hist[0][0])[i] = 0;
     __syncthreads();
     const uint32_t prefix = s_prefix, mask = s_mask;
-    for (int s = threadIdx.x; s < nv; s += kTopkThreads) {
-      const uint32_t u = ordered_key(row[s]);
-      if ((u & mask) == prefix) atomicAdd(&s_hist[(u >> shift) & 0xFFu], 1);
+    for (int s0 = 0; s0 < nv; s0 += kTopkThreads) {
+      const int s = s0 + tid;
+      int bin = -1;
+      if (s < nv) {
+        const uint32_t u = row_key(row, skeys, in_smem, s);
+        if ((u & mask) == prefix) bin = (int)((u >> shift) & 0xFFu);
+      }
+      // lanes of the warp with the same bin add once
+      const unsigned peers = __match_any_sync(0xffffffffu, bin);
+      if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_hist[wid][bin], __popc(peers));
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      int krem = s_krem, acc = 0, dsel = 0;
-      for (int d = 255; d >= 0; --d) {
-        if (acc + s_hist[d] >= krem) { dsel = d; break; }
-        acc += s_hist[d];
+    // totals per digit
+    {
+      const int d = tid;                       // kTopkThreads == 256 digits
+      int sum = 0;
+#pragma unroll
+      for (int w = 0; w < kTopkWarps; ++w) sum += s_hist[w][d];
+      s_hist[0][d] = sum;
+    }
+    __syncthreads();
+    if (wid == 0) {
+      // lane l owns digits 255-8l .. 248-8l (high digits first)
+      const int krem = s_krem;                  // read before any lane of the warp writes it
+      int cnt[8];
+      int local = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        cnt[i] = s_hist[0][255 - 8 * lane - i];
+        local += cnt[i];
       }
-      s_krem = krem - acc;
-      s_prefix = prefix | ((uint32_t)dsel << shift);
-      s_mask = mask | (0xFFu << shift);
+      int incl = local;                         // inclusive scan over lanes (high digits first)
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int before = incl - local;
+      const bool mine = before < krem && incl >= krem;
+      if (mine) {
+        int acc = before, dsel = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (acc + cnt[i] >= krem) { dsel = 255 - 8 * lane - i; break; }
+          acc += cnt[i];
+        }
+        s_krem = krem - acc;
+        s_prefix = prefix | ((uint32_t)dsel << shift);
+        s_mask = mask | (0xFFu << shift);
+      }
     }
     __syncthreads();
   }
   const uint32_t kth = s_prefix;
   const int ties_needed = s_krem;      // keys equal to kth that are taken
-  int out_base = 0, tie_base = 0;
-  for (int c0 = 0; c0 < nv; c0 += kTopkThreads) {
-    const int s = c0 + threadIdx.x;
-    uint32_t u = 0;
-    if (s < nv) u = ordered_key(row[s]);
-    const int is_tie = (s < nv && u == kth) ? 1 : 0;
-    int tie_tot;
-    const int tie_rank = tie_base + block_exclusive_scan(is_tie, s_warp, &tie_tot);
-    const int take = (s < nv) && (u > kth || (is_tie && tie_rank < ties_needed)) ? 1 : 0;
-    int take_tot;
-    const int pos = out_base + block_exclusive_scan(take, s_warp, &take_tot);
+  // Compaction: warp w owns the contiguous index range [lo, hi).  Counts of
+  // keys above kth and equal to kth per warp give every warp its first
+  // output slot and its first tie rank; each warp then writes its range in
+  // index order.
+  const int span = ((nv + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
+  const int lo = min(wid * span, nv), hi = min(lo + span, nv);
+  int gt = 0, eq = 0;
+  for (int s0 = lo; s0 < hi; s0 += 32) {
+    const int s = s0 + lane;
+    const uint32_t u = s < hi ? row_key(row, skeys, in_smem, s) : 0u;
+    gt += __popc(__ballot_sync(0xffffffffu, s < hi && u > kth));
+    eq += __popc(__ballot_sync(0xffffffffu, s < hi && u == kth));
+  }
+  if (lane == 0) { s_hist[1][wid] = gt; s_hist[2][wid] = eq; }
+  __syncthreads();
+  int out_pos = 0, tie_rank = 0;
+  for (int w = 0; w < wid; ++w) {
+    const int e = s_hist[2][w];
+    out_pos += s_hist[1][w] + max(0, min(e, ties_needed - tie_rank));
+    tie_rank += e;
+  }
+  const unsigned below = (1u << lane) - 1u;
+  for (int s0 = lo; s0 < hi; s0 += 32) {
+    const int s = s0 + lane;
+    const uint32_t u = s < hi ? row_key(row, skeys, in_smem, s) : 0u;
+    const unsigned tie_bits = __ballot_sync(0xffffffffu, s < hi && u == kth);
+    const int my_tie = tie_rank + __popc(tie_bits & below);
+    const bool take = s < hi && (u > kth || (u == kth && my_tie < ties_needed));
+    const unsigned take_bits = __ballot_sync(0xffffffffu, take);
     if (take) {
+      const int pos = out_pos + __popc(take_bits & below);
       orow[pos] = s;
       if (srow) srow[pos] = row[s];
     }
-    out_base += take_tot;
-    tie_base += tie_tot;
+    out_pos += __popc(take_bits);
+    tie_rank += __popc(tie_bits);
   }
-  for (int j = out_base + threadIdx.x; j < K; j += kTopkThreads) {
-    orow[j] = -1;
-    if (srow) srow[j] = -INFINITY;
-  }
+  // slots past the selection (only when fewer than K keys exist; nv > K here)
+  if (wid == kTopkWarps - 1)
+    for (int j = out_pos + lane; j < K; j += 32) {
+      orow[j] = -1;
+      if (srow) srow[j] = -INFINITY;
+    }
 }
 
 template <typename T>
@@ -200,8 +245,13 @@ cudaError_t launch_indexer_scores_simt(const v4_config& c, const void* iqp, cons
 cudaError_t launch_topk(const v4_config& c, const float* scores, int32_t* idx, float* iscore,
                         cudaStream_t st) {
   const int N = c.seqlen / c.ratio;
+  // rows up to 160 KB of keys stay in shared memory
+  const int cap = N < 40960 ? N : 40960;
+  const size_t smem = (size_t)cap * sizeof(uint32_t);
+  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   dim3 grid(c.seqlen, c.batch);
-  topk_kernel<<<grid, kTopkThreads, 0, st>>>(scores, idx, iscore, c.seqlen, N, c.topk, c.ratio);
+  topk_kernel<<<grid, kTopkThreads, smem, st>>>(scores, idx, iscore, c.seqlen, N, c.topk, c.ratio, cap);
   note_launch();
   return cudaGetLastError();
 }
