@@ -20,15 +20,18 @@
 // The key tile in shared memory (8 K-blocks of [128 keys x 64 dims], 128-byte
 // swizzle) is the K-major A operand of the first product and, read as
 // MN-major, the A operand of the second.  TMEM: S^T double buffer (2 x 64
-// columns), O^T (256 columns) and the softmax denominators (64 columns:
-// l = ones[128 x keys] . P^T, an extra M=128 MMA whose A operand is one
-// 128-byte all-ones core matrix read with zero strides, so l sums exactly the
-// bf16 P the output uses).  Contiguous key tiles (window rows, HCA
-// entries) and the query rows arrive by TMA boxes; selected entries are
-// gathered row by row with 16-byte cp.async (many small TMA gathers would
-// serialise in the TMA unit).  The output leaves through shared-memory
-// staging and coalesced 16-byte stores, so it never queues behind loads.
-// Rotations read a per-position cos/sin table built once per call.
+// columns) and O^T (256 columns).  The softmax denominators sum exactly the
+// bf16 P the output uses: after publishing its P row, each softmax warp folds
+// its 32 key rows per head with a lane butterfly while the MMAs run, and the
+// four warp partials meet in shared memory at the end of the query.
+// Contiguous key tiles (window rows, HCA entries) and the query rows arrive
+// by TMA boxes; selected entries are gathered row by row with 16-byte
+// cp.async (many small TMA gathers would serialise in the TMA unit).  Each
+// output row leaves with direct stores (the 32 lanes of a warp cover 64
+// contiguous bytes per head; a lane transpose to 16-byte stores measured
+// slower, its shuffles being latency-bound with one softmax warp per SM
+// sub-partition).  Rotations read a per-position cos/sin table built once per
+// call.
 //
 // Warp roles (256 threads): warp 0 producer (per-query selection list, query
 // rows and contiguous tiles by TMA, one third of the gathers), warp 1 MMA
@@ -84,8 +87,7 @@ struct Ctl {
   int redo;
 };
 
-constexpr uint32_t OFF_ONES = (OFF_CTL + sizeof(Ctl) + 127) & ~127u;   // 8 x 8 bf16 ones
-constexpr uint32_t kSmemBytes = OFF_ONES + 128;
+constexpr uint32_t kSmemBytes = OFF_CTL + sizeof(Ctl);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Params {
@@ -174,11 +176,6 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     c->redo = 0;
     fence_barrier_init();
   }
-  if (threadIdx.x < 8) {
-    const uint32_t one2 = 0x3F803F80u;                  // two bf16 1.0
-    reinterpret_cast<uint4*>(smem + OFF_ONES)[threadIdx.x] = make_uint4(one2, one2, one2, one2);
-    fence_proxy_async_smem();
-  }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&map_q);
     prefetch_tmap(&map_kv);
@@ -226,10 +223,8 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         const int nv = p.ratio > 0 ? min((t + 1) / p.ratio, p.N) : 0;
         if (p.ratio > 0 && p.idx != nullptr) {
           // the helpers must have read the previous query's list
-          bool lok = true;
-          if (lane == 0 && qc >= 1) lok = wait_ok(&c->list_free, (qc - 1) & 1, c, p.status);
+          if (lane == 0 && qc >= 1) (void)wait_ok(&c->list_free, (qc - 1) & 1, c, p.status);
           __syncwarp();
-          (void)lok;
           // all selection slots first, then their norms: two dependent rounds
           const int32_t* row = p.idx + ((size_t)b * p.S + t) * p.K;
           int sv[kMaxSel / 32];
@@ -381,7 +376,6 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       const uint64_t dQ = smem_desc(smem_u32(smem + OFF_Q), 16, 1024, kLayoutSW128);
       const uint64_t dA2 = smem_desc(smem_u32(smem + OFF_SLOT), kSlotBytes, 1024, kLayoutSW128);
       const uint64_t dP0 = smem_desc(smem_u32(smem + OFF_P), 128, 2048, kLayoutNone);
-      const uint64_t dOnes = smem_desc(smem_u32(smem + OFF_ONES), 0, 0, kLayoutNone);   // one core matrix, reused
       int qc = 0, g = 0;
       bool ok = true;
       while (ok) {
@@ -422,10 +416,6 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             umma_commit(&c->empty[2 * m]);
             umma_commit(&c->empty[2 * m + 1]);
           }
-          // denominators: every TMEM lane of columns 384..447 gets sum_k P^T[k, h]
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            umma_f16_ss(tmem + 384, dOnes, dP + (uint64_t)((256 * ks) >> 4), id2, (j > 0 || ks > 0) ? 1u : 0u);
           ++g;
         }
         umma_commit(&c->o_full);
@@ -460,8 +450,15 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     // Rotate the last 64 dims of each head of query qc at position t, take
     // the head norms of the stored bf16 values and publish the shift table.
     auto setup_query = [&](int qc, const QInfo& inf) {
-      wait_ok(&c->q_full, qc & 1, c, p.status);
       const int h = ts >> 1, half = ts & 1;
+      // cos/sin of this thread's 16 rotation pairs, fetched before the wait
+      float4 csv[8];
+      {
+        const float4* csp = reinterpret_cast<const float4*>(p.rope_cs + (size_t)inf.t * (kR / 2) + 16 * half);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) csv[i] = csp[i];
+      }
+      wait_ok(&c->q_full, qc & 1, c, p.status);
       uint8_t* qrow = smem + OFF_Q + 7 * kQBlockBytes + h * 128;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
@@ -469,8 +466,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         uint4* ptr = reinterpret_cast<uint4*>(qrow + ((ch ^ (h & 7)) * 16));
         uint4 u = *ptr;
         __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&u);
-        const float4* csp = reinterpret_cast<const float4*>(p.rope_cs + (size_t)inf.t * (kR / 2) + ch * 4);
-        const float4 cs01 = csp[0], cs23 = csp[1];
+        const float4 cs01 = csv[2 * cc], cs23 = csv[2 * cc + 1];
         const float cs[8] = {cs01.x, cs01.y, cs01.z, cs01.w, cs23.x, cs23.y, cs23.z, cs23.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -519,6 +515,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       const float* mlog2 = c->mlog2[qc & 1];
       const int t = inf.t, b = inf.b;
       const int nk_total = inf.n_ent + (t - inf.w_lo + 1);
+      float lsum0 = 0.f, lsum1 = 0.f;           // this warp's denominators of heads 2*lane, 2*lane+1
       for (int j = 0; j < inf.tiles; ++j) {
         const int sb = g & 1;
         bool valid;
@@ -549,6 +546,32 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&c->p_ready[sb]);
+        // Sum the warp's 32 rows per head while the products run: five
+        // butterfly rounds, each lane keeping half of its heads, leave lane L
+        // with heads 2L and 2L+1 (pk[i] packs heads 2i, 2i+1).
+        {
+          float r[32];
+          const bool up = (lane & 16) != 0;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint32_t keep = up ? pk[16 + i] : pk[i];
+            const uint32_t got = __shfl_xor_sync(0xffffffffu, up ? pk[i] : pk[16 + i], 16);
+            r[2 * i] = __uint_as_float(keep << 16) + __uint_as_float(got << 16);
+            r[2 * i + 1] = __uint_as_float(keep & 0xFFFF0000u) + __uint_as_float(got & 0xFFFF0000u);
+          }
+#pragma unroll
+          for (int o = 8, w = 16; o >= 1; o >>= 1, w >>= 1) {
+            const bool hi = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < w; ++i) {
+              const float send = hi ? r[i] : r[w + i];
+              const float keep = hi ? r[w + i] : r[i];
+              r[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+          }
+          lsum0 += r[0];
+          lsum1 += r[1];
+        }
         ++g;
       }
 
@@ -569,37 +592,20 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       }
       wait_ok(&c->o_full, qc & 1, c, p.status);
       tc_fence_after();
-      // per-head scalars, one head per thread; the P buffers are idle here
-      float* hs = reinterpret_cast<float*>(smem + OFF_P);        // [0,64) l, [64,128) 1/l
-      if (ts < 32) {
-        float lv[32];
-        tmem_ld32(tmem + lane_base + 384, lv);                   // every lane holds l_h in column h
-        tmem_wait_ld();
-        if (ts == 0) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(hs + i) = make_float4(lv[i], lv[i + 1], lv[i + 2], lv[i + 3]);
-        }
-      } else if (ts < 64) {
-        float lv[32];
-        tmem_ld32(tmem + lane_base + 384 + 32, lv);
-        tmem_wait_ld();
-        if (ts == 32) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(hs + 32 + i) = make_float4(lv[i], lv[i + 1], lv[i + 2], lv[i + 3]);
-        }
-      }
+      // per-head scalars, one head per thread; the P buffers are idle here:
+      // [0,256) the four warp partials of l, [256,320) 1/l
+      float* hs = reinterpret_cast<float*>(smem + OFF_P);
+      *reinterpret_cast<float2*>(hs + 64 * quarter + 2 * lane) = make_float2(lsum0, lsum1);
       named_bar_sync(1, 128);
       if (ts < kH) {
-        float l = hs[ts];
+        float l = (hs[ts] + hs[64 + ts]) + (hs[128 + ts] + hs[192 + ts]);
         const float m = mlog2[ts] * 0.6931471805599453f;
         if (p.sink != nullptr) l += expf(p.sink[ts] - m);
         // too little mass under the bound: exp underflow may have lost keys
         const bool bad = !(l >= (float)nk_total * 1.0e-26f) || !(l < INFINITY);
         if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&c->redo, 1);
         if (p.lse) p.lse[((size_t)b * p.S + t) * kH + ts] = m + logf(l);
-        hs[kH + ts] = 1.0f / l;
+        hs[256 + ts] = 1.0f / l;
       }
       named_bar_sync(1, 128);
       if (ts == 0 && c->redo) {                 // queue the query once for the running-max kernel
@@ -610,7 +616,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       float inv_l[kH];
 #pragma unroll
       for (int i = 0; i < kH; i += 4) {
-        const float4 v4 = *reinterpret_cast<const float4*>(hs + kH + i);
+        const float4 v4 = *reinterpret_cast<const float4*>(hs + 256 + i);
         inv_l[i] = v4.x;
         inv_l[i + 1] = v4.y;
         inv_l[i + 2] = v4.z;
