@@ -119,7 +119,7 @@ Workspace plan_workspace(const v4_config& c) {
   take(w.iqp, w.iqp_bytes, sel ? B * S * c.idx_heads * c.idx_dim * es : 0);
   take(w.scores, w.scores_bytes, sel ? B * S * N * 4 : 0);
   take(w.idx, w.idx_bytes, sel ? B * S * c.topk * 4 : 0);
-  take(w.knorm, w.knorm_bytes, (B * S + B * N) * 4);
+  take(w.knorm, w.knorm_bytes, key_norm_floats(c) * 4);
   take(w.counters, w.counters_bytes, (2 + B * S) * 4);
   take(w.rope, w.rope_bytes, S * (size_t)(c.rope_dim / 2) * 8);
   w.total = off;
@@ -245,6 +245,9 @@ static v4_status do_mqa(const v4_config& c, const void* q, const void* kv, const
   void* kv_rot = ws + plan.kv_rot;
   float* kv_norm = (float*)(ws + plan.knorm);
   float* ent_norm = kv_norm + (size_t)c.batch * c.seqlen;
+  const size_t n_ent = c.ratio > 0 ? (size_t)c.batch * (c.seqlen / c.ratio) : 0;
+  float* wmax = ent_norm + n_ent;
+  float* emax = wmax + (size_t)c.batch * c.seqlen;
   const bool tc = use_tc_attention(c);
   {
     ProfScope ps(K_ROTATE, st);
@@ -253,7 +256,7 @@ static v4_status do_mqa(const v4_config& c, const void* q, const void* kv, const
         v4_status s = do_rope_table(c, f, ws, st);
         if (s != V4_OK) return s;
       }
-      CU(launch_key_prep(c, kv, ent, table, kv_rot, kv_norm, ent_norm, st), "key prep kernel");
+      CU(launch_key_prep(c, kv, ent, table, kv_rot, kv_norm, ent_norm, wmax, emax, st), "key prep kernel");
     } else {
       CU(launch_rotate_rows(c, kv, f, kv_rot, st), "window-key rotation kernel");
     }
@@ -262,7 +265,7 @@ static v4_status do_mqa(const v4_config& c, const void* q, const void* kv, const
     int* counters = (int*)(ws + plan.counters);
     {
       ProfScope ps(K_ATTN, st);
-      CU(launch_mqa_tc(c, q, kv_rot, ent, idx, sink, table, kv_norm, ent_norm, o, lse, counters, status, st),
+      CU(launch_mqa_tc(c, q, kv_rot, ent, idx, sink, table, wmax, emax, o, lse, counters, status, st),
          "tensor-core attention kernel");
     }
     // queries whose bound-shifted softmax kept too little mass are recomputed

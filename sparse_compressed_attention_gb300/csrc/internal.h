@@ -40,10 +40,19 @@ cudaError_t launch_compress(const v4_config& c, const void* ckv, const void* csc
                             int dim, int hadamard, void* out, cudaStream_t st);
 cudaError_t launch_rotate_rows(const v4_config& c, const void* kv, const float* inv_freq,
                                void* kv_rot, cudaStream_t st);
-// Rotated window keys plus the Euclidean norm of every stored key row
-// (window rows then entry rows), as the tensor-core attention needs them.
+// Rotated window keys, the Euclidean norm of every stored key row (window
+// rows then entry rows) and, from them, the per-query bounds the
+// tensor-core attention shifts by: wmax[B*S] (window maximum) and
+// emax[B*(N+1)] (prefix maximum over entries).  Window <= 1024.
 cudaError_t launch_key_prep(const v4_config& c, const void* kv, const void* ent, const float2* cs_table,
-                            void* kv_rot, float* kv_norm, float* ent_norm, cudaStream_t st);
+                            void* kv_rot, float* kv_norm, float* ent_norm, float* wmax, float* emax,
+                            cudaStream_t st);
+// Floats of the norm and bound arrays above.
+inline size_t key_norm_floats(const v4_config& c) {
+  const size_t T = (size_t)c.batch * c.seqlen;
+  const size_t N = c.ratio > 0 ? (size_t)(c.seqlen / c.ratio) : 0;
+  return 2 * T + (size_t)c.batch * N + (size_t)c.batch * (N + 1);
+}
 // cos/sin of every (position < S, rotated pair): table[pos * R/2 + j].
 cudaError_t launch_rope_table(const v4_config& c, const float* inv_freq, float2* table, cudaStream_t st);
 
@@ -78,7 +87,7 @@ cudaError_t launch_oproj_tc(const v4_config& c, const void* o, const void* wo_a,
                             cudaStream_t st);
 cudaError_t launch_mqa_tc(const v4_config& c, const void* q, const void* kv_rot, const void* ent,
                           const int32_t* idx, const float* sink, const float2* cs_table,
-                          const float* kv_norm, const float* ent_norm, void* o, float* lse,
+                          const float* wmax, const float* emax, void* o, float* lse,
                           int* counters, int* status, cudaStream_t st);
 
 }  // namespace v4

@@ -97,8 +97,8 @@ struct Params {
   const int32_t* idx;          // [B,S,K] or null
   const float* sink;           // [64] or null
   const float2* rope_cs;       // [S][32] cos/sin
-  const float* kv_norm;        // [B*S]
-  const float* ent_norm;       // [B*N]
+  const float* wmax;           // [B*S]   max |key| over the window of each query
+  const float* emax;           // [B*(N+1)] prefix max |entry|
   float* lse;                  // [B,S,64] or null
   int* status;
   int* counters;               // [0] work item, [1] redo count, [2..] redo list
@@ -194,6 +194,29 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     int qc = 0, g = 0;
+    // The selection row and the norm bound of a query are read one query
+    // ahead, so that its list is ready as soon as the previous one is done.
+    const bool gathered = p.ratio > 0 && p.idx != nullptr;
+    int sv[kMaxSel / 32];
+    float kb_next = 0.f;
+    auto fetch_ahead = [&](int it) {
+      if (it >= total) return;
+      const int nb = it % p.B, nt = p.S - 1 - it / p.B;
+      if (gathered) {
+        const int32_t* row = p.idx + ((size_t)nb * p.S + nt) * p.K;
+#pragma unroll
+        for (int i = 0; i < kMaxSel / 32; ++i) {
+          const int j = lane + 32 * i;
+          sv[i] = j < p.K ? row[j] : -1;
+        }
+      }
+      kb_next = p.wmax[(size_t)nb * p.S + nt];
+      if (p.ratio > 0) {
+        const int nv = min((nt + 1) / p.ratio, p.N);
+        kb_next = fmaxf(kb_next, p.emax[(size_t)nb * (p.N + 1) + nv]);
+      }
+    };
+    fetch_ahead(blockIdx.x);
     for (int item = blockIdx.x;; item += gridDim.x) {
       QInfo inf;
       inf.done = item >= total ? 1 : 0;
@@ -207,8 +230,9 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           const int nb = nxt % p.B, nt = p.S - 1 - nxt / p.B;
           const bf16* qn = p.q + ((size_t)nb * p.S + nt) * kH * kD;
           asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(qn), "r"(kH * kD * 2) : "memory");
-          if (p.idx != nullptr && p.K >= 4) {
-            const int32_t* rn = p.idx + ((size_t)nb * p.S + nt) * p.K;
+          const int nn = nxt + gridDim.x;      // the selection is read one query ahead of its use
+          if (p.idx != nullptr && p.K >= 4 && nn < total) {
+            const int32_t* rn = p.idx + ((size_t)(nn % p.B) * p.S + (p.S - 1 - nn / p.B)) * p.K;
             const uint32_t bytes = (uint32_t)(p.K * 4) & ~15u;
             if ((((uintptr_t)rn) & 15u) == 0 && bytes > 0)
               asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(rn), "r"(bytes) : "memory");
@@ -217,59 +241,36 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       }
       inf.b = b;
       inf.t = t;
-      float kmax = 0.f;
+      // kmax bounds |k| over every key the query can see (for a selection,
+      // over all visible entries: a superset, so still a bound)
+      const float kmax = kb_next;
       int n_ent = 0;
       if (!inf.done) {
         const int nv = p.ratio > 0 ? min((t + 1) / p.ratio, p.N) : 0;
-        if (p.ratio > 0 && p.idx != nullptr) {
+        if (gathered) {
           // the helpers must have read the previous query's list
           if (lane == 0 && qc >= 1) (void)wait_ok(&c->list_free, (qc - 1) & 1, c, p.status);
           __syncwarp();
-          // all selection slots first, then their norms: two dependent rounds
-          const int32_t* row = p.idx + ((size_t)b * p.S + t) * p.K;
-          int sv[kMaxSel / 32];
-#pragma unroll
-          for (int i = 0; i < kMaxSel / 32; ++i) {
-            const int j = lane + 32 * i;
-            sv[i] = j < p.K ? row[j] : -1;
-          }
-          float nrm[kMaxSel / 32];
-#pragma unroll
-          for (int i = 0; i < kMaxSel / 32; ++i) {
-            if (sv[i] < -1 || sv[i] >= nv) {
-              set_status(p.status, kStatusBadIndex);
-              sv[i] = -1;
-            }
-            nrm[i] = sv[i] >= 0 ? p.ent_norm[(size_t)b * p.N + sv[i]] : 0.f;
-          }
           int base = 0;
 #pragma unroll
           for (int i = 0; i < kMaxSel / 32; ++i) {
-            const bool ok = sv[i] >= 0;
+            int e = sv[i];
+            if (e < -1 || e >= nv) {
+              set_status(p.status, kStatusBadIndex);
+              e = -1;
+            }
+            const bool ok = e >= 0;
             const unsigned m = __ballot_sync(0xffffffffu, ok);
-            if (ok) list[base + __popc(m & ((1u << lane) - 1u))] = sv[i];
+            if (ok) list[base + __popc(m & ((1u << lane) - 1u))] = e;
             base += __popc(m);
-            kmax = fmaxf(kmax, nrm[i]);
           }
           n_ent = base;
         } else if (p.ratio > 0) {
           n_ent = nv;
-          for (int s0 = 0; s0 < nv; s0 += 128) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int s = s0 + lane + 32 * i;
-              if (s < nv) kmax = fmaxf(kmax, p.ent_norm[(size_t)b * p.N + s]);
-            }
-          }
         }
         inf.w_lo = max(0, t - p.window + 1);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int u = inf.w_lo + lane + 32 * i;
-          if (u <= t) kmax = fmaxf(kmax, p.kv_norm[(size_t)b * p.S + u]);
-        }
-        for (int o = 16; o > 0; o >>= 1) kmax = fmaxf(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
         __syncwarp();
+        fetch_ahead(item + gridDim.x);
       }
       inf.n_ent = n_ent;
       inf.ent_tiles = (n_ent + kTileKeys - 1) / kTileKeys;
@@ -668,7 +669,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
 
 cudaError_t launch_mqa_tc(const v4_config& cfg, const void* q, const void* kv_rot, const void* ent,
                           const int32_t* idx, const float* sink, const float2* cs_table,
-                          const float* kv_norm, const float* ent_norm, void* o, float* lse,
+                          const float* wmax, const float* emax, void* o, float* lse,
                           int* counters, int* status, cudaStream_t st) {
   const int B = cfg.batch, S = cfg.seqlen;
   const int N = cfg.ratio > 0 ? S / cfg.ratio : 0;
@@ -688,8 +689,8 @@ cudaError_t launch_mqa_tc(const v4_config& cfg, const void* q, const void* kv_ro
   prm.idx = idx;
   prm.sink = sink;
   prm.rope_cs = cs_table;
-  prm.kv_norm = kv_norm;
-  prm.ent_norm = ent_norm;
+  prm.wmax = wmax;
+  prm.emax = emax;
   prm.lse = lse;
   prm.status = status;
   prm.counters = counters;

@@ -26,7 +26,7 @@ namespace {
 // table).  The Flash shapes (D=512, R=64, bf16) reach all three at B*S=8192.
 constexpr long long kMaxTokens = 8192;
 constexpr size_t kKvBytes = 8u << 20;
-constexpr size_t kNormBytes = 2 * kMaxTokens * sizeof(float);            // window rows + entries
+constexpr size_t kNormBytes = 5 * kMaxTokens * sizeof(float);            // norms and their bounds
 constexpr size_t kCounterBytes = (2 + kMaxTokens) * sizeof(int);
 constexpr size_t kRopeBytes = 524288 / 2 * sizeof(float2);
 constexpr size_t kOffNorm = kKvBytes;
@@ -100,16 +100,18 @@ extern "C" v4_status v4_sparse_mqa_fwd_noalloc(const v4_config* cfg, const void*
   void* kv_rot = base;
   float* kv_norm = (float*)(base + kOffNorm);
   float* ent_norm = kv_norm + tokens;
+  float* wmax = ent_norm + (c.ratio > 0 ? (long long)c.batch * (c.seqlen / c.ratio) : 0);
+  float* emax = wmax + tokens;
   int* counters = (int*)(base + kOffCounters);
   float2* table = (float2*)(base + kOffRope);
   const int32_t* sel = c.topk > 0 ? idx : nullptr;
   cudaError_t e;
   if (c.path != V4_PATH_SIMT && mqa_tc_supported(c)) {
     if ((e = launch_rope_table(c, inv_freq, table, st)) != cudaSuccess) return set_error(V4_ERR_CUDA, cudaGetErrorString(e));
-    if ((e = launch_key_prep(c, kv, ent, table, kv_rot, kv_norm, ent_norm, st)) != cudaSuccess)
+    if ((e = launch_key_prep(c, kv, ent, table, kv_rot, kv_norm, ent_norm, wmax, emax, st)) != cudaSuccess)
       return set_error(V4_ERR_CUDA, cudaGetErrorString(e));
     // launch_mqa_tc clears the redo count it needs before its kernel runs
-    if ((e = launch_mqa_tc(c, q, kv_rot, ent, sel, sink, table, kv_norm, ent_norm, o, lse, counters, status, st)) !=
+    if ((e = launch_mqa_tc(c, q, kv_rot, ent, sel, sink, table, wmax, emax, o, lse, counters, status, st)) !=
         cudaSuccess)
       return set_error(V4_ERR_CUDA, cudaGetErrorString(e));
     if ((e = launch_mqa_simt(c, q, kv_rot, ent, sel, sink, inv_freq, o, lse, status, counters + 1, st)) != cudaSuccess)
