@@ -637,12 +637,25 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         }
 #pragma unroll
         for (int i = 0; i < kH; ++i) v[i] *= inv_l[i];
-        if (m == 3) {
+        if (m == 3 && quarter >= 2) {
+          // rotated dims 448..511: the partner of each pair is the
+          // neighbouring lane; the values cross through the idle second P
+          // buffer (sixteen 16-byte stores and loads instead of 64 shuffles)
+          float4* xb = reinterpret_cast<float4*>(smem + OFF_P + kPBytes + (quarter - 2) * (kPBytes / 2));
+#pragma unroll
+          for (int c4 = 0; c4 < kH / 4; ++c4)
+            xb[c4 * 32 + lane] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+          __syncwarp();
           const bool odd = lane & 1;
 #pragma unroll
-          for (int i = 0; i < kH; ++i) {
-            const float other = __shfl_xor_sync(0xffffffffu, v[i], 1);
-            if (dim3 >= kD - kR) v[i] = odd ? (-other * ds + v[i] * dc) : (v[i] * dc + other * ds);
+          for (int c4 = 0; c4 < kH / 4; ++c4) {
+            const float4 o4 = xb[c4 * 32 + (lane ^ 1)];
+            const float oth[4] = {o4.x, o4.y, o4.z, o4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int i = 4 * c4 + e;
+              v[i] = odd ? (v[i] * dc - oth[e] * ds) : (v[i] * dc + oth[e] * ds);
+            }
           }
         }
 #pragma unroll
