@@ -64,7 +64,7 @@ constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_SLOT = OFF_Q + 8 * kQBlockBytes;           // 65536
 constexpr uint32_t OFF_P = OFF_SLOT + kSlots * kSlotBytes;        // 196608
 constexpr uint32_t OFF_LIST = OFF_P + 2 * kPBytes;                // 229376
-constexpr uint32_t OFF_CTL = OFF_LIST + kMaxSel * 4;              // 231424
+constexpr uint32_t OFF_CTL = OFF_LIST + 2 * kMaxSel * 2;          // 231424 (two 16-bit lists)
 
 struct QInfo {
   int b, t, n_ent, ent_tiles, tiles, w_lo, done;
@@ -72,8 +72,10 @@ struct QInfo {
 };
 
 struct Ctl {
-  uint64_t full[kSlots], empty[kSlots];    // full: 96 gather-lane arrivals + TMA bytes
-  uint64_t list_free;                      // warps 2-3 have read the selection list
+  uint64_t full_g[kSlots];                 // gathered K-block landed: 96 gather-lane arrivals
+  uint64_t full_t[kSlots];                 // contiguous K-block landed: one arrival + TMA bytes
+  uint64_t empty[kSlots];
+  uint64_t list_free[2];                   // warps 2-3 have read selection list 0 / 1
   uint64_t q_full, q_ready, q_empty;
   uint64_t s_full[2], p_ready[2];
   uint64_t o_full, o_empty;
@@ -137,7 +139,8 @@ __device__ __forceinline__ void gather_kblock(uint8_t* slot, const bf16* ent_b, 
 }
 
 // Selection-list rows of tile j for gather warp gw of nw (row 0 pads short tiles).
-__device__ __forceinline__ void load_rows(const int* list, int n_ent, int j, int gw, int nw, int lane, int* sidx) {
+__device__ __forceinline__ void load_rows(const uint16_t* list, int n_ent, int j, int gw, int nw, int lane,
+                                          int* sidx) {
 #pragma unroll
   for (int i = 0; i < kMaxGroups; ++i) {
     const int grp = gw + nw * i;
@@ -151,15 +154,20 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
               const __grid_constant__ CUtensorMap map_ent, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Ctl* c = reinterpret_cast<Ctl*>(smem + OFF_CTL);
-  int* list = reinterpret_cast<int*>(smem + OFF_LIST);
+  uint16_t* lists = reinterpret_cast<uint16_t*>(smem + OFF_LIST);   // [2][kMaxSel], by query parity
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if ((smem_u32(smem) & 1023u) != 0) {          // swizzled operands need 1 KB alignment
     if (threadIdx.x == 0) set_status(p.status, V4_ERR_UNSUPPORTED);
     return;
   }
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kSlots; ++i) { mbar_init(&c->full[i], kGatherLanes); mbar_init(&c->empty[i], 1); }
-    mbar_init(&c->list_free, 64);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&c->full_g[i], kGatherLanes);
+      mbar_init(&c->full_t[i], 1);
+      mbar_init(&c->empty[i], 1);
+    }
+    mbar_init(&c->list_free[0], 64);
+    mbar_init(&c->list_free[1], 64);
     mbar_init(&c->q_full, 1);
     mbar_init(&c->q_ready, 128);
     mbar_init(&c->q_empty, 1);
@@ -193,9 +201,10 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int qc = 0, g = 0;
-    // The selection row and the norm bound of a query are read one query
-    // ahead, so that its list is ready as soon as the previous one is done.
+    // Query qc+1 is described (selection list, bound, tile counts) and
+    // published while query qc's first tile loads, so every role can move on
+    // to it without waiting; its selection row and bound are read one more
+    // query ahead.  Lists alternate between two 16-bit buffers.
     const bool gathered = p.ratio > 0 && p.idx != nullptr;
     int sv[kMaxSel / 32];
     float kb_next = 0.f;
@@ -216,121 +225,122 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         kb_next = fmaxf(kb_next, p.emax[(size_t)nb * (p.N + 1) + nv]);
       }
     };
-    fetch_ahead(blockIdx.x);
-    for (int item = blockIdx.x;; item += gridDim.x) {
+    auto prepare = [&](int qn, int it) -> QInfo {
       QInfo inf;
-      inf.done = item >= total ? 1 : 0;
-      int b = 0, t = 0;
-      if (!inf.done) {
-        b = item % p.B;
-        t = p.S - 1 - item / p.B;
-        // warm L2 with the query rows and selection of this CTA's next query
-        const int nxt = item + gridDim.x;
-        if (lane == 0 && nxt < total) {
-          const int nb = nxt % p.B, nt = p.S - 1 - nxt / p.B;
-          const bf16* qn = p.q + ((size_t)nb * p.S + nt) * kH * kD;
-          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(qn), "r"(kH * kD * 2) : "memory");
-          const int nn = nxt + gridDim.x;      // the selection is read one query ahead of its use
-          if (p.idx != nullptr && p.K >= 4 && nn < total) {
-            const int32_t* rn = p.idx + ((size_t)(nn % p.B) * p.S + (p.S - 1 - nn / p.B)) * p.K;
-            const uint32_t bytes = (uint32_t)(p.K * 4) & ~15u;
-            if ((((uintptr_t)rn) & 15u) == 0 && bytes > 0)
-              asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(rn), "r"(bytes) : "memory");
-          }
-        }
-      }
-      inf.b = b;
-      inf.t = t;
+      inf.done = it >= total ? 1 : 0;
+      inf.b = inf.done ? 0 : it % p.B;
+      inf.t = inf.done ? 0 : p.S - 1 - it / p.B;
       // kmax bounds |k| over every key the query can see (for a selection,
       // over all visible entries: a superset, so still a bound)
-      const float kmax = kb_next;
-      int n_ent = 0;
+      inf.kmax = kb_next;
+      inf.n_ent = 0;
+      inf.w_lo = 0;
       if (!inf.done) {
-        const int nv = p.ratio > 0 ? min((t + 1) / p.ratio, p.N) : 0;
+        if (lane == 0) {                      // warm L2 with its query rows, loaded one query later
+          const bf16* qn_rows = p.q + ((size_t)inf.b * p.S + inf.t) * kH * kD;
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(qn_rows), "r"(kH * kD * 2) : "memory");
+        }
+        const int nv = p.ratio > 0 ? min((inf.t + 1) / p.ratio, p.N) : 0;
         if (gathered) {
-          // the helpers must have read the previous query's list
-          if (lane == 0 && qc >= 1) (void)wait_ok(&c->list_free, (qc - 1) & 1, c, p.status);
+          // the helpers must have read the list this buffer held two queries ago
+          if (lane == 0 && qn >= 2) (void)wait_ok(&c->list_free[qn & 1], ((qn >> 1) - 1) & 1, c, p.status);
           __syncwarp();
+          uint16_t* lst = lists + (qn & 1) * kMaxSel;
+          // every ballot first, then the stores: no chain through the count
+          unsigned msk[kMaxSel / 32];
+#pragma unroll
+          for (int i = 0; i < kMaxSel / 32; ++i) {
+            if (sv[i] < -1 || sv[i] >= nv) {
+              set_status(p.status, kStatusBadIndex);
+              sv[i] = -1;
+            }
+            msk[i] = __ballot_sync(0xffffffffu, sv[i] >= 0);
+          }
+          const unsigned below = (1u << lane) - 1u;
           int base = 0;
 #pragma unroll
           for (int i = 0; i < kMaxSel / 32; ++i) {
-            int e = sv[i];
-            if (e < -1 || e >= nv) {
-              set_status(p.status, kStatusBadIndex);
-              e = -1;
-            }
-            const bool ok = e >= 0;
-            const unsigned m = __ballot_sync(0xffffffffu, ok);
-            if (ok) list[base + __popc(m & ((1u << lane) - 1u))] = e;
-            base += __popc(m);
+            if (sv[i] >= 0) lst[base + __popc(msk[i] & below)] = (uint16_t)sv[i];
+            base += __popc(msk[i]);
           }
-          n_ent = base;
+          inf.n_ent = base;
         } else if (p.ratio > 0) {
-          n_ent = nv;
+          inf.n_ent = nv;
         }
-        inf.w_lo = max(0, t - p.window + 1);
+        inf.w_lo = max(0, inf.t - p.window + 1);
         __syncwarp();
-        fetch_ahead(item + gridDim.x);
+        fetch_ahead(it + gridDim.x);
       }
-      inf.n_ent = n_ent;
-      inf.ent_tiles = (n_ent + kTileKeys - 1) / kTileKeys;
+      inf.ent_tiles = (inf.n_ent + kTileKeys - 1) / kTileKeys;
       inf.tiles = inf.ent_tiles + 1;            // + the window tile
-      inf.kmax = kmax;
-      // publish the query
-      const int is = qc & 1;
-      bool ok = true;
       if (lane == 0) {
-        if (qc >= 2) ok = wait_ok(&c->info_empty[is], ((qc >> 1) - 1) & 1, c, p.status);
+        const int is = qn & 1;
+        if (qn >= 2) (void)wait_ok(&c->info_empty[is], ((qn >> 1) - 1) & 1, c, p.status);
         c->info[is] = inf;
         mbar_arrive(&c->info_full[is]);
       }
-      ok = __shfl_sync(0xffffffffu, (int)ok, 0);
-      if (inf.done || !ok) break;
-      // queries: the 64 head rows of (b, t)
-      if (lane == 0) {
-        if (qc >= 1) ok = wait_ok(&c->q_empty, (qc - 1) & 1, c, p.status);
-        if (ok) {
-          mbar_expect_tx(&c->q_full, 8 * kQBlockBytes);
-          for (int kb = 0; kb < 8; ++kb)
-            tma_load_2d(smem + OFF_Q + kb * kQBlockBytes, &map_q, 64 * kb, (b * p.S + t) * kH, &c->q_full);
-        }
-      }
+      __syncwarp();
+      return inf;
+    };
+
+    int qc = 0, g = 0;
+    fetch_ahead(blockIdx.x);
+    QInfo cur = prepare(0, blockIdx.x);
+    bool ok = true;
+    for (int item = blockIdx.x; !cur.done; item += gridDim.x) {
+      // query rows: one 8 KB box per lane 0..7
+      if (lane == 0 && qc >= 1) ok = wait_ok(&c->q_empty, (qc - 1) & 1, c, p.status);
       ok = __shfl_sync(0xffffffffu, (int)ok, 0);
       if (!ok) break;
-      // key tiles
-      for (int j = 0; j < inf.tiles && ok; ++j) {
-        const bool window_tile = j == inf.ent_tiles;
-        int sidx[kMaxGroups];
-        const int nw = 3;
-        if (!window_tile && p.idx != nullptr) load_rows(list, n_ent, j, 0, nw, lane, sidx);
-        for (int kb = 0; kb < kSlots; ++kb) {
-          if (lane == 0 && g >= 1) ok = wait_ok(&c->empty[kb], (g - 1) & 1, c, p.status);
-          ok = __shfl_sync(0xffffffffu, (int)ok, 0);
-          if (!ok) break;
-          uint8_t* dst = smem + OFF_SLOT + kb * kSlotBytes;
-          if (window_tile || p.idx == nullptr) {
-            if (lane == 0) {
-              mbar_expect_tx(&c->full[kb], kSlotBytes);
+      if (lane == 0) mbar_expect_tx(&c->q_full, 8 * kQBlockBytes);
+      __syncwarp();
+      if (lane < 8)
+        tma_load_2d(smem + OFF_Q + lane * kQBlockBytes, &map_q, 64 * lane, (cur.b * p.S + cur.t) * kH, &c->q_full);
+      const uint16_t* lst = lists + (qc & 1) * kMaxSel;
+      QInfo nxt;
+      nxt.done = 1;
+      for (int j = 0; j < cur.tiles && ok; ++j) {
+        const bool window_tile = j == cur.ent_tiles;
+        if (window_tile || !gathered) {
+          // contiguous rows: lane kb loads K-block kb as soon as its slot is free
+          bool lok = true;
+          if (lane < kSlots) {
+            const int kb = lane;
+            if (g >= 1) lok = wait_ok(&c->empty[kb], (g - 1) & 1, c, p.status);
+            if (lok) {
+              uint8_t* dst = smem + OFF_SLOT + kb * kSlotBytes;
+              mbar_expect_tx(&c->full_t[kb], kSlotBytes);
               if (window_tile)
-                tma_load_2d(dst, &map_kv, 64 * kb, b * p.S + t - (kTileKeys - 1), &c->full[kb]);
+                tma_load_2d(dst, &map_kv, 64 * kb, cur.b * p.S + cur.t - (kTileKeys - 1), &c->full_t[kb]);
               else
-                tma_load_2d(dst, &map_ent, 64 * kb, b * p.N + j * kTileKeys, &c->full[kb]);
-            } else {
-              mbar_arrive(&c->full[kb]);
+                tma_load_2d(dst, &map_ent, 64 * kb, cur.b * p.N + j * kTileKeys, &c->full_t[kb]);
             }
-          } else {
-            gather_kblock(dst, p.ent + (size_t)b * p.N * kD, sidx, 0, nw, lane, kb, &c->full[kb]);
+          }
+          ok = __all_sync(0xffffffffu, lok);
+        } else {
+          int sidx[kMaxGroups];
+          const int nw = 3;
+          load_rows(lst, cur.n_ent, j, 0, nw, lane, sidx);
+          for (int kb = 0; kb < kSlots; ++kb) {
+            if (lane == 0 && g >= 1) ok = wait_ok(&c->empty[kb], (g - 1) & 1, c, p.status);
+            ok = __shfl_sync(0xffffffffu, (int)ok, 0);
+            if (!ok) break;
+            gather_kblock(smem + OFF_SLOT + kb * kSlotBytes, p.ent + (size_t)cur.b * p.N * kD, sidx, 0, nw, lane,
+                          kb, &c->full_g[kb]);
           }
         }
+        if (j == 0) nxt = prepare(qc + 1, item + gridDim.x);
         ++g;
       }
       if (!ok) break;
       ++qc;
+      cur = nxt;
       __syncwarp();
     }
   } else if (warp == 2 || warp == 3) {
     // ------------------------------------------------------------ gather helpers
     const int gw = warp - 1;                  // row groups gw, gw+3, ...
+    const bool gathered = p.ratio > 0 && p.idx != nullptr;
     int qc = 0, g = 0;
     bool ok = true;
     while (ok) {
@@ -342,25 +352,25 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       __syncwarp();
       mbar_arrive(&c->info_empty[is]);
       if (inf.done || !ok) break;
-      const bool gathered = p.idx != nullptr;
-      if (!gathered || inf.ent_tiles == 0) mbar_arrive(&c->list_free);
+      if (!gathered || inf.ent_tiles == 0) mbar_arrive(&c->list_free[is]);
+      const uint16_t* lst = lists + is * kMaxSel;
       const bf16* ent_b = p.ent + (size_t)inf.b * p.N * kD;
       for (int j = 0; j < inf.tiles && ok; ++j) {
-        const bool window_tile = j == inf.ent_tiles;
+        // Contiguous tiles come by TMA alone, but their slot releases are still
+        // awaited: a parity wait is only unambiguous one phase ahead.
+        const bool contiguous = j == inf.ent_tiles || !gathered;
         int sidx[kMaxGroups];
         const int nw = 3;
-        if (!window_tile && gathered) {
-          load_rows(list, inf.n_ent, j, gw, nw, lane, sidx);
-          if (j == inf.ent_tiles - 1) mbar_arrive(&c->list_free);
+        if (!contiguous) {
+          load_rows(lst, inf.n_ent, j, gw, nw, lane, sidx);
+          if (j == inf.ent_tiles - 1) mbar_arrive(&c->list_free[is]);
         }
         for (int kb = 0; kb < kSlots; ++kb) {
           if (lane == 0 && g >= 1) ok = wait_ok(&c->empty[kb], (g - 1) & 1, c, p.status);
           ok = __shfl_sync(0xffffffffu, (int)ok, 0);
           if (!ok) break;
-          if (window_tile || !gathered)
-            mbar_arrive(&c->full[kb]);
-          else
-            gather_kblock(smem + OFF_SLOT + kb * kSlotBytes, ent_b, sidx, gw, nw, lane, kb, &c->full[kb]);
+          if (!contiguous)
+            gather_kblock(smem + OFF_SLOT + kb * kSlotBytes, ent_b, sidx, gw, nw, lane, kb, &c->full_g[kb]);
         }
         ++g;
       }
@@ -377,7 +387,8 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       const uint64_t dQ = smem_desc(smem_u32(smem + OFF_Q), 16, 1024, kLayoutSW128);
       const uint64_t dA2 = smem_desc(smem_u32(smem + OFF_SLOT), kSlotBytes, 1024, kLayoutSW128);
       const uint64_t dP0 = smem_desc(smem_u32(smem + OFF_P), 128, 2048, kLayoutNone);
-      int qc = 0, g = 0;
+      const bool gathered = p.ratio > 0 && p.idx != nullptr;
+      int qc = 0, g = 0, gg = 0, gt = 0;      // all tiles, gathered tiles, contiguous tiles
       bool ok = true;
       while (ok) {
         const int is = qc & 1;
@@ -391,9 +402,12 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         for (int j = 0; j < inf.tiles && ok; ++j) {
           const int sb = g & 1;
           const uint32_t s_tmem = tmem + 64 * sb;
+          const bool contiguous = j == inf.ent_tiles || !gathered;
+          uint64_t* fullb = contiguous ? c->full_t : c->full_g;
+          const uint32_t fpar = (contiguous ? gt : gg) & 1;
 #pragma unroll
           for (int kb = 0; kb < kSlots; ++kb) {
-            ok = ok && wait_ok(&c->full[kb], g & 1, c, p.status);
+            ok = ok && wait_ok(&fullb[kb], fpar, c, p.status);
             fence_proxy_async_smem();                 // cp.async writes -> tensor-core reads
             tc_fence_after();
 #pragma unroll
@@ -417,6 +431,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             umma_commit(&c->empty[2 * m]);
             umma_commit(&c->empty[2 * m + 1]);
           }
+          if (contiguous) ++gt; else ++gg;
           ++g;
         }
         umma_commit(&c->o_full);
@@ -731,7 +746,8 @@ cudaError_t launch_mqa_tc(const v4_config& cfg, const void* q, const void* kv_ro
 
 bool mqa_tc_supported(const v4_config& c) {
   return c.dtype == V4_BF16 && c.n_heads == kH && c.head_dim == kD && c.rope_dim == kR &&
-         c.window >= 1 && c.window <= kTileKeys && c.topk <= kMaxSel && (c.ratio == 0 || c.ratio >= 1);
+         c.window >= 1 && c.window <= kTileKeys && c.topk <= kMaxSel && (c.ratio == 0 || c.ratio >= 1) &&
+         (c.topk == 0 || c.ratio == 0 || c.seqlen / c.ratio <= 65536);    // 16-bit selection lists
 }
 
 }  // namespace v4
