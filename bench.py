@@ -31,9 +31,10 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 
 METRIC = "attention-layer fwd tokens/s at S=16K (CSA & HCA)"
-WORKLOAD = ("DeepSeek-V4-Flash attention layer pair fwd: CSA (ratio 4 overlapped, indexer 64x128 "
-            "fp32 scoring, top-512, window 128) + HCA (ratio 128, window 128), B=1, S=16384, "
-            "H=64, D=512, R=64, bf16")
+def workload(S):
+    return ("DeepSeek-V4-Flash attention layer pair fwd: CSA (ratio 4 overlapped, indexer 64x128 "
+            "fp32 scoring, top-512, window 128) + HCA (ratio 128, window 128), B=1, S=%d, "
+            "H=64, D=512, R=64, bf16" % S)
 
 
 # ---------------------------------------------------------------------------
@@ -67,9 +68,9 @@ def layer_work(p):
 # S=16384, from the ncu capture summarised in profiles/dram_traffic_s16384.md.
 # A figure is reported only while its kernel source is unchanged (sha256).
 NCU_TRAFFIC = {
-    "csa_attention": ("mqa_tc.cu", "a689d0f5330de780b5295c7c0cbc27d98f723eb9be288966fa52f75131138ad0", 2162458880),
-    "hca_attention": ("mqa_tc.cu", "a689d0f5330de780b5295c7c0cbc27d98f723eb9be288966fa52f75131138ad0", 2120372992),
-    "csa_indexer": ("indexer_tc.cu", "1590624bd98a7b0e06ee2c59fbc95e8cbb3e7a448f92f6d5b9ee4cfc7c7f5f4e", 399407872),
+    "csa_attention": ("mqa_tc.cu", "5a5a70b0bbb968ae9b20c6d0800bb8ddbc18dd340992e648205f3e125d6116e1", 2163579904),
+    "hca_attention": ("mqa_tc.cu", "5a5a70b0bbb968ae9b20c6d0800bb8ddbc18dd340992e648205f3e125d6116e1", 2124130560),
+    "csa_indexer": ("indexer_tc.cu", "1590624bd98a7b0e06ee2c59fbc95e8cbb3e7a448f92f6d5b9ee4cfc7c7f5f4e", 396634112),
 }
 
 
@@ -336,7 +337,7 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; activations unit-RMS N(0,1), q from a random rank-1024 path)",
-        "config": {"workload": WORKLOAD, "global_batch": ws_, "seq_len": S, "layers_per_step": 2,
+        "config": {"workload": workload(S), "global_batch": ws_, "seq_len": S, "layers_per_step": 2,
                    "parallelism": "replicas" if ws_ > 1 else "single",
                    "l2": "no flush: inputs larger than L2 (q and o 1 GiB per layer)"},
         "clocks": clocks, "gpu_launches": launches, "device_status": status,
@@ -493,7 +494,7 @@ def run_reference(args):
             "n_gpus": ws_, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(est * 1e3, 1), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": S, "layers_per_step": 2},
+            "config": {"workload": workload(S), "global_batch": 1, "seq_len": S, "layers_per_step": 2},
             "cpu_baseline": cb,
             "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
