@@ -11,11 +11,13 @@
 //   I[t, s] = sum_h w'[t,h] * max(D^T[s,(t,h)], 0)   for s < n_vis(t)
 //
 // One CTA owns a group of 4 consecutive queries at a time (its prepared
-// query rows, 64 KB, stay in shared memory) and streams the causally
-// visible entry tiles through a 4-stage TMA ring.  The accumulator is
+// query rows, 64 KB, stay in shared memory; two buffers, so the next group's
+// rows load while this group's tiles run) and streams the causally visible
+// entry tiles through a 3-stage TMA ring.  The accumulator is
 // double-buffered in TMEM (2 x 256 columns) so the epilogue of one tile (one
 // thread per entry: 4 x 64 TMEM columns, ReLU, weighted head sum, masked
-// store of the four scores) overlaps the MMAs of the next.
+// store of the four scores) overlaps the MMAs of the next; the scaled head
+// weights of the next group are fetched during the current one.
 // Warp roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
 // owner, warps 2-5 epilogue.  Groups are handed out round-robin, heaviest
 // (largest t) first.  Flash shapes only: Hi = 64, Di = 128, bf16.
@@ -35,24 +37,25 @@ namespace {
 constexpr int kHi = 64, kDi = 128;
 constexpr int kQG = 4;                                // queries per group
 constexpr int kThreads = 192;
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr uint32_t kABlock = 128 * 128;               // 128 entries x 64 dims x 2 B
 constexpr uint32_t kAStage = 2 * kABlock;             // both K-blocks of a tile
 constexpr uint32_t kBBlock = 256 * 128;               // 256 rows x 64 dims x 2 B
-constexpr uint32_t OFF_B = 0;                         // 2 K-blocks: 65536
-constexpr uint32_t OFF_A = 2 * kBBlock;               // stages: 4 x 32768
-constexpr uint32_t OFF_W = OFF_A + kStages * kAStage; // 196608: w' [4][64] fp32
-constexpr uint32_t OFF_CTL = OFF_W + kQG * kHi * 4;   // 197632
+constexpr uint32_t OFF_B = 0;                         // 2 buffers x 2 K-blocks: 131072
+constexpr uint32_t OFF_A = 4 * kBBlock;               // stages: 3 x 32768
+constexpr uint32_t OFF_W = OFF_A + kStages * kAStage; // 229376: w' [2][4][64] fp32
+constexpr uint32_t OFF_CTL = OFF_W + 2 * kQG * kHi * 4;   // 231424
 
 struct Ctl {
   uint64_t a_full[kStages], a_empty[kStages];
-  uint64_t b_full, b_empty;
+  uint64_t b_full[2], b_empty[2];
   uint64_t acc_full[2], acc_empty[2];
   uint64_t fin;
   uint32_t tmem_base;
   int abort;
 };
 constexpr uint32_t kSmemBytes = OFF_CTL + sizeof(Ctl);
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Params {
   const float* w;          // [B,S,64] unscaled weights
@@ -85,8 +88,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) { mbar_init(&c->a_full[i], 1); mbar_init(&c->a_empty[i], 1); }
-    mbar_init(&c->b_full, 1);
-    mbar_init(&c->b_empty, 1);
+    for (int i = 0; i < 2; ++i) { mbar_init(&c->b_full[i], 1); mbar_init(&c->b_empty[i], 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&c->acc_full[i], 1); mbar_init(&c->acc_empty[i], 128); }
     mbar_init(&c->fin, 1);
     c->abort = 0;
@@ -116,11 +118,13 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         int b, t0, tiles;
         group_of(gi, p, groups_per_b, b, t0, tiles);
         if (tiles == 0) continue;
-        if (gq >= 1) ok = mbar_wait(&c->b_empty, (gq - 1) & 1, &c->abort, p.status);
+        const int bb = gq & 1;
+        if (gq >= 2) ok = mbar_wait(&c->b_empty[bb], ((gq >> 1) - 1) & 1, &c->abort, p.status);
         if (!ok) break;
-        mbar_expect_tx(&c->b_full, 2 * kBBlock);
+        mbar_expect_tx(&c->b_full[bb], 2 * kBBlock);
         for (int kb = 0; kb < 2; ++kb)
-          tma_load_2d(smem + OFF_B + kb * kBBlock, &map_q, 64 * kb, (b * p.S + t0) * kHi, &c->b_full);
+          tma_load_2d(smem + OFF_B + (2 * bb + kb) * kBBlock, &map_q, 64 * kb, (b * p.S + t0) * kHi,
+                      &c->b_full[bb]);
         for (int j = 0; j < tiles && ok; ++j) {
           if (use >= kStages) ok = mbar_wait(&c->a_empty[st], ((use / kStages) - 1) & 1, &c->abort, p.status);
           if (!ok) break;
@@ -147,7 +151,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         int b, t0, tiles;
         group_of(gi, p, groups_per_b, b, t0, tiles);
         if (tiles == 0) continue;
-        ok = mbar_wait(&c->b_full, gq & 1, &c->abort, p.status);
+        const int bb = gq & 1;
+        ok = mbar_wait(&c->b_full[bb], (gq >> 1) & 1, &c->abort, p.status);
+        const uint64_t dB = dB0 + (uint64_t)((2 * bb * kBBlock) >> 4);
         for (int j = 0; j < tiles && ok; ++j) {
           const int ab = tile_ct & 1;
           ok = mbar_wait(&c->a_full[st], (use / kStages) & 1, &c->abort, p.status);
@@ -161,7 +167,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
               umma_f16_ss(d, dA + (uint64_t)((kb * kABlock + 32 * ks) >> 4),
-                          dB0 + (uint64_t)((kb * kBBlock + 32 * ks) >> 4), idesc, (kb | ks) != 0);
+                          dB + (uint64_t)((kb * kBBlock + 32 * ks) >> 4), idesc, (kb | ks) != 0);
           }
           umma_commit(&c->a_empty[st]);
           umma_commit(&c->acc_full[ab]);
@@ -169,7 +175,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           st = (st + 1) % kStages;
           ++tile_ct;
         }
-        umma_commit(&c->b_empty);
+        umma_commit(&c->b_empty[bb]);
         ++gq;
       }
       umma_commit(&c->fin);
@@ -182,20 +188,42 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     const int quarter = warp & 3;
     const int krow = 32 * quarter + lane;
     const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
+    // scaled weights of a group's 4 queries: each thread fetches two of the
+    // 256, one group ahead
+    float pf_w[2];
+    int pf_gi = -1;
+    auto fetch_w = [&](int g, float* out) {
+      int bg = 0, tg = 0, tl = 0;
+      if (g < total) group_of(g, p, groups_per_b, bg, tg, tl);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int i = ts + 128 * k;
+        const int t = tg + i / kHi;
+        out[k] = (g < total && t < p.S) ? p.w[((size_t)bg * p.S + t) * kHi + (i % kHi)] * p.wscale : 0.f;
+      }
+    };
+    fetch_w(blockIdx.x, pf_w);
+    pf_gi = blockIdx.x;
     int gq = 0, tile_ct = 0;
     for (int gi = blockIdx.x; gi < total; gi += gridDim.x) {
       int b, t0, tiles;
       group_of(gi, p, groups_per_b, b, t0, tiles);
       if (tiles == 0) continue;
-      // scaled weights of the group's 4 queries
-      if (gq >= 1) {
-        named_bar_sync(1, 128);       // every thread is done with the previous group's w'
+      float wv[2];
+      if (pf_gi == gi) {
+        wv[0] = pf_w[0];
+        wv[1] = pf_w[1];
+      } else {
+        fetch_w(gi, wv);
       }
-      for (int i = ts; i < kQG * kHi; i += 128) {
-        const int t = t0 + i / kHi;
-        s_w[i] = t < p.S ? p.w[((size_t)b * p.S + t) * kHi + (i % kHi)] * p.wscale : 0.f;
-      }
+      // buffer gq & 1 was last read for group gq-2, which every thread has
+      // finished before the barrier of group gq-1
+      float* sw = s_w + (gq & 1) * kQG * kHi;
+      sw[ts] = wv[0];
+      sw[ts + 128] = wv[1];
       named_bar_sync(1, 128);
+      fetch_w(gi + gridDim.x, pf_w);
+      pf_gi = gi + gridDim.x;
       for (int j = 0; j < tiles; ++j) {
         const int ab = tile_ct & 1;
         mbar_wait(&c->acc_full[ab], (tile_ct >> 1) & 1, &c->abort, p.status);
@@ -204,14 +232,16 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         float sc[kQG];
 #pragma unroll
         for (int q = 0; q < kQG; ++q) {
-          float v[kHi];
-          tmem_ld32(tmem + lane_base + 256 * ab + 64 * q, v);
-          tmem_ld32(tmem + lane_base + 256 * ab + 64 * q + 32, v + 32);
-          tmem_wait_ld();
-          const float* wq = s_w + q * kHi;
+          const float* wq = sw + q * kHi;
           float acc = 0.f;
 #pragma unroll
-          for (int h = 0; h < kHi; ++h) acc = fmaf(wq[h], fmaxf(v[h], 0.f), acc);
+          for (int half = 0; half < 2; ++half) {       // heads in order 0..63
+            float v[32];
+            tmem_ld32(tmem + lane_base + 256 * ab + 64 * q + 32 * half, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 32; ++h) acc = fmaf(wq[32 * half + h], fmaxf(v[h], 0.f), acc);
+          }
           sc[q] = acc;
         }
         tc_fence_before();

@@ -144,6 +144,56 @@ def test_indexer_topk_prepared(name, p, path):
     assert swaps <= max(2, B * S * K // 10000)
 
 
+@pytest.mark.parametrize("pattern", ["all_zero", "mostly_zero"])
+def test_topk_ties_and_crowded_bins(pattern):
+    """Selection when many scores are equal.  With all-zero index keys every
+    score is exactly 0: rows keep their K lowest indices (the tie rule), and
+    rows with more than 2048 visible entries put them all in one histogram bin
+    (the kernel's crowded-bin path).  With seven keys in eight zero, the K-th
+    score is a zero tied with ~2000 others, below the random scores of the
+    remaining keys."""
+    p = SI.preset("csa_bf16_4k", S=9000, q_mode="direct")
+    x, xd, f, fd = _setup(p, seed=4)
+    ikey = O.compress(np64(x["ickv"]), np64(x["icscore"]), np64(x["iape"]), None, f, p["ratio"],
+                      p["overlap"], 1e-6, hadamard=True, store_bf16=True)
+    if pattern == "all_zero":
+        ikey[:] = 0.0
+    else:
+        keep = np.arange(ikey.shape[1]) % 8 == 0
+        ikey[:, ~keep] = 0.0
+    iqp = O.indexer_query_prep(np64(x["iq"]), f, store_bf16=True)
+    cfg = V.config_from_preset(p)
+    B, S, K = p["B"], p["S"], p["K"]
+    idx = torch.empty(B, S, K, dtype=torch.int32, device="cuda")
+    V.v4_indexer_topk(cfg, torch.from_numpy(iqp).to(torch.bfloat16).cuda(), 1,
+                      torch.from_numpy(ikey).to(torch.bfloat16).cuda(), xd["w"], fd, idx, None,
+                      V.alloc_workspace(cfg))
+    torch.cuda.synchronize()
+    gi = idx.cpu().numpy()[0]
+    N = S // p["ratio"]
+    rows = np.unique(np.concatenate([np.linspace(2100, S - 1, 40).round().astype(int),
+                                     [2047, 2048, 4 * 2048 + 3, 4 * 2049 - 1, S - 1]]))
+    if pattern == "all_zero":
+        for t in rows:
+            nv = min(O.n_visible(int(t), p["ratio"]), N)
+            assert np.array_equal(gi[t], np.arange(K) if nv > K else
+                                  np.concatenate([np.arange(nv), -np.ones(K - nv, int)])), t
+        return
+    w = np64(x["w"])[0]
+    c = O.indexer_scale(p["Hi"], p["Di"])
+    sc = O.indexer_scores(iqp[:, rows], ikey, w[None, rows], p["ratio"], rows=rows, rows_only=True)[0]
+    check_topk_rows(gi[rows], sc, iqp[0], ikey[0], w, p["ratio"], K, rows, c)
+    for i, t in enumerate(rows):
+        nv = min(O.n_visible(int(t), p["ratio"]), N)
+        row = sc[i, :nv]
+        kth = np.sort(row)[::-1][K - 1]
+        if kth == 0.0:            # exact zeros: the lowest-index ones are kept
+            zeros = np.nonzero(row == 0.0)[0]
+            need = K - int(np.sum(row > 0.0))
+            kept = set(gi[t][gi[t] >= 0].tolist())
+            assert set(zeros[:need].tolist()) <= kept and not (set(zeros[need:].tolist()) & kept), t
+
+
 def _mqa_case(p, mode, sink, seed=0):
     x, xd, f, fd = _setup(p, seed=seed, sink=sink)
     bf = p["dtype"] == "bf16"
