@@ -18,8 +18,9 @@
 // thread per entry: 4 x 64 TMEM columns, ReLU, weighted head sum, masked
 // store of the four scores) overlaps the MMAs of the next; the scaled head
 // weights of the next group are fetched during the current one.
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
-// owner, warps 2-5 epilogue.  Groups are handed out round-robin, heaviest
+// Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
+// owner, warps 2-9 epilogue (two per TMEM lane quarter, each summing two of
+// the four queries: one warp per quarter could not keep up with the MMAs).  Groups are handed out round-robin, heaviest
 // (largest t) first.  Flash shapes only: Hi = 64, Di = 128, bf16.
 #include <cuda.h>
 #include <math.h>
@@ -36,7 +37,8 @@ namespace {
 
 constexpr int kHi = 64, kDi = 128;
 constexpr int kQG = 4;                                // queries per group
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = 256;
 constexpr int kStages = 3;
 constexpr uint32_t kABlock = 128 * 128;               // 128 entries x 64 dims x 2 B
 constexpr uint32_t kAStage = 2 * kABlock;             // both K-blocks of a tile
@@ -89,7 +91,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) { mbar_init(&c->a_full[i], 1); mbar_init(&c->a_empty[i], 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&c->b_full[i], 1); mbar_init(&c->b_empty[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&c->acc_full[i], 1); mbar_init(&c->acc_empty[i], 128); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&c->acc_full[i], 1); mbar_init(&c->acc_empty[i], kEpiThreads); }
     mbar_init(&c->fin, 1);
     c->abort = 0;
     fence_barrier_init();
@@ -184,54 +186,45 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int ts = threadIdx.x - 64;
+    const int ts = threadIdx.x - 64;          // 0..255
     const int quarter = warp & 3;
+    const int q0 = 2 * ((warp - 2) >> 2);     // this warp's queries q0, q0+1
     const int krow = 32 * quarter + lane;
     const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
-    // scaled weights of a group's 4 queries: each thread fetches two of the
-    // 256, one group ahead
-    float pf_w[2];
+    // scaled weight ts of a group (query ts/64, head ts%64), one group ahead
+    float pf_w = 0.f;
     int pf_gi = -1;
-    auto fetch_w = [&](int g, float* out) {
+    auto fetch_w = [&](int g) -> float {
       int bg = 0, tg = 0, tl = 0;
-      if (g < total) group_of(g, p, groups_per_b, bg, tg, tl);
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int i = ts + 128 * k;
-        const int t = tg + i / kHi;
-        out[k] = (g < total && t < p.S) ? p.w[((size_t)bg * p.S + t) * kHi + (i % kHi)] * p.wscale : 0.f;
-      }
+      if (g >= total) return 0.f;
+      group_of(g, p, groups_per_b, bg, tg, tl);
+      const int t = tg + ts / kHi;
+      return t < p.S ? p.w[((size_t)bg * p.S + t) * kHi + (ts % kHi)] * p.wscale : 0.f;
     };
-    fetch_w(blockIdx.x, pf_w);
+    pf_w = fetch_w(blockIdx.x);
     pf_gi = blockIdx.x;
     int gq = 0, tile_ct = 0;
     for (int gi = blockIdx.x; gi < total; gi += gridDim.x) {
       int b, t0, tiles;
       group_of(gi, p, groups_per_b, b, t0, tiles);
       if (tiles == 0) continue;
-      float wv[2];
-      if (pf_gi == gi) {
-        wv[0] = pf_w[0];
-        wv[1] = pf_w[1];
-      } else {
-        fetch_w(gi, wv);
-      }
+      const float wv = pf_gi == gi ? pf_w : fetch_w(gi);
       // buffer gq & 1 was last read for group gq-2, which every thread has
       // finished before the barrier of group gq-1
       float* sw = s_w + (gq & 1) * kQG * kHi;
-      sw[ts] = wv[0];
-      sw[ts + 128] = wv[1];
-      named_bar_sync(1, 128);
-      fetch_w(gi + gridDim.x, pf_w);
+      sw[ts] = wv;
+      named_bar_sync(1, kEpiThreads);
+      pf_w = fetch_w(gi + gridDim.x);
       pf_gi = gi + gridDim.x;
       for (int j = 0; j < tiles; ++j) {
         const int ab = tile_ct & 1;
         mbar_wait(&c->acc_full[ab], (tile_ct >> 1) & 1, &c->abort, p.status);
         tc_fence_after();
         const int s = 128 * j + krow;
-        float sc[kQG];
+        float sc[2];
 #pragma unroll
-        for (int q = 0; q < kQG; ++q) {
+        for (int qq = 0; qq < 2; ++qq) {
+          const int q = q0 + qq;
           const float* wq = sw + q * kHi;
           float acc = 0.f;
 #pragma unroll
@@ -242,14 +235,14 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 #pragma unroll
             for (int h = 0; h < 32; ++h) acc = fmaf(wq[32 * half + h], fmaxf(v[h], 0.f), acc);
           }
-          sc[q] = acc;
+          sc[qq] = acc;
         }
         tc_fence_before();
         mbar_arrive(&c->acc_empty[ab]);
 #pragma unroll
-        for (int q = 0; q < kQG; ++q) {
-          const int t = t0 + q;
-          if (t < p.S && s < min((t + 1) / p.ratio, p.N)) p.scores[((size_t)b * p.S + t) * p.N + s] = sc[q];
+        for (int qq = 0; qq < 2; ++qq) {
+          const int t = t0 + q0 + qq;
+          if (t < p.S && s < min((t + 1) / p.ratio, p.N)) p.scores[((size_t)b * p.S + t) * p.N + s] = sc[qq];
         }
         ++tile_ct;
       }
