@@ -33,10 +33,10 @@
 // sub-partition).  Rotations read a per-position cos/sin table built once per
 // call.
 //
-// Warp roles (256 threads): warp 0 producer (per-query selection list, query
+// Warp roles (384 threads): warp 0 producer (per-query selection list, query
 // rows and contiguous tiles by TMA, one third of the gathers), warp 1 MMA
-// issuer and TMEM owner, warps 2-3 gather the other two thirds, warps 4-7
-// softmax + epilogue (one TMEM lane quarter each).
+// issuer and TMEM owner, warps 2-3 gather the other two thirds, warps 4-11
+// softmax + epilogue (two per TMEM lane quarter, 32 heads each).
 #include <cuda.h>
 #include <math.h>
 
@@ -51,7 +51,8 @@ using namespace sm100;
 namespace {
 
 constexpr int kH = 64, kD = 512, kR = 64;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
+constexpr int kSoftThreads = 256;                 // warps 4-11
 constexpr int kGatherLanes = 96;                  // warps 0, 2, 3
 constexpr int kTileKeys = 128;
 constexpr int kSlots = 8;                         // one tile: 8 K-blocks of 64 dims
@@ -169,16 +170,16 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     mbar_init(&c->list_free[0], 64);
     mbar_init(&c->list_free[1], 64);
     mbar_init(&c->q_full, 1);
-    mbar_init(&c->q_ready, 128);
+    mbar_init(&c->q_ready, kSoftThreads);
     mbar_init(&c->q_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c->s_full[i], 1);
-      mbar_init(&c->p_ready[i], 128);
+      mbar_init(&c->p_ready[i], kSoftThreads);
       mbar_init(&c->info_full[i], 1);
-      mbar_init(&c->info_empty[i], 1 + 128 + 64);
+      mbar_init(&c->info_empty[i], 1 + kSoftThreads + 64);
     }
     mbar_init(&c->o_full, 1);
-    mbar_init(&c->o_empty, 128);
+    mbar_init(&c->o_empty, kSoftThreads);
     mbar_init(&c->fin, 1);
     c->abort = 0;
     c->redo = 0;
@@ -444,8 +445,12 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int ts = threadIdx.x - 128;         // 0..127
+    // Eight warps: two per TMEM lane quarter, head halves hh = 0 / 1 (heads
+    // 32*hh .. 32*hh+31 of every row the quarter holds).
+    const int ts = threadIdx.x - 128;         // 0..255
     const int quarter = warp & 3;             // TMEM lane quarter of this warp
+    const int hh = (warp - 4) >> 2;           // head half
+    const int h0 = 32 * hh;
     const int krow = 32 * quarter + lane;     // key row / dim row owned in TMEM
     const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
     const float log2e = 1.4426950408889634f;
@@ -458,27 +463,29 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       inf = c->info[is];
       mbar_arrive(&c->info_empty[is]);
       if (ts == 0) c->decision = (c->abort || inf.done) ? 1 : 0;
-      named_bar_sync(1, 128);
+      named_bar_sync(1, kSoftThreads);
       const bool more = c->decision == 0;
-      named_bar_sync(1, 128);
+      named_bar_sync(1, kSoftThreads);
       return more;
     };
     // Rotate the last 64 dims of each head of query qc at position t, take
     // the head norms of the stored bf16 values and publish the shift table.
+    // Four threads per head: two 16-byte chunks of the rotated K-block and
+    // two K-blocks of the norm each.
     auto setup_query = [&](int qc, const QInfo& inf) {
-      const int h = ts >> 1, half = ts & 1;
-      // cos/sin of this thread's 16 rotation pairs, fetched before the wait
-      float4 csv[8];
+      const int h = ts >> 2, part = ts & 3;
+      // cos/sin of this thread's 8 rotation pairs, fetched before the wait
+      float4 csv[4];
       {
-        const float4* csp = reinterpret_cast<const float4*>(p.rope_cs + (size_t)inf.t * (kR / 2) + 16 * half);
+        const float4* csp = reinterpret_cast<const float4*>(p.rope_cs + (size_t)inf.t * (kR / 2) + 8 * part);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) csv[i] = csp[i];
+        for (int i = 0; i < 4; ++i) csv[i] = csp[i];
       }
       wait_ok(&c->q_full, qc & 1, c, p.status);
       uint8_t* qrow = smem + OFF_Q + 7 * kQBlockBytes + h * 128;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const int ch = 4 * half + cc;                        // 16-byte chunk of dims 448..511
+      for (int cc = 0; cc < 2; ++cc) {
+        const int ch = 2 * part + cc;                        // 16-byte chunk of dims 448..511
         uint4* ptr = reinterpret_cast<uint4*>(qrow + ((ch ^ (h & 7)) * 16));
         uint4 u = *ptr;
         __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&u);
@@ -492,15 +499,15 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         }
         *ptr = u;
       }
-      __syncwarp();
+      __syncwarp();                            // the head's four threads share this warp
       float ss4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const int kb = 4 * half + kk;
+      for (int kk = 0; kk < 2; ++kk) {
+        const int kb = 2 * part + kk;
         const uint4* r = reinterpret_cast<const uint4*>(smem + OFF_Q + kb * kQBlockBytes + h * 128);
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
-          uint4 u = r[cc ^ (h & 7)];            // spread the 16 heads of a warp over the banks
+          uint4 u = r[cc ^ (h & 7)];            // spread the heads of a warp over the banks
           const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -512,14 +519,15 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       }
       float ss = (ss4[0] + ss4[1]) + (ss4[2] + ss4[3]);
       ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-      if (half == 0) {
+      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+      if (part == 0) {
         float m = p.scale * sqrtf(ss) * inf.kmax;
         m = m * (1.0f + 1e-5f) + 1e-6f;                     // covers rounding of the bound itself
         if (p.sink != nullptr) m = fmaxf(m, p.sink[h]);
         c->mlog2[qc & 1][h] = m * log2e;
       }
       fence_proxy_async_smem();
-      named_bar_sync(1, 128);
+      named_bar_sync(1, kSoftThreads);
       mbar_arrive(&c->q_ready);
     };
 
@@ -528,10 +536,10 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     bool more = next_query(0, inf);
     if (more) setup_query(0, inf);
     while (more) {
-      const float* mlog2 = c->mlog2[qc & 1];
+      const float* mlog2 = c->mlog2[qc & 1] + h0;
       const int t = inf.t, b = inf.b;
       const int nk_total = inf.n_ent + (t - inf.w_lo + 1);
-      float lsum0 = 0.f, lsum1 = 0.f;           // this warp's denominators of heads 2*lane, 2*lane+1
+      float lsum = 0.f;                         // this warp's denominator of head h0 + lane
       for (int j = 0; j < inf.tiles; ++j) {
         const int sb = g & 1;
         bool valid;
@@ -543,20 +551,20 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         }
         wait_ok(&c->s_full[sb], (g >> 1) & 1, c, p.status);
         tc_fence_after();
-        float v[kH];
-        tmem_ld32(tmem + lane_base + 64 * sb, v);
-        tmem_ld32(tmem + lane_base + 64 * sb + 32, v + 32);
+        float v[32];
+        tmem_ld32(tmem + lane_base + 64 * sb + h0, v);
         tmem_wait_ld();
-        uint32_t pk[kH / 2];
+        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < kH / 2; ++i) {
+        for (int i = 0; i < 16; ++i) {
           float x0 = valid ? ex2_approx(fmaf(v[2 * i], c1, -mlog2[2 * i])) : 0.f;
           float x1 = valid ? ex2_approx(fmaf(v[2 * i + 1], c1, -mlog2[2 * i + 1])) : 0.f;
           pk[i] = pack_bf16x2(x0, x1);
         }
-        uint8_t* prow = smem + OFF_P + sb * kPBytes + krow * 16;
+        // P^T [8-head column block][key]: this half's four blocks
+        uint8_t* prow = smem + OFF_P + sb * kPBytes + krow * 16 + (4 * hh) * 2048;
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
+        for (int cc = 0; cc < 4; ++cc)
           *reinterpret_cast<uint4*>(prow + cc * 2048) =
               make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
         fence_proxy_async_smem();
@@ -564,19 +572,19 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         mbar_arrive(&c->p_ready[sb]);
         // Sum the warp's 32 rows per head while the products run: five
         // butterfly rounds, each lane keeping half of its heads, leave lane L
-        // with heads 2L and 2L+1 (pk[i] packs heads 2i, 2i+1).
+        // with head h0 + L (pk[i] packs heads h0 + 2i, h0 + 2i + 1).
         {
-          float r[32];
+          float r[16];
           const bool up = (lane & 16) != 0;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const uint32_t keep = up ? pk[16 + i] : pk[i];
-            const uint32_t got = __shfl_xor_sync(0xffffffffu, up ? pk[i] : pk[16 + i], 16);
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t keep = up ? pk[8 + i] : pk[i];
+            const uint32_t got = __shfl_xor_sync(0xffffffffu, up ? pk[i] : pk[8 + i], 16);
             r[2 * i] = __uint_as_float(keep << 16) + __uint_as_float(got << 16);
             r[2 * i + 1] = __uint_as_float(keep & 0xFFFF0000u) + __uint_as_float(got & 0xFFFF0000u);
           }
 #pragma unroll
-          for (int o = 8, w = 16; o >= 1; o >>= 1, w >>= 1) {
+          for (int o = 8, w = 8; o >= 1; o >>= 1, w >>= 1) {
             const bool hi = (lane & o) != 0;
 #pragma unroll
             for (int i = 0; i < w; ++i) {
@@ -585,8 +593,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
               r[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
             }
           }
-          lsum0 += r[0];
-          lsum1 += r[1];
+          lsum += r[0];
         }
         ++g;
       }
@@ -609,13 +616,14 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       wait_ok(&c->o_full, qc & 1, c, p.status);
       tc_fence_after();
       // per-head scalars, one head per thread; the P buffers are idle here:
-      // [0,256) the four warp partials of l, [256,320) 1/l
+      // [0,256) the four quarter partials of l, [256,320) 1/l
       float* hs = reinterpret_cast<float*>(smem + OFF_P);
-      *reinterpret_cast<float2*>(hs + 64 * quarter + 2 * lane) = make_float2(lsum0, lsum1);
-      named_bar_sync(1, 128);
+      const float* mlog2_all = c->mlog2[qc & 1];
+      hs[64 * quarter + h0 + lane] = lsum;
+      named_bar_sync(1, kSoftThreads);
       if (ts < kH) {
         float l = (hs[ts] + hs[64 + ts]) + (hs[128 + ts] + hs[192 + ts]);
-        const float m = mlog2[ts] * 0.6931471805599453f;
+        const float m = mlog2_all[ts] * 0.6931471805599453f;
         if (p.sink != nullptr) l += expf(p.sink[ts] - m);
         // too little mass under the bound: exp underflow may have lost keys
         const bool bad = !(l >= (float)nk_total * 1.0e-26f) || !(l < INFINITY);
@@ -623,16 +631,16 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         if (p.lse) p.lse[((size_t)b * p.S + t) * kH + ts] = m + logf(l);
         hs[256 + ts] = 1.0f / l;
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1, kSoftThreads);
       if (ts == 0 && c->redo) {                 // queue the query once for the running-max kernel
         const int slot = atomicAdd(&p.counters[1], 1);
         p.counters[2 + slot] = b * p.S + t;
         c->redo = 0;
       }
-      float inv_l[kH];
+      float inv_l[32];
 #pragma unroll
-      for (int i = 0; i < kH; i += 4) {
-        const float4 v4 = *reinterpret_cast<const float4*>(hs + 256 + i);
+      for (int i = 0; i < 32; i += 4) {
+        const float4 v4 = *reinterpret_cast<const float4*>(hs + 256 + h0 + i);
         inv_l[i] = v4.x;
         inv_l[i + 1] = v4.y;
         inv_l[i + 2] = v4.z;
@@ -640,30 +648,29 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       }
       // o[t, h, 128m + krow]: for each head the 32 lanes of a warp write 64
       // contiguous bytes
-      bf16* obase = p.o + ((size_t)b * p.S + t) * kH * kD + krow;
+      bf16* obase = p.o + ((size_t)b * p.S + t) * kH * kD + (size_t)h0 * kD + krow;
       for (int m = 0; m < 4; ++m) {
-        float v[kH];
-        tmem_ld32(tmem + lane_base + 128 + 64 * m, v);
-        tmem_ld32(tmem + lane_base + 128 + 64 * m + 32, v + 32);
+        float v[32];
+        tmem_ld32(tmem + lane_base + 128 + 64 * m + h0, v);
         tmem_wait_ld();
         if (m == 3) {
           tc_fence_before();
           mbar_arrive(&c->o_empty);
         }
 #pragma unroll
-        for (int i = 0; i < kH; ++i) v[i] *= inv_l[i];
+        for (int i = 0; i < 32; ++i) v[i] *= inv_l[i];
         if (m == 3 && quarter >= 2) {
           // rotated dims 448..511: the partner of each pair is the
           // neighbouring lane; the values cross through the idle second P
-          // buffer (sixteen 16-byte stores and loads instead of 64 shuffles)
-          float4* xb = reinterpret_cast<float4*>(smem + OFF_P + kPBytes + (quarter - 2) * (kPBytes / 2));
+          // buffer (eight 16-byte stores and loads instead of 32 shuffles)
+          float4* xb = reinterpret_cast<float4*>(smem + OFF_P + kPBytes + (2 * (quarter - 2) + hh) * (kPBytes / 4));
 #pragma unroll
-          for (int c4 = 0; c4 < kH / 4; ++c4)
+          for (int c4 = 0; c4 < 8; ++c4)
             xb[c4 * 32 + lane] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
           __syncwarp();
           const bool odd = lane & 1;
 #pragma unroll
-          for (int c4 = 0; c4 < kH / 4; ++c4) {
+          for (int c4 = 0; c4 < 8; ++c4) {
             const float4 o4 = xb[c4 * 32 + (lane ^ 1)];
             const float oth[4] = {o4.x, o4.y, o4.z, o4.w};
 #pragma unroll
@@ -674,9 +681,9 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           }
         }
 #pragma unroll
-        for (int i = 0; i < kH; ++i) obase[(size_t)i * kD + 128 * m] = __float2bfloat16_rn(v[i]);
+        for (int i = 0; i < 32; ++i) obase[(size_t)i * kD + 128 * m] = __float2bfloat16_rn(v[i]);
       }
-      named_bar_sync(1, 128);                   // the scalars in the P buffer are read; P may be rewritten
+      named_bar_sync(1, kSoftThreads);          // the scalars in the P buffers are read; P may be rewritten
       inf = nxt;
       ++qc;
     }
