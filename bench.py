@@ -68,9 +68,9 @@ def layer_work(p):
 # S=16384, from the ncu capture summarised in profiles/dram_traffic_s16384.md.
 # A figure is reported only while its kernel source is unchanged (sha256).
 NCU_TRAFFIC = {
-    "csa_attention": ("mqa_tc.cu", "5a5a70b0bbb968ae9b20c6d0800bb8ddbc18dd340992e648205f3e125d6116e1", 2163579904),
-    "hca_attention": ("mqa_tc.cu", "5a5a70b0bbb968ae9b20c6d0800bb8ddbc18dd340992e648205f3e125d6116e1", 2124130560),
-    "csa_indexer": ("indexer_tc.cu", "1590624bd98a7b0e06ee2c59fbc95e8cbb3e7a448f92f6d5b9ee4cfc7c7f5f4e", 396634112),
+    "csa_attention": ("mqa_tc.cu", "f9e219a7c7c38ecc68047a3c7f1f6abdbf9da1159db2301cfe19ddc8ebf67b4c", 2162200320),
+    "hca_attention": ("mqa_tc.cu", "f9e219a7c7c38ecc68047a3c7f1f6abdbf9da1159db2301cfe19ddc8ebf67b4c", 2123518720),
+    "csa_indexer": ("indexer_tc.cu", "ecff08a0aaf63cfbe4cb2a13b428f4d1b048212bf3642ec0a93bc2a95ab9a281", 395812352),
 }
 
 

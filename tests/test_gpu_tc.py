@@ -163,6 +163,19 @@ def test_full_size_layer_sampled_rows(name):
             total += len(r)
         assert agree >= 0.99 * total, (agree, total)
         idx_rows = sel["idx"]
+        # stage-wise: the oracle's scores fed the GPU's own prepared queries
+        # and index keys select the same sets outside the tie band
+        iqp_g = V.v4_indexer_prep(cfg, x["iq"], xd["inv_freq"], torch.empty_like(x["iq"]))
+        iqp_rows = np64(iqp_g[:, torch.from_numpy(rows).cuda()])
+        ikey_g = np64(outs["ikey"])
+        sc = O.indexer_scores(iqp_rows, ikey_g, w_rows, p["ratio"], rows=rows, rows_only=True)[0]
+        iqp_full = np.zeros((S,) + iqp_rows.shape[2:])
+        iqp_full[rows] = iqp_rows[0]
+        w_full = np.zeros((S, p["Hi"]))
+        w_full[rows] = w_rows[0]
+        swaps = check_topk_rows(gi, sc, iqp_full, ikey_g[0], w_full, p["ratio"], K, rows,
+                                O.indexer_scale(p["Hi"], p["Di"]))
+        assert swaps <= 2, swaps
     q_rows = np64(x["q"][:, torch.from_numpy(rows).cuda()])
     # the oracle attends with its own entries and its own selection
     ro, rl = O.sparse_mqa(q_rows, np64(x["kv"]), ent, idx_rows, None, f, p["ratio"], p["W"],
