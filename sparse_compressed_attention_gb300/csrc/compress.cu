@@ -352,6 +352,80 @@ __global__ void indexer_prep_kernel(const T* __restrict__ iq, const float2* __re
   if (live) store8(out + row * Di + lane * 8, e);
 }
 
+// The same transform for Di = 128 with four lanes per row: a lane holds 32
+// consecutive elements, so five butterfly stages run inside the thread and
+// only two cross lanes (a quarter of the shuffles of the kernel above), and
+// each thread has 64 bytes (bf16) in flight.
+template <typename T>
+__global__ void __launch_bounds__(256)
+indexer_prep_d128_kernel(const T* __restrict__ iq, const float2* __restrict__ cs_table,
+                         const float* __restrict__ inv_freq, T* __restrict__ out,
+                         long long rows, int S, int Hi, int R) {
+  constexpr int Di = 128, kLanes = 4, kPer = 32;
+  const long long gt = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const long long row = gt / kLanes;
+  const int lane = (int)(gt % kLanes);
+  const bool live = row < rows;
+  const int c0 = lane * kPer;
+  float e[kPer];
+#pragma unroll
+  for (int q = 0; q < kPer / 8; ++q) {
+    if (live) load8(iq + row * Di + c0 + 8 * q, e + 8 * q);
+    else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) e[8 * q + k] = 0.f;
+    }
+  }
+  if (live && c0 + kPer > Di - R) {
+    const long long t = (row / Hi) % S;
+#pragma unroll
+    for (int k = 0; k < kPer / 2; ++k) {
+      const int c = c0 + 2 * k;
+      if (c >= Di - R) {
+        const int j = (c - (Di - R)) / 2;
+        float cs, sn;
+        if (cs_table) {
+          const float2 v = cs_table[t * (R / 2) + j];
+          cs = v.x;
+          sn = v.y;
+        } else {
+          rope_cos_sin(t, inv_freq[j], &cs, &sn);
+        }
+        rot_pair(e[2 * k], e[2 * k + 1], cs, sn);
+      }
+    }
+  }
+  // in-thread butterflies (h = 1 .. 16)
+#pragma unroll
+  for (int h = 1; h < kPer; h <<= 1) {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      if ((k & h) == 0) {
+        const float a = e[k], b = e[k + h];
+        e[k] = a + b;
+        e[k + h] = a - b;
+      }
+    }
+  }
+  // cross-lane butterflies (h = 32, 64)
+#pragma unroll
+  for (int hl = 1; hl < kLanes; hl <<= 1) {
+    const bool upper = (lane & hl) != 0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const float other = __shfl_xor_sync(0xffffffffu, e[k], hl);
+      e[k] = upper ? (other - e[k]) : (e[k] + other);
+    }
+  }
+  const float hs = 1.0f / sqrtf((float)Di);
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) e[k] *= hs;
+  if (live) {
+#pragma unroll
+    for (int q = 0; q < kPer / 8; ++q) store8(out + row * Di + c0 + 8 * q, e + 8 * q);
+  }
+}
+
 template <typename T>
 cudaError_t compress_t(const v4_config& c, const void* ckv, const void* cscore, const float* ape,
                        const float* norm_w, const float* inv_freq, int dim, int hadamard,
@@ -440,8 +514,19 @@ cudaError_t launch_key_prep(const v4_config& c, const void* kv, const void* ent,
 cudaError_t launch_indexer_prep(const v4_config& c, const void* iq, const float2* cs_table,
                                 const float* inv_freq, void* iqp, cudaStream_t st) {
   const long long rows = (long long)c.batch * c.seqlen * c.idx_heads;
-  const int lanes = c.idx_dim / 8;
   const int threads = 256;
+  if (c.idx_dim == 128) {
+    const long long blocks = (rows * 4 + threads - 1) / threads;
+    if (c.dtype == V4_BF16)
+      indexer_prep_d128_kernel<bf16><<<(unsigned)blocks, threads, 0, st>>>(
+          (const bf16*)iq, cs_table, inv_freq, (bf16*)iqp, rows, c.seqlen, c.idx_heads, c.rope_dim);
+    else
+      indexer_prep_d128_kernel<float><<<(unsigned)blocks, threads, 0, st>>>(
+          (const float*)iq, cs_table, inv_freq, (float*)iqp, rows, c.seqlen, c.idx_heads, c.rope_dim);
+    note_launch();
+    return cudaGetLastError();
+  }
+  const int lanes = c.idx_dim / 8;
   const long long blocks = (rows * lanes + threads - 1) / threads;
   if (c.dtype == V4_BF16)
     indexer_prep_kernel<bf16><<<(unsigned)blocks, threads, 0, st>>>(
