@@ -410,6 +410,135 @@ def run_e2e(args, layers, dev):
 
 
 # ---------------------------------------------------------------------------
+# Other workloads (not the default line): the 43-layer Flash stack with the
+# grouped output projection, and a single CSA layer (the long-context case)
+# ---------------------------------------------------------------------------
+STACK_ORDER = ["swa", "swa"] + ["csa", "hca"] * 20 + ["csa"]      # 2 SWA + 21 CSA + 20 HCA
+
+
+def make_stack_layer(kind, B, S, device, seed):
+    import torch
+
+    import seeded_inputs as SI
+    import sparse_compressed_attention_gb300 as V
+    name = {"swa": "swa_bf16_16k", "csa": "csa_bf16_16k", "hca": "hca_bf16_16k"}[kind]
+    p = SI.preset(name, B=B, S=S)
+    x = SI.make_layer_inputs(p, device, seed=seed, wo_a=True)
+    yarn = p["yarn"]
+    x["inv_freq"] = V.v4_rope_inv_freq(p["theta"], p["R"], yarn, SI.YARN_ORIGINAL_LEN if yarn > 1 else 0,
+                                       SI.YARN_BETA_FAST, SI.YARN_BETA_SLOW).to(device)
+    cfg = V.config_from_preset(p)
+    H = p["H"]
+    outs = {"o": torch.empty_like(x["q"]), "lse": torch.empty(B, S, H, device=device),
+            "y": torch.empty(B, S, x["wo_a"].shape[0] * x["wo_a"].shape[2], dtype=x["q"].dtype, device=device)}
+    if p["K"] > 0:
+        outs["idx"] = torch.empty(B, S, p["K"], dtype=torch.int32, device=device)
+    return dict(name=kind, p=p, x=x, outs=outs, cfg=cfg, ws=V.alloc_workspace(cfg, device))
+
+
+def run_workload(args):
+    """--workload stack | csa: one JSON line for that workload (1 GPU)."""
+    import torch
+
+    import sparse_compressed_attention_gb300 as V
+    from sparse_compressed_attention_gb300 import build as Bld
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    Bld.build()
+    V.lib()
+    S = args.seq
+    if args.workload == "stack":
+        B = 2
+        kinds = {k: make_stack_layer(k, B, S, dev, seed=2000 + i) for i, k in enumerate(("swa", "csa", "hca"))}
+        order = [kinds[k] for k in STACK_ORDER]
+        metric = "Flash stack fwd tokens/s (43 layers: 2 SWA + 21 CSA + 20 HCA, grouped wo_a)"
+        wl = ("DeepSeek-V4-Flash 43-layer attention stack fwd with the 8-group x 1024 grouped O projection, "
+              "B=%d, S=%d, H=64, D=512, R=64, bf16" % (B, S))
+    else:
+        B = 1
+        order = [make_layer("csa_bf16_16k", S, dev, seed=3000)]
+        for L in order:
+            L["name"] = "csa"
+        metric = "CSA layer fwd tokens/s at S=%d" % S
+        wl = ("DeepSeek-V4-Flash CSA layer fwd (ratio 4 overlapped, indexer 64x128 fp32 scoring, top-512, "
+              "window 128), B=1, S=%d, H=64, D=512, R=64, bf16" % S)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        for L in order:
+            run_layer(L)
+    torch.cuda.synchronize(dev)
+    clk = ClockSampler(smi_index(0))
+    clk.start()
+    t_pre = time.time()
+    while time.time() - t_pre < 0.3:
+        for L in order:
+            run_layer(L)
+        torch.cuda.synchronize(dev)
+    V.v4_profile_enable(True)
+    launches0 = V.v4_launch_count()
+    marks = []
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        for L in order:
+            run_layer(L)
+            marks.append((L["name"], V.v4_profile_count()))
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    launches = V.v4_launch_count() - launches0
+    V.v4_profile_enable(False)
+    clk.stop()
+    ms = ev0.elapsed_time(ev1)
+    recs = V.v4_profile_records()
+    per, start = {}, 0
+    for name, end in marks:
+        for kind, t in recs[start:end]:
+            per.setdefault((name, kind), []).append(t)
+        start = end
+    kern = {"%s/%s" % k: {"launches": len(v), "avg_ms": sum(v) / len(v), "total_ms": sum(v)}
+            for k, v in per.items()}
+    peaks = load_peaks()
+    csa = next(L for L in order if L["name"] == "csa")
+    wk = layer_work(csa["p"])
+    roof, other = None, []
+    a = per.get(("csa", "attention"), [])
+    if a:
+        a_ms = sum(a) / len(a)
+        tf = wk["attn_flops"] / (a_ms / 1e3) / 1e12
+        roof = {"kernel": "csa attention", "bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16"],
+                "unit": "TFLOP/s", "frac": round(tf / peaks["bf16"], 4), "traffic": None,
+                "flops_per_launch": wk["attn_flops"], "avg_launch_ms": round(a_ms, 4)}
+    isc = per.get(("csa", "indexer_scores"), [])
+    if isc:
+        a_ms = sum(isc) / len(isc)
+        tf = wk["idx_flops"] / (a_ms / 1e3) / 1e12
+        other.append({"kernel": "csa indexer scores", "bound": "tensor", "achieved": round(tf, 2),
+                      "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": round(tf / peaks["bf16"], 4),
+                      "flops_per_launch": wk["idx_flops"], "avg_launch_ms": round(a_ms, 4)})
+    op = [t for (n, k), v in per.items() if k == "o_proj" for t in v]
+    if op:
+        a_ms = sum(op) / len(op)
+        fl = 2.0 * B * S * 8 * 4096 * 1024
+        tf = fl / (a_ms / 1e3) / 1e12
+        other.append({"kernel": "grouped wo_a projection", "bound": "tensor", "achieved": round(tf, 2),
+                      "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": round(tf / peaks["bf16"], 4),
+                      "flops_per_launch": fl, "avg_launch_ms": round(a_ms, 4)})
+    line = {"metric": metric, "value": round(B * S * args.steps / (ms / 1e3), 1), "unit": "tokens/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; activations unit-RMS N(0,1), q from a random rank-1024 path)",
+            "config": {"workload": wl, "global_batch": B, "seq_len": S, "layers_per_step": len(order)},
+            "clocks": clk.summary(t0, t1), "gpu_launches": launches,
+            "device_status": V.v4_get_device_status(), "roofline": roof, "roofline_other": other,
+            "kernels": kern}
+    print(json.dumps(line), flush=True)
+
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle on a bounded sample (rank 0 only)
 # ---------------------------------------------------------------------------
 def oracle_sample(inputs_by_layer, rows_per_layer):
