@@ -185,10 +185,10 @@ static v4_status check_ws(const v4_config& c, void* ws, size_t bytes) {
 // and the layer call.
 // ---------------------------------------------------------------------------
 static v4_status do_compress(const v4_config& c, const void* ckv, const void* cs, const float* ape,
-                             const float* nw, const float* f, int dim, int had, void* out,
-                             cudaStream_t st) {
+                             const float* nw, const float* f, const float2* table, int dim, int had,
+                             void* out, cudaStream_t st) {
   ProfScope ps(K_COMPRESS, st);
-  CU(launch_compress(c, ckv, cs, ape, nw, f, dim, had, out, st), "compress kernel");
+  CU(launch_compress(c, ckv, cs, ape, nw, f, table, dim, had, out, st), "compress kernel");
   return V4_OK;
 }
 
@@ -337,7 +337,7 @@ v4_status v4_compress(const v4_config* cfg, const void* ckv, const void* cscore,
   OPT(norm_w, "norm_w");
   if (cfg->rope_dim > 0) REQ(inv_freq, "inv_freq");
   if (cfg->seqlen / cfg->ratio > 0) REQ(out, "out");
-  return do_compress(*cfg, ckv, cscore, ape, norm_w, inv_freq, dim, hadamard ? 1 : 0, out,
+  return do_compress(*cfg, ckv, cscore, ape, norm_w, inv_freq, nullptr, dim, hadamard ? 1 : 0, out,
                      (cudaStream_t)stream);
 }
 
@@ -476,13 +476,14 @@ v4_status v4_attn_layer_fwd(const v4_config* cfg, const v4_layer_inputs* in, v4_
   s = do_rope_table(c, in->inv_freq, ws, st);
   if (s != V4_OK) return s;
   if (comp) {
-    s = do_compress(c, in->ckv, in->cscore, in->ape, in->norm_w, in->inv_freq, c.head_dim, 0, ent, st);
+    s = do_compress(c, in->ckv, in->cscore, in->ape, in->norm_w, in->inv_freq, (const float2*)(ws + plan.rope),
+                    c.head_dim, 0, ent, st);
     if (s != V4_OK) return s;
   }
   if (sel) {
     if (comp) {
-      s = do_compress(c, in->ickv, in->icscore, in->iape, in->inorm_w, in->inv_freq, c.idx_dim, 1,
-                      ikey, st);
+      s = do_compress(c, in->ickv, in->icscore, in->iape, in->inorm_w, in->inv_freq,
+                      (const float2*)(ws + plan.rope), c.idx_dim, 1, ikey, st);
       if (s != V4_OK) return s;
     }
     s = do_indexer(c, in->iq, 0, ikey, in->w, in->inv_freq, idx, out->iscore, ws, st, true);

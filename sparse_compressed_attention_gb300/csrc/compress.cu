@@ -17,23 +17,25 @@ namespace v4 {
 
 namespace {
 
-constexpr int kCompThreads = 256;
-
-// One block per (entry s, batch b).  Thread tid works on channel vector
-// cv = tid % ncv (8 channels) and member slice ms = tid / ncv; it runs an
-// online softmax over the members m with m % nms == ms.  The nms partial
-// states of a channel are merged in shared memory, then the block finishes
-// the entry: RMSNorm, weight, RoPE at r*s, optional Hadamard, store.
-template <typename T>
-__global__ void __launch_bounds__(kCompThreads)
+// One block per (entry s, batch b); 256 threads, or 512 for groups of 32
+// members and more.  Thread tid works on channel vector cv = tid % ncv (8
+// channels) and member slice ms = tid / ncv; it runs an online softmax over
+// the members m with m % nms == ms (with PAIR, two members' loads at a time:
+// for the long groups, whose slices hold many members each).  The nms
+// partial states of a channel are merged in shared memory, then the block
+// finishes the entry: RMSNorm, weight, RoPE at r*s (from the per-call cos/sin
+// table when one is given), optional Hadamard, store.
+template <typename T, bool PAIR>
+__global__ void __launch_bounds__(PAIR ? 512 : 256)
 compress_kernel(const T* __restrict__ ckv, const T* __restrict__ cscore,
                 const float* __restrict__ ape, const float* __restrict__ norm_w,
-                const float* __restrict__ inv_freq, T* __restrict__ out,
+                const float* __restrict__ inv_freq, const float2* __restrict__ cs_table, T* __restrict__ out,
                 int S, int N, int dim, int R, int ratio, int overlap, float eps,
                 int hadamard) {
   extern __shared__ float sm[];
+  const int nthr = blockDim.x;
   const int ncv = dim / 8;
-  const int nms = kCompThreads / ncv;        // >= 1 because dim <= 2048
+  const int nms = nthr / ncv;                // >= 1 because dim <= 2048
   float* s_m = sm;                           // [nms][dim]
   float* s_l = s_m + nms * dim;              // [nms][dim]
   float* s_a = s_l + nms * dim;              // [nms][dim]
@@ -53,17 +55,15 @@ compress_kernel(const T* __restrict__ ckv, const T* __restrict__ cscore,
     float m[8], l[8], acc[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) { m[k] = -INFINITY; l[k] = 0.f; acc[k] = 0.f; }
-    for (int mi = ms; mi < G; mi += nms) {
-      // member mi in chronological order: ape row first_row + mi
-      const int row = first_row + mi;
+    // member mi in chronological order: ape row first_row + mi
+    auto member_off = [&](int mi, size_t* off, int* row) {
+      *row = first_row + mi;
       int tok, half;
-      if (overlap && row < ratio) { tok = ratio * (s - 1) + row; half = 1; }
-      else { tok = ratio * s + (row - overlap * ratio); half = 0; }
-      const size_t off = (((size_t)b * S + tok) * P + half) * dim + cv * 8;
-      float sc[8], x[8], a[8];
-      load8(cscore + off, sc);
-      load8(ckv + off, x);
-      load8(ape + (size_t)row * dim + cv * 8, a);
+      if (overlap && *row < ratio) { tok = ratio * (s - 1) + *row; half = 1; }
+      else { tok = ratio * s + (*row - overlap * ratio); half = 0; }
+      *off = (((size_t)b * S + tok) * P + half) * dim + cv * 8;
+    };
+    auto update = [&](const float* sc, const float* x, const float* a) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         float lam = sc[k] + a[k];
@@ -78,6 +78,32 @@ compress_kernel(const T* __restrict__ ckv, const T* __restrict__ cscore,
           acc[k] += e * x[k];
         }
       }
+    };
+    int mi = ms;
+    for (; PAIR && mi + nms < G; mi += 2 * nms) {   // two members' loads in flight
+      size_t off0, off1;
+      int row0, row1;
+      member_off(mi, &off0, &row0);
+      member_off(mi + nms, &off1, &row1);
+      float sc0[8], x0[8], a0[8], sc1[8], x1[8], a1[8];
+      load8(cscore + off0, sc0);
+      load8(ckv + off0, x0);
+      load8(ape + (size_t)row0 * dim + cv * 8, a0);
+      load8(cscore + off1, sc1);
+      load8(ckv + off1, x1);
+      load8(ape + (size_t)row1 * dim + cv * 8, a1);
+      update(sc0, x0, a0);
+      update(sc1, x1, a1);
+    }
+    for (; mi < G; mi += nms) {
+      size_t off0;
+      int row0;
+      member_off(mi, &off0, &row0);
+      float sc0[8], x0[8], a0[8];
+      load8(cscore + off0, sc0);
+      load8(ckv + off0, x0);
+      load8(ape + (size_t)row0 * dim + cv * 8, a0);
+      update(sc0, x0, a0);
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -90,7 +116,7 @@ compress_kernel(const T* __restrict__ ckv, const T* __restrict__ cscore,
 
   // merge the member slices, accumulate the sum of squares
   float ss = 0.f;
-  for (int c = tid; c < dim; c += kCompThreads) {
+  for (int c = tid; c < dim; c += nthr) {
     float mm = -INFINITY;
     for (int j = 0; j < nms; ++j) mm = fmaxf(mm, s_m[j * dim + c]);
     float ll = 0.f, aa = 0.f;
@@ -109,20 +135,26 @@ compress_kernel(const T* __restrict__ ckv, const T* __restrict__ cscore,
   if ((tid & 31) == 0) s_red[tid >> 5] = ss;
   __syncthreads();
   if (tid < 32) {
-    float v = tid < kCompThreads / 32 ? s_red[tid] : 0.f;
+    float v = tid < nthr / 32 ? s_red[tid] : 0.f;
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     if (tid == 0) s_red[0] = v;
   }
   __syncthreads();
   const float rinv = 1.0f / sqrtf(s_red[0] / (float)dim + eps);
-  for (int c = tid; c < dim; c += kCompThreads)
+  for (int c = tid; c < dim; c += nthr)
     s_e[c] = s_e[c] * rinv * (norm_w ? norm_w[c] : 1.f);
   __syncthreads();
   // RoPE on interleaved pairs of the last R channels, position r*s
   const long long pos = (long long)ratio * s;
-  for (int j = tid; j < R / 2; j += kCompThreads) {
+  for (int j = tid; j < R / 2; j += nthr) {
     float cs, sn;
-    rope_cos_sin(pos, inv_freq[j], &cs, &sn);
+    if (cs_table) {
+      const float2 v = cs_table[pos * (R / 2) + j];
+      cs = v.x;
+      sn = v.y;
+    } else {
+      rope_cos_sin(pos, inv_freq[j], &cs, &sn);
+    }
     const int c0 = dim - R + 2 * j;
     float a = s_e[c0], bb = s_e[c0 + 1];
     rot_pair(a, bb, cs, sn);
@@ -132,7 +164,7 @@ compress_kernel(const T* __restrict__ ckv, const T* __restrict__ cscore,
   __syncthreads();
   if (hadamard) {
     for (int h = 1; h < dim; h <<= 1) {
-      for (int i = tid; i < dim / 2; i += kCompThreads) {
+      for (int i = tid; i < dim / 2; i += nthr) {
         const int lo = (i / h) * 2 * h + (i % h);
         float a = s_e[lo], bb = s_e[lo + h];
         s_e[lo] = a + bb;
@@ -141,11 +173,11 @@ compress_kernel(const T* __restrict__ ckv, const T* __restrict__ cscore,
       __syncthreads();
     }
     const float hs = 1.0f / sqrtf((float)dim);
-    for (int c = tid; c < dim; c += kCompThreads) s_e[c] *= hs;
+    for (int c = tid; c < dim; c += nthr) s_e[c] *= hs;
     __syncthreads();
   }
   T* dst = out + ((size_t)b * N + s) * dim;
-  for (int c8 = tid; c8 < ncv; c8 += kCompThreads) store8(dst + c8 * 8, s_e + c8 * 8);
+  for (int c8 = tid; c8 < ncv; c8 += nthr) store8(dst + c8 * 8, s_e + c8 * 8);
 }
 
 // Rotate every row of kv [rows, D] at its own position u = row % S (last R
@@ -428,20 +460,23 @@ indexer_prep_d128_kernel(const T* __restrict__ iq, const float2* __restrict__ cs
 
 template <typename T>
 cudaError_t compress_t(const v4_config& c, const void* ckv, const void* cscore, const float* ape,
-                       const float* norm_w, const float* inv_freq, int dim, int hadamard,
-                       void* out, cudaStream_t st) {
+                       const float* norm_w, const float* inv_freq, const float2* cs_table, int dim,
+                       int hadamard, void* out, cudaStream_t st) {
   const int N = c.seqlen / c.ratio;
   if (N == 0) return cudaSuccess;
   const int ncv = dim / 8;
-  const int nms = kCompThreads / ncv;
+  const int G = (1 + c.overlap) * c.ratio;
+  int threads = G >= 32 ? 512 : 256;
+  while (threads > 32 && threads / ncv < 1) threads *= 2;   // dim <= 2048: 256 threads cover it
+  const int nms = threads / ncv;
   const size_t smem = (size_t)(3 * nms * dim + dim) * sizeof(float);
-  auto kern = compress_kernel<T>;
+  auto kern = G >= 32 ? compress_kernel<T, true> : compress_kernel<T, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(N, c.batch);
-  kern<<<grid, kCompThreads, smem, st>>>((const T*)ckv, (const T*)cscore, ape, norm_w, inv_freq,
-                                         (T*)out, c.seqlen, N, dim, c.rope_dim, c.ratio,
-                                         c.overlap, c.rms_eps, hadamard);
+  kern<<<grid, threads, smem, st>>>((const T*)ckv, (const T*)cscore, ape, norm_w, inv_freq, cs_table,
+                                    (T*)out, c.seqlen, N, dim, c.rope_dim, c.ratio,
+                                    c.overlap, c.rms_eps, hadamard);
   note_launch();
   return cudaGetLastError();
 }
@@ -450,10 +485,10 @@ cudaError_t compress_t(const v4_config& c, const void* ckv, const void* cscore, 
 
 cudaError_t launch_compress(const v4_config& c, const void* ckv, const void* cscore,
                             const float* ape, const float* norm_w, const float* inv_freq,
-                            int dim, int hadamard, void* out, cudaStream_t st) {
+                            const float2* cs_table, int dim, int hadamard, void* out, cudaStream_t st) {
   if (c.dtype == V4_BF16)
-    return compress_t<bf16>(c, ckv, cscore, ape, norm_w, inv_freq, dim, hadamard, out, st);
-  return compress_t<float>(c, ckv, cscore, ape, norm_w, inv_freq, dim, hadamard, out, st);
+    return compress_t<bf16>(c, ckv, cscore, ape, norm_w, inv_freq, cs_table, dim, hadamard, out, st);
+  return compress_t<float>(c, ckv, cscore, ape, norm_w, inv_freq, cs_table, dim, hadamard, out, st);
 }
 
 cudaError_t launch_rotate_rows(const v4_config& c, const void* kv, const float* inv_freq,

@@ -35,9 +35,11 @@ struct Workspace {
 Workspace plan_workspace(const v4_config& c);
 
 // ---- compressor and preparation kernels (compress.cu)
+// cs_table: the per-call cos/sin table of positions < S, or null (angles
+// computed in place).
 cudaError_t launch_compress(const v4_config& c, const void* ckv, const void* cscore,
                             const float* ape, const float* norm_w, const float* inv_freq,
-                            int dim, int hadamard, void* out, cudaStream_t st);
+                            const float2* cs_table, int dim, int hadamard, void* out, cudaStream_t st);
 cudaError_t launch_rotate_rows(const v4_config& c, const void* kv, const float* inv_freq,
                                void* kv_rot, cudaStream_t st);
 // Rotated window keys, the Euclidean norm of every stored key row (window
