@@ -458,6 +458,126 @@ indexer_prep_d128_kernel(const T* __restrict__ iq, const float2* __restrict__ cs
   }
 }
 
+// Short groups (G <= 16 members, e.g. CSA's 8) with dim/8 a power of two in
+// [16, 256]: one thread per 8 channels runs the whole online softmax over
+// the members (no merge step), the entry's threads reduce the RMS by warp
+// shuffles (and shared memory when the entry spans warps), rotate their own
+// pairs and, for dim/8 <= 32, run the Hadamard as the query prep does (three
+// stages in the thread, the rest across lanes).  Several entries per block.
+template <typename T>
+__global__ void __launch_bounds__(256)
+compress_short_kernel(const T* __restrict__ ckv, const T* __restrict__ cscore,
+                      const float* __restrict__ ape, const float* __restrict__ norm_w,
+                      const float* __restrict__ inv_freq, const float2* __restrict__ cs_table,
+                      T* __restrict__ out, int S, int N, int dim, int R, int ratio, int overlap, float eps,
+                      int hadamard) {
+  __shared__ float s_part[8];                        // per-warp partial sums of squares
+  const int ncv = dim / 8;
+  const int per_block = 256 / ncv;
+  const int e_in = threadIdx.x / ncv, cv = threadIdx.x % ncv;
+  const int s = blockIdx.x * per_block + e_in;
+  const int b = blockIdx.y;
+  const bool live = s < N;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int P = 1 + overlap;
+  const int ss_ = live ? s : 0;
+  const int G = (overlap && ss_ >= 1) ? 2 * ratio : ratio;
+  const int first_row = (overlap && ss_ >= 1) ? 0 : overlap * ratio;
+  float m[8], l[8], acc[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) { m[k] = -INFINITY; l[k] = 0.f; acc[k] = 0.f; }
+  if (live) {
+    for (int mi = 0; mi < G; ++mi) {
+      const int row = first_row + mi;
+      int tok, half;
+      if (overlap && row < ratio) { tok = ratio * (ss_ - 1) + row; half = 1; }
+      else { tok = ratio * ss_ + (row - overlap * ratio); half = 0; }
+      const size_t off = (((size_t)b * S + tok) * P + half) * dim + cv * 8;
+      float sc[8], x[8], a[8];
+      load8(cscore + off, sc);
+      load8(ckv + off, x);
+      load8(ape + (size_t)row * dim + cv * 8, a);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float lam = sc[k] + a[k];
+        if (lam > m[k]) {
+          float f = expf(m[k] - lam);
+          l[k] = l[k] * f + 1.f;
+          acc[k] = acc[k] * f + x[k];
+          m[k] = lam;
+        } else {
+          float e = expf(lam - m[k]);
+          l[k] += e;
+          acc[k] += e * x[k];
+        }
+      }
+    }
+  }
+  float v[8];
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    v[k] = live ? acc[k] / l[k] : 0.f;
+    ss += v[k] * v[k];
+  }
+  // sum of squares over the entry's ncv threads
+  if (ncv <= 32) {
+    for (int o = ncv / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  } else {
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) s_part[wid] = ss;
+    __syncthreads();
+    const int w0 = (e_in * ncv) >> 5, nw = ncv >> 5;
+    ss = 0.f;
+    for (int w = 0; w < nw; ++w) ss += s_part[w0 + w];
+  }
+  const float rinv = 1.0f / sqrtf(ss / (float)dim + eps);
+  const int c0 = cv * 8;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) v[k] = v[k] * rinv * (norm_w ? norm_w[c0 + k] : 1.f);
+  if (c0 >= dim - R) {
+    const long long pos = (long long)ratio * ss_;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int j = (c0 - (dim - R)) / 2 + k;
+      float cs, sn;
+      if (cs_table) {
+        const float2 cvv = cs_table[pos * (R / 2) + j];
+        cs = cvv.x;
+        sn = cvv.y;
+      } else {
+        rope_cos_sin(pos, inv_freq[j], &cs, &sn);
+      }
+      rot_pair(v[2 * k], v[2 * k + 1], cs, sn);
+    }
+  }
+  if (hadamard) {                                     // dim/8 <= 32 (checked by the launcher)
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if ((k & h) == 0) {
+          const float a = v[k], d = v[k + h];
+          v[k] = a + d;
+          v[k + h] = a - d;
+        }
+      }
+    }
+    for (int hl = 1; hl < ncv; hl <<= 1) {
+      const bool upper = (cv & hl) != 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float other = __shfl_xor_sync(0xffffffffu, v[k], hl);
+        v[k] = upper ? (other - v[k]) : (v[k] + other);
+      }
+    }
+    const float hs = 1.0f / sqrtf((float)dim);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] *= hs;
+  }
+  if (live) store8(out + ((size_t)b * N + s) * dim + c0, v);
+}
+
 template <typename T>
 cudaError_t compress_t(const v4_config& c, const void* ckv, const void* cscore, const float* ape,
                        const float* norm_w, const float* inv_freq, const float2* cs_table, int dim,
@@ -466,6 +586,16 @@ cudaError_t compress_t(const v4_config& c, const void* ckv, const void* cscore, 
   if (N == 0) return cudaSuccess;
   const int ncv = dim / 8;
   const int G = (1 + c.overlap) * c.ratio;
+  const bool pow2 = (ncv & (ncv - 1)) == 0;
+  if (G <= 16 && pow2 && ncv >= 16 && ncv <= 256 && (!hadamard || ncv <= 32)) {
+    const int per_block = 256 / ncv;
+    dim3 grid((N + per_block - 1) / per_block, c.batch);
+    compress_short_kernel<T><<<grid, 256, 0, st>>>((const T*)ckv, (const T*)cscore, ape, norm_w, inv_freq,
+                                                    cs_table, (T*)out, c.seqlen, N, dim, c.rope_dim, c.ratio,
+                                                    c.overlap, c.rms_eps, hadamard);
+    note_launch();
+    return cudaGetLastError();
+  }
   int threads = G >= 32 ? 512 : 256;
   while (threads > 32 && threads / ncv < 1) threads *= 2;   // dim <= 2048: 256 threads cover it
   const int nms = threads / ncv;
