@@ -325,3 +325,34 @@ def test_bad_index_is_flagged_and_skipped():
     V.v4_reset_device_status()
     assert V.v4_get_device_status() == 0
     assert torch.equal(o1, o2)
+
+
+def test_layer_call_replays_in_a_cuda_graph():
+    """The layer entry point captured in a CUDA graph (as the benchmark times
+    it) gives bit-identical outputs on replay to an eager call."""
+    p = SI.preset("csa_bf16_4k", S=1024, q_mode="direct")
+    x = SI.make_layer_inputs(p, "cuda", seed=9)
+    x["inv_freq"] = torch.from_numpy(inv_freq_for(p)).cuda()
+    cfg = V.config_from_preset(p)
+    B, S, H, K = p["B"], p["S"], p["H"], p["K"]
+
+    def outputs():
+        return {"o": torch.empty_like(x["q"]), "lse": torch.empty(B, S, H, device="cuda"),
+                "idx": torch.empty(B, S, K, dtype=torch.int32, device="cuda")}
+
+    ws = V.alloc_workspace(cfg)
+    eager = outputs()
+    V.v4_attn_layer_fwd(cfg, x, eager, ws)
+    torch.cuda.synchronize()
+    replayed = outputs()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        V.v4_attn_layer_fwd(cfg, x, replayed, ws)
+    for k in replayed:
+        replayed[k].zero_()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for k in eager:
+        assert torch.equal(eager[k], replayed[k]), k
+    assert V.v4_get_device_status() == 0
