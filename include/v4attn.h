@@ -56,7 +56,12 @@ typedef enum {
 typedef enum { V4_F32 = 0, V4_BF16 = 1 } v4_dtype;
 
 /* Kernel family selection (cfg->path). AUTO picks the tensor-core kernels
- * when the shapes and dtype allow it, otherwise the CUDA-core kernels. */
+ * when the shapes and dtype allow it, otherwise the CUDA-core kernels.
+ * Tensor-core attention: bf16, n_heads a multiple of 64 up to 512 (each
+ * 64-head slice of a query is one work item), head_dim 512, rope_dim 64,
+ * 1 <= window <= 128, topk <= 1024.  Tensor-core indexer: bf16,
+ * idx_heads 64, idx_dim 128.  V4_PATH_TC returns V4_ERR_UNSUPPORTED for
+ * other shapes. */
 typedef enum { V4_PATH_AUTO = 0, V4_PATH_SIMT = 1, V4_PATH_TC = 2 } v4_path;
 
 typedef struct v4_config {

@@ -120,7 +120,8 @@ Workspace plan_workspace(const v4_config& c) {
   take(w.scores, w.scores_bytes, sel ? B * S * N * 4 : 0);
   take(w.idx, w.idx_bytes, sel ? B * S * c.topk * 4 : 0);
   take(w.knorm, w.knorm_bytes, key_norm_floats(c) * 4);
-  take(w.counters, w.counters_bytes, (2 + B * S) * 4);
+  // redo list: one entry per (query, 64-head slice) at most
+  take(w.counters, w.counters_bytes, (2 + B * S * (size_t)(c.n_heads > 64 ? (c.n_heads + 63) / 64 : 1)) * 4);
   take(w.rope, w.rope_bytes, S * (size_t)(c.rope_dim / 2) * 8);
   w.total = off;
   return w;
@@ -387,7 +388,7 @@ v4_status v4_sparse_mqa_fwd(const v4_config* cfg, const void* q, const void* kv,
   OPT(lse, "lse");
   if (cfg->rope_dim > 0) REQ(inv_freq, "inv_freq");
   if (cfg->path == V4_PATH_TC && !mqa_tc_supported(*cfg))
-    return fail(V4_ERR_UNSUPPORTED, "tensor-core attention needs bf16, H=64, D=512, R=64, 1 <= W <= 128, K <= 512");
+    return fail(V4_ERR_UNSUPPORTED, "tensor-core attention needs bf16, H a multiple of 64 up to 512, D=512, R=64, 1 <= W <= 128, K <= 1024");
   s = check_ws(*cfg, workspace, ws_bytes);
   if (s != V4_OK) return s;
   return do_mqa(*cfg, q, kv, ent, cfg->topk > 0 ? idx : nullptr, sink, inv_freq, o, lse,
@@ -464,7 +465,7 @@ v4_status v4_attn_layer_fwd(const v4_config* cfg, const v4_layer_inputs* in, v4_
     if (s != V4_OK) return s;
   }
   if (c.path == V4_PATH_TC && !mqa_tc_supported(c))
-    return fail(V4_ERR_UNSUPPORTED, "tensor-core attention needs bf16, H=64, D=512, R=64, 1 <= W <= 128, K <= 512");
+    return fail(V4_ERR_UNSUPPORTED, "tensor-core attention needs bf16, H a multiple of 64 up to 512, D=512, R=64, 1 <= W <= 128, K <= 1024");
   s = check_ws(c, workspace, ws_bytes);
   if (s != V4_OK) return s;
   char* ws = (char*)workspace;

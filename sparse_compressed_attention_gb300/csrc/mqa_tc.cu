@@ -59,16 +59,16 @@ constexpr int kSlots = 8;                         // one tile: 8 K-blocks of 64 
 constexpr uint32_t kSlotBytes = 128 * 128;        // 128 keys x 64 dims x 2 B
 constexpr uint32_t kQBlockBytes = 64 * 128;       // 64 heads x 64 dims x 2 B
 constexpr uint32_t kPBytes = 128 * 64 * 2;        // 128 keys x 64 heads x 2 B
-constexpr int kMaxSel = 512;
+constexpr int kMaxSel = 1024;
 
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_SLOT = OFF_Q + 8 * kQBlockBytes;           // 65536
 constexpr uint32_t OFF_P = OFF_SLOT + kSlots * kSlotBytes;        // 196608
-constexpr uint32_t OFF_LIST = OFF_P + 2 * kPBytes;                // 229376
-constexpr uint32_t OFF_CTL = OFF_LIST + 2 * kMaxSel * 2;          // 231424 (two 16-bit lists)
+constexpr uint32_t OFF_LIST = OFF_P + kPBytes;                    // 212992 (one P^T buffer)
+constexpr uint32_t OFF_CTL = OFF_LIST + 2 * kMaxSel * 2;          // 217088 (two 16-bit lists)
 
 struct QInfo {
-  int b, t, n_ent, ent_tiles, tiles, w_lo, done;
+  int b, t, hs, n_ent, ent_tiles, tiles, w_lo, done;     // hs: head slice (64 heads each)
   float kmax;
 };
 
@@ -94,18 +94,19 @@ constexpr uint32_t kSmemBytes = OFF_CTL + sizeof(Ctl);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Params {
-  const bf16* q;               // [B,S,64,512] (L2 prefetch of upcoming queries)
+  const bf16* q;               // [B,S,H,512] (L2 prefetch of upcoming queries)
   const bf16* ent;             // [B,N,512] gathered entries
-  bf16* o;                     // [B,S,64,512]
+  bf16* o;                     // [B,S,H,512]
   const int32_t* idx;          // [B,S,K] or null
-  const float* sink;           // [64] or null
+  const float* sink;           // [H] or null
   const float2* rope_cs;       // [S][32] cos/sin
   const float* wmax;           // [B*S]   max |key| over the window of each query
   const float* emax;           // [B*(N+1)] prefix max |entry|
-  float* lse;                  // [B,S,64] or null
+  float* lse;                  // [B,S,H] or null
   int* status;
   int* counters;               // [0] work item, [1] redo count, [2..] redo list
   int B, S, N, ratio, window, K;
+  int H, HS;                   // heads, head slices of 64
   float scale;
 };
 
@@ -198,7 +199,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = c->tmem_base;
-  const int total = p.B * p.S;
+  const int total = p.B * p.S * p.HS;        // work items: (query, head slice)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -211,7 +212,8 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     float kb_next = 0.f;
     auto fetch_ahead = [&](int it) {
       if (it >= total) return;
-      const int nb = it % p.B, nt = p.S - 1 - it / p.B;
+      const int qi = it / p.HS;
+      const int nb = qi % p.B, nt = p.S - 1 - qi / p.B;
       if (gathered) {
         const int32_t* row = p.idx + ((size_t)nb * p.S + nt) * p.K;
 #pragma unroll
@@ -229,8 +231,9 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     auto prepare = [&](int qn, int it) -> QInfo {
       QInfo inf;
       inf.done = it >= total ? 1 : 0;
-      inf.b = inf.done ? 0 : it % p.B;
-      inf.t = inf.done ? 0 : p.S - 1 - it / p.B;
+      inf.b = inf.done ? 0 : (it / p.HS) % p.B;
+      inf.t = inf.done ? 0 : p.S - 1 - (it / p.HS) / p.B;
+      inf.hs = inf.done ? 0 : it % p.HS;
       // kmax bounds |k| over every key the query can see (for a selection,
       // over all visible entries: a superset, so still a bound)
       inf.kmax = kb_next;
@@ -238,7 +241,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       inf.w_lo = 0;
       if (!inf.done) {
         if (lane == 0) {                      // warm L2 with its query rows, loaded one query later
-          const bf16* qn_rows = p.q + ((size_t)inf.b * p.S + inf.t) * kH * kD;
+          const bf16* qn_rows = p.q + (((size_t)inf.b * p.S + inf.t) * p.H + kH * inf.hs) * kD;
           asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(qn_rows), "r"(kH * kD * 2) : "memory");
         }
         const int nv = p.ratio > 0 ? min((inf.t + 1) / p.ratio, p.N) : 0;
@@ -296,7 +299,8 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       if (lane == 0) mbar_expect_tx(&c->q_full, 8 * kQBlockBytes);
       __syncwarp();
       if (lane < 8)
-        tma_load_2d(smem + OFF_Q + lane * kQBlockBytes, &map_q, 64 * lane, (cur.b * p.S + cur.t) * kH, &c->q_full);
+        tma_load_2d(smem + OFF_Q + lane * kQBlockBytes, &map_q, 64 * lane, (cur.b * p.S + cur.t) * p.H + kH * cur.hs,
+                    &c->q_full);
       const uint16_t* lst = lists + (qc & 1) * kMaxSel;
       QInfo nxt;
       nxt.done = 1;
@@ -422,7 +426,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           ok = wait_ok(&c->p_ready[sb], (g >> 1) & 1, c, p.status);
           if (ok && j == 0 && qc >= 1) ok = wait_ok(&c->o_empty, (qc - 1) & 1, c, p.status);
           tc_fence_after();
-          const uint64_t dP = dP0 + (uint64_t)((sb * kPBytes) >> 4);
+          const uint64_t dP = dP0;                   // one P^T buffer: S(j+1) commits after O(j)
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
 #pragma unroll
@@ -523,7 +527,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       if (part == 0) {
         float m = p.scale * sqrtf(ss) * inf.kmax;
         m = m * (1.0f + 1e-5f) + 1e-6f;                     // covers rounding of the bound itself
-        if (p.sink != nullptr) m = fmaxf(m, p.sink[h]);
+        if (p.sink != nullptr) m = fmaxf(m, p.sink[kH * inf.hs + h]);
         c->mlog2[qc & 1][h] = m * log2e;
       }
       fence_proxy_async_smem();
@@ -537,7 +541,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     if (more) setup_query(0, inf);
     while (more) {
       const float* mlog2 = c->mlog2[qc & 1] + h0;
-      const int t = inf.t, b = inf.b;
+      const int t = inf.t, b = inf.b, hsl = inf.hs;
       const int nk_total = inf.n_ent + (t - inf.w_lo + 1);
       float lsum = 0.f;                         // this warp's denominator of head h0 + lane
       for (int j = 0; j < inf.tiles; ++j) {
@@ -562,7 +566,9 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           pk[i] = pack_bf16x2(x0, x1);
         }
         // P^T [8-head column block][key]: this half's four blocks
-        uint8_t* prow = smem + OFF_P + sb * kPBytes + krow * 16 + (4 * hh) * 2048;
+        // (one buffer: this tile's S completing implies the previous tile's
+        // O products, issued before it, have completed too)
+        uint8_t* prow = smem + OFF_P + krow * 16 + (4 * hh) * 2048;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
           *reinterpret_cast<uint4*>(prow + cc * 2048) =
@@ -624,11 +630,11 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       if (ts < kH) {
         float l = (hs[ts] + hs[64 + ts]) + (hs[128 + ts] + hs[192 + ts]);
         const float m = mlog2_all[ts] * 0.6931471805599453f;
-        if (p.sink != nullptr) l += expf(p.sink[ts] - m);
+        if (p.sink != nullptr) l += expf(p.sink[kH * hsl + ts] - m);
         // too little mass under the bound: exp underflow may have lost keys
         const bool bad = !(l >= (float)nk_total * 1.0e-26f) || !(l < INFINITY);
         if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&c->redo, 1);
-        if (p.lse) p.lse[((size_t)b * p.S + t) * kH + ts] = m + logf(l);
+        if (p.lse) p.lse[((size_t)b * p.S + t) * p.H + kH * hsl + ts] = m + logf(l);
         hs[256 + ts] = 1.0f / l;
       }
       named_bar_sync(1, kSoftThreads);
@@ -648,7 +654,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       }
       // o[t, h, 128m + krow]: for each head the 32 lanes of a warp write 64
       // contiguous bytes
-      bf16* obase = p.o + ((size_t)b * p.S + t) * kH * kD + (size_t)h0 * kD + krow;
+      bf16* obase = p.o + (((size_t)b * p.S + t) * p.H + kH * hsl + h0) * kD + krow;
       for (int m = 0; m < 4; ++m) {
         float v[32];
         tmem_ld32(tmem + lane_base + 128 + 64 * m + h0, v);
@@ -661,23 +667,29 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         for (int i = 0; i < 32; ++i) v[i] *= inv_l[i];
         if (m == 3 && quarter >= 2) {
           // rotated dims 448..511: the partner of each pair is the
-          // neighbouring lane; the values cross through the idle second P
-          // buffer (eight 16-byte stores and loads instead of 32 shuffles)
-          float4* xb = reinterpret_cast<float4*>(smem + OFF_P + kPBytes + (2 * (quarter - 2) + hh) * (kPBytes / 4));
-#pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4)
-            xb[c4 * 32 + lane] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
-          __syncwarp();
+          // neighbouring lane; the values cross through the idle P buffer
+          // (after the per-head scalars), sixteen heads per round
+          float4* xb = reinterpret_cast<float4*>(smem + OFF_P + 2048 + (2 * (quarter - 2) + hh) * 2048);
           const bool odd = lane & 1;
 #pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 o4 = xb[c4 * 32 + (lane ^ 1)];
-            const float oth[4] = {o4.x, o4.y, o4.z, o4.w};
+          for (int rnd = 0; rnd < 2; ++rnd) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int i = 4 * c4 + e;
-              v[i] = odd ? (v[i] * dc - oth[e] * ds) : (v[i] * dc + oth[e] * ds);
+            for (int c4 = 0; c4 < 4; ++c4) {
+              const int i = 16 * rnd + 4 * c4;
+              xb[c4 * 32 + lane] = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
             }
+            __syncwarp();
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+              const float4 o4 = xb[c4 * 32 + (lane ^ 1)];
+              const float oth[4] = {o4.x, o4.y, o4.z, o4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int i = 16 * rnd + 4 * c4 + e;
+                v[i] = odd ? (v[i] * dc - oth[e] * ds) : (v[i] * dc + oth[e] * ds);
+              }
+            }
+            __syncwarp();
           }
         }
 #pragma unroll
@@ -709,7 +721,7 @@ cudaError_t launch_mqa_tc(const v4_config& cfg, const void* q, const void* kv_ro
   const int B = cfg.batch, S = cfg.seqlen;
   const int N = cfg.ratio > 0 ? S / cfg.ratio : 0;
   CUtensorMap mq, mkv, ment;
-  const uint64_t qrows = (uint64_t)B * S * kH;
+  const uint64_t qrows = (uint64_t)B * S * cfg.n_heads;
   int e = 0;
   e |= make_tmap_bf16_2d(&mq, q, kD, qrows, 64, 64, true);
   e |= make_tmap_bf16_2d(&mkv, kv_rot, kD, (uint64_t)B * S, 64, kTileKeys, true);
@@ -735,6 +747,8 @@ cudaError_t launch_mqa_tc(const v4_config& cfg, const void* q, const void* kv_ro
   prm.ratio = cfg.ratio;
   prm.window = cfg.window;
   prm.K = cfg.topk;
+  prm.H = cfg.n_heads;
+  prm.HS = cfg.n_heads / kH;
   prm.scale = cfg.softmax_scale > 0.f ? cfg.softmax_scale : 1.0f / sqrtf((float)kD);
   cudaError_t err = cudaFuncSetAttribute(mqa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
@@ -742,8 +756,8 @@ cudaError_t launch_mqa_tc(const v4_config& cfg, const void* q, const void* kv_ro
   int sms = 0, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int total = B * S;
-  const int grid = total < sms ? total : sms;
+  const long long total = (long long)B * S * (cfg.n_heads / kH);
+  const int grid = (int)(total < sms ? total : sms);
   err = cudaMemsetAsync(counters + 1, 0, sizeof(int), st);
   if (err != cudaSuccess) return err;
   mqa_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mq, mkv, ment, prm);
@@ -752,7 +766,8 @@ cudaError_t launch_mqa_tc(const v4_config& cfg, const void* q, const void* kv_ro
 }
 
 bool mqa_tc_supported(const v4_config& c) {
-  return c.dtype == V4_BF16 && c.n_heads == kH && c.head_dim == kD && c.rope_dim == kR &&
+  return c.dtype == V4_BF16 && c.n_heads >= kH && c.n_heads % kH == 0 && c.n_heads <= 8 * kH &&
+         c.head_dim == kD && c.rope_dim == kR &&
          c.window >= 1 && c.window <= kTileKeys && c.topk <= kMaxSel && (c.ratio == 0 || c.ratio >= 1) &&
          (c.topk == 0 || c.ratio == 0 || c.seqlen / c.ratio <= 65536);    // 16-bit selection lists
 }

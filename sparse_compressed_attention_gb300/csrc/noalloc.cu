@@ -27,7 +27,7 @@ namespace {
 constexpr long long kMaxTokens = 8192;
 constexpr size_t kKvBytes = 8u << 20;
 constexpr size_t kNormBytes = 5 * kMaxTokens * sizeof(float);            // norms and their bounds
-constexpr size_t kCounterBytes = (2 + kMaxTokens) * sizeof(int);
+constexpr size_t kCounterBytes = (2 + 8 * kMaxTokens) * sizeof(int);      // up to 8 head slices
 constexpr size_t kRopeBytes = 524288 / 2 * sizeof(float2);
 constexpr size_t kOffNorm = kKvBytes;
 constexpr size_t kOffCounters = kOffNorm + kNormBytes;
@@ -91,7 +91,7 @@ extern "C" v4_status v4_sparse_mqa_fwd_noalloc(const v4_config* cfg, const void*
   if (c.rope_dim > 0 && (!inv_freq || !aligned(inv_freq)))
     return set_error(V4_ERR_INVALID_ARG, "inv_freq must be non-null and 16-byte aligned");
   if (c.path == V4_PATH_TC && !mqa_tc_supported(c))
-    return set_error(V4_ERR_UNSUPPORTED, "tensor-core attention needs bf16, H=64, D=512, R=64, 1 <= W <= 128, K <= 512");
+    return set_error(V4_ERR_UNSUPPORTED, "tensor-core attention needs bf16, H a multiple of 64 up to 512, D=512, R=64, 1 <= W <= 128, K <= 1024");
   unsigned char* base = scratch_ptr(&s);
   if (!base) return s;
   int* status = device_status_ptr();

@@ -81,6 +81,10 @@ CASES = [
     ("hca_b2_ragged", "hca_bf16_16k", dict(S=777, B=2, ratio=16), "hca", False),
     ("swa_s300", "swa_bf16_16k", dict(S=300), "swa", False),
     ("swa_w7_b2", "swa_bf16_16k", dict(S=100, B=2, W=7), "swa", True),
+    # V4-Pro-like shapes: 128 heads (two 64-head slices per query), top-1024
+    ("pro_csa_h128_k1024_sink", "csa_bf16_4k", dict(S=4500, H=128, K=1024), "csa", True),
+    ("pro_hca_h128", "hca_bf16_16k", dict(S=700, H=128), "hca", False),
+    ("csa_h192_b2", "csa_bf16_4k", dict(S=400, B=2, H=192, K=96), "csa", False),
 ]
 
 
