@@ -201,12 +201,12 @@ def barrier():
 # ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
-def make_layer(name, S, device, seed):
+def make_layer(name, S, device, seed, **over):
     import torch
 
     import seeded_inputs as SI
     import sparse_compressed_attention_gb300 as V
-    p = SI.preset(name, S=S)
+    p = SI.preset(name, S=S, **over)
     x = SI.make_layer_inputs(p, device, seed=seed)
     yarn = p["yarn"]
     f = V.v4_rope_inv_freq(p["theta"], p["R"], yarn, SI.YARN_ORIGINAL_LEN if yarn > 1 else 0,
@@ -479,7 +479,15 @@ def run_workload(args):
     Bld.build()
     V.lib()
     S = args.seq
-    if args.workload == "stack":
+    if args.workload == "pro":
+        B = 1
+        order = [make_layer("csa_bf16_16k", S, dev, seed=4000, H=128, K=1024),
+                 make_layer("hca_bf16_16k", S, dev, seed=4001, H=128)]
+        order[0]["name"], order[1]["name"] = "csa", "hca"
+        metric = "attention-layer fwd tokens/s at S=%d (CSA & HCA), 128 heads, top-1024" % S
+        wl = ("DeepSeek-V4-Pro-like attention layer pair fwd (128 heads, top-1024; other shapes as Flash), "
+              "B=1, S=%d, H=128, D=512, R=64, bf16" % S)
+    elif args.workload == "stack":
         B = 2
         kinds = {k: make_stack_layer(k, B, S, dev, seed=2000 + i) for i, k in enumerate(("swa", "csa", "hca"))}
         order = [kinds[k] for k in STACK_ORDER]
@@ -699,9 +707,10 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager calls instead of a captured step")
-    ap.add_argument("--workload", choices=["pair", "stack", "csa"], default="pair",
+    ap.add_argument("--workload", choices=["pair", "stack", "csa", "pro"], default="pair",
                     help="pair: the CSA + HCA layer pair (the reported line); stack: the 43-layer "
-                         "Flash stack with grouped wo_a at B=2; csa: one CSA layer (e.g. --seq 65536)")
+                         "Flash stack with grouped wo_a at B=2; csa: one CSA layer (e.g. --seq 65536); "
+                         "pro: the pair with 128 heads and top-1024")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
