@@ -1,4 +1,5 @@
-"""CPU oracle for the DeepSeek-V4-Flash compressed attention forward.
+"""CPU oracle for the DeepSeek-V4-Flash compressed attention forward and the
+gradient of its attention step.
 
 TEST INFRASTRUCTURE ONLY. This module is the slow, plain, float64 statement of
 what the attention path computes. Only the tests, ``__graft_entry__.smoke()``
@@ -39,7 +40,10 @@ Readings of points the pages leave open (each is listed in the design doc):
   * top-k keeps the min(K, n_vis) best entries, equal scores going to the
     lower index; short rows are padded with -1;
   * the optional attention sink is one extra logit per head that enters the
-    softmax denominator only.
+    softmax denominator only;
+  * the attention backward is the exact gradient of this forward (the pages
+    give its kernels, not its formulas): entry gradients are w.r.t. the stored
+    rotated entries, window gradients w.r.t. the un-rotated latent.
 """
 from __future__ import annotations
 
@@ -399,6 +403,88 @@ def sparse_mqa(q, kv, ent, idx, sink, inv_freq, ratio, window, scale=None,
             o[b, i] = rope_derotate(out, t, inv_freq)
             lse[b, i] = m + np.log(den)
     return maybe_bf16(o, store_bf16), lse
+
+
+# ---------------------------------------------------------------------------
+# Attention backward  ([BLOG] "Attention kernels for the three layer types",
+# backward: the gradient of the same forward, split there into dQ, a
+# head-dimension contraction ("interm") and the delta rowsum(O * dO))
+# ---------------------------------------------------------------------------
+def sparse_mqa_bwd(q, kv, ent, idx, sink, inv_freq, ratio, window, dout, scale=None, rows=None):
+    """Exact gradients of L = sum(dout * o) for o = sparse_mqa(...).
+
+    Written out by the chain rule for one query t with keys k_j (chosen
+    entries, then window tokens rotated at their positions u) and
+    qr_h = rot(q_h, t):
+        p_hj   = exp(scale qr_h . k_j - lse_h)      (the sink takes the rest)
+        g_h    = rot(dout_h, t)                     (o = rot(o', -t), o' = sum_j p_hj k_j)
+        delta_h = g_h . o'_h  (= dout_h . o_h, rotation is orthogonal)
+        ds_hj  = p_hj (g_h . k_j - delta_h)         (gradient of the logit)
+        dq_h   = rot(scale sum_j ds_hj k_j, -t)
+        dk_j   = scale sum_h ds_hj qr_h + sum_h p_hj g_h   (key = value)
+        dsink_h = -p_sink,h delta_h,  p_sink,h = exp(sink_h - lse_h)
+    Entry gradients are taken w.r.t. the stored (rotated) entries; window
+    gradients w.r.t. the un-rotated latent kv, i.e. rot(dk_u, -u).
+
+    q, dout [B,S,H,D] and idx [B,S,K] are indexed by position t.
+    Returns dq [B,T,H,D] for the ``rows`` (all by default), dkv [B,S,D],
+    dent [B,N,D] (None without entries) and dsink [H] (None without sink);
+    dkv, dent and dsink hold the contributions of the listed rows only.
+    """
+    q = np.asarray(q, dtype=F64)
+    dout = np.asarray(dout, dtype=F64)
+    kv = np.asarray(kv, dtype=F64)
+    B, S, H, D = q.shape
+    scale = D ** -0.5 if (scale is None or scale <= 0) else scale
+    rows = np.arange(S) if rows is None else np.asarray(rows)
+    have_ent = ratio > 0 and ent is not None
+    entf = np.asarray(ent, dtype=F64) if have_ent else None
+    z = None if sink is None else np.asarray(sink, dtype=F64)
+    dq = np.zeros((B, len(rows), H, D), dtype=F64)
+    dkv = np.zeros((B, S, D), dtype=F64)
+    dent = np.zeros_like(entf) if have_ent else None
+    dsink = np.zeros(H, dtype=F64) if z is not None else None
+    for b in range(B):
+        for i, t in enumerate(rows):
+            t = int(t)
+            sel = np.zeros(0, dtype=np.int64)
+            if have_ent:
+                nv = min(n_visible(t, ratio), entf.shape[1])
+                if idx is not None:
+                    sel = np.asarray(idx[b, t])
+                    sel = sel[sel >= 0].astype(np.int64)
+                    if np.any(sel >= nv):
+                        raise ValueError("selected entry is not causally visible")
+                else:
+                    sel = np.arange(nv)
+            lo, hi = window_range(t, window)
+            u = np.arange(lo, hi)
+            keys = np.concatenate([entf[b, sel] if have_ent else np.zeros((0, D)),
+                                   rope_rotate(kv[b, lo:hi], u, inv_freq)], axis=0)
+            if keys.shape[0] == 0:
+                continue                                   # o = 0 whatever the inputs
+            qr = rope_rotate(q[b, t], t, inv_freq)         # [H, D]
+            logits = scale * (qr @ keys.T)                 # [H, nk]
+            m = logits.max(axis=1)
+            if z is not None:
+                m = np.maximum(m, z)
+            e = np.exp(logits - m[:, None])
+            den = e.sum(axis=1) + (np.exp(z - m) if z is not None else 0.0)
+            p = e / den[:, None]
+            o_rot = p @ keys                               # [H, D], before de-rotation
+            g = rope_rotate(dout[b, t], t, inv_freq)       # gradient of o_rot
+            delta = (g * o_rot).sum(axis=1)
+            ds = p * (g @ keys.T - delta[:, None])
+            dq[b, i] = rope_derotate(scale * (ds @ keys), t, inv_freq)
+            dk = scale * (ds.T @ qr) + p.T @ g             # [nk, D]
+            ns = sel.shape[0]
+            if ns:
+                np.add.at(dent[b], sel, dk[:ns])
+            if hi > lo:
+                dkv[b, lo:hi] += rope_derotate(dk[ns:], u, inv_freq)
+            if z is not None:
+                dsink -= np.exp(z - m) / den * delta
+    return dq, dkv, dent, dsink
 
 
 # ---------------------------------------------------------------------------
