@@ -215,6 +215,43 @@ v4_status v4_sparse_mqa_fwd_noalloc(const v4_config* cfg, const void* q, const v
                                     const float* inv_freq, void* o, float* lse, void* stream);
 
 /* ----------------------------------------------------------------------
+ * Backward of v4_sparse_mqa_fwd: the gradients of L = sum(dout * o).
+ * [BLOG] "Attention kernels for the three layer types", backward: a dQ pass
+ * that regathers the keys and recomputes the softmax, the delta
+ * rowsum(O * dO), and a head-dimension contraction scattered into the
+ * key/value gradient (fused here with dQ; fp32 reductions in L2).
+ *
+ * With p = softmax probabilities of v4_sparse_mqa_fwd (from lse), g =
+ * rot(dout, t), delta = dout . o and ds = p (g . key - delta):
+ *   dq   = rot(scale * sum_j ds_j key_j, -t)
+ *   dkey = scale * sum_h ds_h rot(q_h, t) + sum_h p_h g_h     (key = value)
+ *   dent[b, e] = sum of dkey over every (query, slot) that read entry e
+ *   dkv[b, u]  = rot(sum of dkey over queries whose window holds u, -u)
+ *   dsink[h]   = -sum_t exp(sink[h] - lse[t, h]) delta[t, h]
+ *
+ * Inputs are those of the forward call plus its outputs:
+ *   o    : [B, S, H, D] the forward output.   lse : [B, S, H] fp32 (required).
+ *   dout : [B, S, H, D] gradient of o.
+ * Outputs (overwritten):
+ *   dq    : [B, S, H, D] (storage dtype).
+ *   dkv   : [B, S, D] fp32, gradient of the un-rotated window latent kv.
+ *   dent  : [B, N, D] fp32, gradient of the rotated entries; required iff
+ *           r > 0 and N > 0, else NULL.
+ *   dsink : [H] fp32; required iff sink != NULL.
+ * Shapes: those of the tensor-core forward (bf16, H a multiple of 64 up to
+ * 512, D = 512, R = 64, 1 <= W <= 128, K <= 1024); others return
+ * V4_ERR_UNSUPPORTED.  Reduction order of dkv / dent / dsink follows the
+ * GPU's scheduling, so they are not bitwise reproducible.
+ * workspace : at least v4_bwd_workspace_size bytes, 256-byte aligned.
+ * --------------------------------------------------------------------*/
+v4_status v4_bwd_workspace_size(const v4_config* cfg, size_t* bytes);
+v4_status v4_sparse_mqa_bwd(const v4_config* cfg, const void* q, const void* kv,
+                            const void* ent, const int32_t* idx, const float* sink,
+                            const float* inv_freq, const void* o, const float* lse,
+                            const void* dout, void* dq, float* dkv, float* dent,
+                            float* dsink, void* workspace, size_t ws_bytes, void* stream);
+
+/* ----------------------------------------------------------------------
  * Grouped low-rank output projection.  [BLOG] "The DeepSeek-V4-Flash
  * architecture": the 64 x 512 output splits into o_groups groups, each
  * through an o_rank bottleneck.  Group g holds heads g*H/G .. (g+1)*H/G-1
@@ -283,7 +320,9 @@ uint64_t v4_launch_count(void);
  * records and starts recording; v4_profile_enable(0) stops.  Record i
  * (launch order, 0-based) is read with v4_profile_get, which waits for its
  * stop event.  kind: 0 compressor, 1 window-key rotation, 2 indexer query
- * prep, 3 indexer scores, 4 top-k, 5 attention, 6 output projection.
+ * prep, 3 indexer scores, 4 top-k, 5 attention, 6 output projection,
+ * 7 backward prep (clears, tables, key rotation, query/gradient rotation and
+ * delta), 8 attention backward, 9 window-gradient de-rotation.
  * --------------------------------------------------------------------*/
 v4_status v4_profile_enable(int32_t on);
 int32_t v4_profile_count(void);

@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for the compressed-attention forward.
+"""Seeded synthetic inputs for the compressed-attention forward and backward.
 
 Shared by the tests, ``bench.py`` and the callers of the CPU oracle.  It holds
 no step of the attention method: only workload shapes, random draws in a fixed
@@ -135,6 +135,24 @@ def make_layer_inputs(p, device="cpu", seed=0, sink=False, wo_a=False):
     else:
         x["wo_a"] = None
     return x
+
+
+def make_entries(p, device="cpu", seed=3):
+    """Stand-in for compressor output when the attention is tested alone:
+    unit-RMS N(0,1) rows [B, S // ratio, D] in the storage dtype (the
+    compressor's entries are RMS-normalised rows)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    N = p["S"] // p["ratio"] if p["ratio"] > 0 else 0
+    return _unit_rms(_normal((p["B"], N, p["D"]), g, device)).to(torch_dtype(p))
+
+
+def make_output_grad(p, device="cpu", seed=2):
+    """Gradient of the attention output for the backward: unit-RMS rows of
+    N(0,1), [B,S,H,D] in the preset's storage dtype."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return _unit_rms(_normal((p["B"], p["S"], p["H"], p["D"]), g, device)).to(torch_dtype(p))
 
 
 def random_topk_indices(B, S, ratio, K, device="cpu", seed=1):

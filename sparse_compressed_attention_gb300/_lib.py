@@ -26,9 +26,10 @@ STATUS_NAMES = {0: "V4_OK", 1: "V4_ERR_INVALID_ARG", 2: "V4_ERR_UNSUPPORTED", 3:
 EXPORTS = ["v4_rope_inv_freq", "v4_workspace_size", "v4_compress", "v4_indexer_prep",
            "v4_indexer_topk", "v4_sparse_mqa_fwd", "v4_grouped_o_proj", "v4_attn_layer_fwd",
            "v4_last_error", "v4_get_device_status", "v4_reset_device_status", "v4_launch_count",
-           "v4_profile_enable", "v4_profile_count", "v4_profile_get", "v4_sparse_mqa_fwd_noalloc"]
+           "v4_profile_enable", "v4_profile_count", "v4_profile_get", "v4_sparse_mqa_fwd_noalloc",
+           "v4_bwd_workspace_size", "v4_sparse_mqa_bwd"]
 PROFILE_KINDS = {0: "compress", 1: "window_rotate", 2: "indexer_prep", 3: "indexer_scores", 4: "topk",
-                 5: "attention", 6: "o_proj"}
+                 5: "attention", 6: "o_proj", 7: "bwd_prep", 8: "bwd_attention", 9: "bwd_derotate"}
 
 
 class V4Error(RuntimeError):
@@ -78,6 +79,8 @@ def lib(path=None):
         "v4_sparse_mqa_fwd": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
         "v4_sparse_mqa_fwd_noalloc": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
         "v4_grouped_o_proj": [cfgp, vp, vp, vp, vp],
+        "v4_bwd_workspace_size": [cfgp, C.POINTER(sz)],
+        "v4_sparse_mqa_bwd": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
         "v4_attn_layer_fwd": [cfgp, C.POINTER(v4_layer_inputs), C.POINTER(v4_layer_outputs), vp, sz, vp],
         "v4_get_device_status": [vp, C.POINTER(i32)],
         "v4_reset_device_status": [vp],
@@ -213,6 +216,34 @@ def v4_sparse_mqa_fwd_noalloc(cfg, q, kv, ent, idx, sink, inv_freq, o, lse, stre
                                            _ptr(o, "o", dt), _ptr(lse, "lse", torch.float32, optional=True),
                                            _stream(stream)))
     return o
+
+
+def v4_bwd_workspace_size(cfg):
+    n = C.c_size_t(0)
+    _check(lib().v4_bwd_workspace_size(C.byref(cfg), C.byref(n)))
+    return n.value
+
+
+def alloc_bwd_workspace(cfg, device=None):
+    return torch.empty(max(v4_bwd_workspace_size(cfg), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def v4_sparse_mqa_bwd(cfg, q, kv, ent, idx, sink, inv_freq, o, lse, dout, dq, dkv, dent, dsink, workspace,
+                      stream=None):
+    """Gradients of sum(dout * o) for v4_sparse_mqa_fwd; dq, dkv, dent, dsink are written."""
+    dt = _storage(cfg)
+    _check(lib().v4_sparse_mqa_bwd(C.byref(cfg), _ptr(q, "q", dt), _ptr(kv, "kv", dt),
+                                   _ptr(ent, "ent", dt, optional=True),
+                                   _ptr(idx, "idx", torch.int32, optional=True),
+                                   _ptr(sink, "sink", torch.float32, optional=True),
+                                   _ptr(inv_freq, "inv_freq", torch.float32),
+                                   _ptr(o, "o", dt), _ptr(lse, "lse", torch.float32), _ptr(dout, "dout", dt),
+                                   _ptr(dq, "dq", dt), _ptr(dkv, "dkv", torch.float32),
+                                   _ptr(dent, "dent", torch.float32, optional=True),
+                                   _ptr(dsink, "dsink", torch.float32, optional=True),
+                                   _ptr(workspace, "workspace", torch.uint8), workspace.numel(),
+                                   _stream(stream)))
+    return dq, dkv, dent, dsink
 
 
 def v4_grouped_o_proj(cfg, o, wo_a, y, stream=None):

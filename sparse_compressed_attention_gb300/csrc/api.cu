@@ -64,7 +64,7 @@ static bool g_prof_on = false;
 static std::vector<ProfRec> g_prof;
 
 enum { K_COMPRESS = 0, K_ROTATE = 1, K_IDX_PREP = 2, K_IDX_SCORE = 3, K_TOPK = 4, K_ATTN = 5,
-       K_OPROJ = 6 };
+       K_OPROJ = 6, K_BWD_PREP = 7, K_BWD_ATTN = 8, K_BWD_FIN = 9 };
 
 struct ProfScope {
   bool on = false;
@@ -123,6 +123,31 @@ Workspace plan_workspace(const v4_config& c) {
   // redo list: one entry per (query, 64-head slice) at most
   take(w.counters, w.counters_bytes, (2 + B * S * (size_t)(c.n_heads > 64 ? (c.n_heads + 63) / 64 : 1)) * 4);
   take(w.rope, w.rope_bytes, S * (size_t)(c.rope_dim / 2) * 8);
+  w.total = off;
+  return w;
+}
+
+// Backward workspace: cos/sin table, rotated window keys with their norms,
+// rotated queries and output gradients, delta.
+struct BwdWorkspace {
+  size_t rope = 0, kv_rot = 0, knorm = 0, qr = 0, dor = 0, delta = 0, total = 0;
+};
+
+static BwdWorkspace plan_bwd_workspace(const v4_config& c) {
+  BwdWorkspace w;
+  const size_t es = c.dtype == V4_BF16 ? 2 : 4;
+  const size_t B = c.batch, S = c.seqlen, D = c.head_dim, H = c.n_heads;
+  size_t off = 0;
+  auto take = [&](size_t& at, size_t n) {
+    at = off;
+    off = align256(off + n);
+  };
+  take(w.rope, S * (size_t)(c.rope_dim / 2) * 8);
+  take(w.kv_rot, B * S * D * es);
+  take(w.knorm, key_norm_floats(c) * 4);
+  take(w.qr, B * S * H * D * es);
+  take(w.dor, B * S * H * D * es);
+  take(w.delta, B * S * H * 4);
   w.total = off;
   return w;
 }
@@ -393,6 +418,82 @@ v4_status v4_sparse_mqa_fwd(const v4_config* cfg, const void* q, const void* kv,
   if (s != V4_OK) return s;
   return do_mqa(*cfg, q, kv, ent, cfg->topk > 0 ? idx : nullptr, sink, inv_freq, o, lse,
                 (char*)workspace, (cudaStream_t)stream, false);
+}
+
+v4_status v4_bwd_workspace_size(const v4_config* cfg, size_t* bytes) {
+  v4_status s = check_cfg(cfg);
+  if (s != V4_OK) return s;
+  if (!bytes) return fail(V4_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = plan_bwd_workspace(*cfg).total;
+  return V4_OK;
+}
+
+v4_status v4_sparse_mqa_bwd(const v4_config* cfg, const void* q, const void* kv, const void* ent,
+                            const int32_t* idx, const float* sink, const float* inv_freq, const void* o,
+                            const float* lse, const void* dout, void* dq, float* dkv, float* dent,
+                            float* dsink, void* workspace, size_t ws_bytes, void* stream) {
+  v4_status s = check_cfg(cfg);
+  if (s != V4_OK) return s;
+  const v4_config& c = *cfg;
+  if (!mqa_bwd_tc_supported(c))
+    return fail(V4_ERR_UNSUPPORTED,
+                "attention backward needs bf16, H a multiple of 64 up to 512, D=512, R=64, 1 <= W <= 128, K <= 1024");
+  const bool comp = c.ratio > 0 && c.seqlen / c.ratio > 0;
+  REQ(q, "q");
+  REQ(kv, "kv");
+  REQ(o, "o");
+  REQ(lse, "lse");
+  REQ(dout, "dout");
+  REQ(dq, "dq");
+  REQ(dkv, "dkv");
+  REQ(inv_freq, "inv_freq");
+  if (comp) {
+    REQ(ent, "ent");
+    REQ(dent, "dent");
+  }
+  if (c.topk > 0) REQ(idx, "idx");
+  OPT(sink, "sink");
+  if (sink) REQ(dsink, "dsink");
+  const BwdWorkspace plan = plan_bwd_workspace(c);
+  if (ws_bytes < plan.total) return fail(V4_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, plan.total);
+  if (!workspace) return fail(V4_ERR_WORKSPACE, "workspace is NULL");
+  if ((uintptr_t)workspace & 255u) return fail(V4_ERR_WORKSPACE, "workspace not 256-byte aligned");
+  int* status = status_ptr();
+  if (!status) return fail(V4_ERR_CUDA, "device status word unavailable");
+  char* ws = (char*)workspace;
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t B = c.batch, S = c.seqlen, D = c.head_dim;
+  const size_t N = comp ? S / c.ratio : 0;
+  const float2* table = (const float2*)(ws + plan.rope);
+  float* delta = (float*)(ws + plan.delta);
+  void* kv_rot = ws + plan.kv_rot;
+  {
+    ProfScope ps(K_BWD_PREP, st);
+    CU(cudaMemsetAsync(dkv, 0, B * S * D * 4, st), "dkv clear");
+    if (comp) CU(cudaMemsetAsync(dent, 0, B * N * D * 4, st), "dent clear");
+    if (sink) CU(cudaMemsetAsync(dsink, 0, (size_t)c.n_heads * 4, st), "dsink clear");
+    CU(launch_rope_table(c, inv_freq, (float2*)(ws + plan.rope), st), "rope table kernel");
+    float* kv_norm = (float*)(ws + plan.knorm);
+    float* ent_norm = kv_norm + B * S;
+    float* wmax = ent_norm + B * N;
+    float* emax = wmax + B * S;
+    CU(launch_key_prep(c, kv, comp ? ent : nullptr, table, kv_rot, kv_norm, ent_norm, wmax, emax, st),
+       "key prep kernel");
+    CU(launch_mqa_bwd_prep(c, q, o, dout, lse, sink, table, ws + plan.qr, ws + plan.dor, delta, sink ? dsink : nullptr,
+                           st),
+       "backward prep kernel");
+  }
+  {
+    ProfScope ps(K_BWD_ATTN, st);
+    CU(launch_mqa_bwd_tc(c, ws + plan.qr, ws + plan.dor, kv_rot, comp ? ent : nullptr, c.topk > 0 ? idx : nullptr,
+                         lse, delta, table, dq, dkv, comp ? dent : nullptr, status, st),
+       "tensor-core attention backward kernel");
+  }
+  {
+    ProfScope ps(K_BWD_FIN, st);
+    CU(launch_mqa_bwd_derotate(c, dkv, table, st), "window-gradient de-rotation kernel");
+  }
+  return V4_OK;
 }
 
 static v4_status check_oproj(const v4_config& c) {

@@ -92,4 +92,20 @@ cudaError_t launch_mqa_tc(const v4_config& c, const void* q, const void* kv_rot,
                           const float* wmax, const float* emax, void* o, float* lse,
                           int* counters, int* status, cudaStream_t st);
 
+// ---- attention backward (mqa_bwd_tc.cu)
+bool mqa_bwd_tc_supported(const v4_config& c);
+// qr = rot(q, t), dor = rot(dout, t) (storage dtype), delta = dout . o per
+// (query, head); dsink (nullable, pre-zeroed) += -exp(sink - lse) delta.
+cudaError_t launch_mqa_bwd_prep(const v4_config& c, const void* q, const void* o, const void* dout,
+                                const float* lse, const float* sink, const float2* cs_table, void* qr, void* dor,
+                                float* delta, float* dsink, cudaStream_t st);
+// dq, and the fp32 reductions into dkv (gradient of the rotated window keys,
+// pre-zeroed) and dent (pre-zeroed; nullable when there are no entries).
+cudaError_t launch_mqa_bwd_tc(const v4_config& c, const void* qr, const void* dor, const void* kv_rot,
+                              const void* ent, const int32_t* idx, const float* lse, const float* delta,
+                              const float2* cs_table, void* dq, float* dkv, float* dent, int* status,
+                              cudaStream_t st);
+// dkv[b, u] = rot(dkv[b, u], -u) in place
+cudaError_t launch_mqa_bwd_derotate(const v4_config& c, float* dkv, const float2* cs_table, cudaStream_t st);
+
 }  // namespace v4
