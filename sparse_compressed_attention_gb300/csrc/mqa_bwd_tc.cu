@@ -31,8 +31,11 @@
 // Warp roles (384 threads): warp 0 producer (per-query selection list, [Qr; dO']
 // by TMA, a third of the key gathers), warp 1 MMA issuer and TMEM owner,
 // warps 2-3 the other gathers, warps 4-7 softmax (TMEM lane quarters 0-1
-// hold the S rows, 2-3 the dP rows; P crosses through shared memory), warps
-// 8-11 reduce dKV^T into the accumulators and write dQ.
+// hold the S rows, 2-3 the dP rows; P crosses through shared memory; they
+// also reduce keys 16..31 of each dKV^T tile), warps 8-11 reduce keys 0..15
+// and write dQ.  Element-wise fp32 reductions from the SM reach the L2's
+// rate only with many warps issuing them: four warps alone measured about
+// 14 GB/s per SM and bounded the whole kernel.
 #include <cuda.h>
 #include <math.h>
 
@@ -147,6 +150,33 @@ __device__ __forceinline__ void gather_tile(uint8_t* kbuf, const QInfo& q, const
   cp_async_mbar_arrive(full);
 }
 
+// Reduce keys [k0, k0 + 16) of tile j's dKV^T (all four M-blocks) into the
+// fp32 accumulators and release each M-block's TMEM columns.  The warp's 32
+// TMEM lanes are 32 consecutive dims of an M-block: one warp-wide 128-byte
+// reduction per key.  Keys past the query's last carry exact zeros; they add
+// into the tile's first key row, so the loop has no branch.
+__device__ __forceinline__ void drain_dkv(uint32_t t_dkv, int k0, const QInfo& q, const int32_t* lst, int j,
+                                          int lane, int quarter, const Params& p, int BN, Ctl* c) {
+  const int kk = kT * j + k0 + (lane & 15);
+  const int rid = key_row(q, lst, kk < q.n_keys ? kk : kT * j, p.N, p.S, BN);
+  float* rowp = rid < BN ? p.dent + (size_t)rid * kD : p.dkr + (size_t)(rid - BN) * kD;
+  const unsigned long long rowv = reinterpret_cast<unsigned long long>(rowp);
+#pragma unroll 1
+  for (int m = 0; m < 4; ++m) {
+    float v[16];
+    tmem_ld16(t_dkv + kT * m + k0, v);
+    tmem_wait_ld();
+    tc_fence_before();
+    mbar_arrive(&c->dkv_empty[m]);
+    const int d = 128 * m + 32 * quarter + lane;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      float* dst = reinterpret_cast<float*>(__shfl_sync(0xffffffffu, rowv, k)) + d;
+      atomicAdd(dst, v[k]);
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 mqa_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
                   const Params p) {
@@ -168,12 +198,12 @@ mqa_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       mbar_init(&c->sd_empty[i], kSoftThreads);
       mbar_init(&c->info_full[i], 1);
       mbar_init(&c->info_empty[i], 64 + 1 + kSoftThreads + kEpiThreads);
-      mbar_init(&c->list_free[i], 64 + kEpiThreads);
+      mbar_init(&c->list_free[i], 64 + kSoftThreads + kEpiThreads);
     }
     mbar_init(&c->ds_ready, kSoftThreads);
     mbar_init(&c->ds_free, 1);
     mbar_init(&c->dkv_full, 1);
-    for (int m = 0; m < 4; ++m) mbar_init(&c->dkv_empty[m], kEpiThreads);
+    for (int m = 0; m < 4; ++m) mbar_init(&c->dkv_empty[m], kSoftThreads + kEpiThreads);
     mbar_init(&c->dq_full, 1);
     mbar_init(&c->dq_empty, kEpiThreads);
     mbar_init(&c->fin, 1);
@@ -225,9 +255,14 @@ mqa_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         const int nv = p.ratio > 0 ? min((t + 1) / p.ratio, p.N) : 0;
         const unsigned below = (1u << lane) - 1u;
         if (inf.listed) {
+          // every load first, then the ballots: one memory latency per row
           const int32_t* row = p.idx + ((size_t)b * p.S + t) * p.K;
-          for (int i0 = 0; i0 < p.K; i0 += 32) {
-            int v = i0 + lane < p.K ? row[i0 + lane] : -1;
+          int sv[kMaxSel / 32];
+#pragma unroll
+          for (int i = 0; i < kMaxSel / 32; ++i) sv[i] = 32 * i + lane < p.K ? row[32 * i + lane] : -1;
+#pragma unroll
+          for (int i = 0; i < kMaxSel / 32; ++i) {
+            int v = sv[i];
             if (v < -1 || v >= nv) {
               set_status(p.status, kStatusBadIndex);
               v = -1;
@@ -396,6 +431,7 @@ mqa_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     int qc = 0, g = 0;
     QInfo inf;
     while (receive(qc, inf)) {
+      const int32_t* lst = lists + (qc & 1) * kMaxSel;
       const size_t hrow = ((size_t)inf.b * p.S + inf.t) * p.H + kH * inf.hs + h;
       const float lse2 = is_s ? p.lse[hrow] * log2e : 0.f;
       const float dlt = is_s ? 0.f : p.delta[hrow];
@@ -442,6 +478,20 @@ mqa_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                          pack_bf16x2(x[8 * c8 + 4], x[8 * c8 + 5]), pack_bf16x2(x[8 * c8 + 6], x[8 * c8 + 7]));
         fence_proxy_async_smem();
         mbar_arrive(&c->ds_ready);
+        // keys 16..31 of the previous tile's dKV^T (its products completed
+        // with the ds_free phase waited above); the query's last tile is
+        // drained once its products finish
+        if (j >= 1) {
+          wait_ok(&c->dkv_full, (gj - 1) & 1, c, p.status);
+          tc_fence_after();
+          drain_dkv(tmem + lane_base + TM_DKV, 16, inf, lst, j - 1, lane, quarter, p, BN, c);
+        }
+        if (j == inf.tiles - 1) {
+          wait_ok(&c->dkv_full, gj & 1, c, p.status);
+          tc_fence_after();
+          drain_dkv(tmem + lane_base + TM_DKV, 16, inf, lst, j, lane, quarter, p, BN, c);
+          mbar_arrive(&c->list_free[qc & 1]);
+        }
       }
       g += inf.tiles;
       ++qc;
@@ -457,29 +507,10 @@ mqa_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       const int32_t* lst = lists + is * kMaxSel;
       for (int j = 0; j < inf.tiles; ++j) {
         const int gj = g + j;
-        const int rid = kT * j + lane < inf.n_keys ? key_row(inf, lst, kT * j + lane, p.N, p.S, BN) : -1;
-        if (j == inf.tiles - 1) mbar_arrive(&c->list_free[is]);
         wait_ok(&c->dkv_full, gj & 1, c, p.status);
         tc_fence_after();
-#pragma unroll 1
-        for (int m = 0; m < 4; ++m) {
-          float v[32];
-          tmem_ld32(tmem + lane_base + TM_DKV + kT * m, v);
-          tmem_wait_ld();
-          tc_fence_before();
-          mbar_arrive(&c->dkv_empty[m]);
-          const int d = 128 * m + 32 * quarter + lane;
-          // a warp's 32 lanes cover 32 consecutive dims of one key: one
-          // 128-byte reduction per key
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int r = __shfl_sync(0xffffffffu, rid, k);
-            if (r >= 0) {
-              float* dst = r < BN ? p.dent + (size_t)r * kD + d : p.dkr + (size_t)(r - BN) * kD + d;
-              atomicAdd(dst, v[k]);
-            }
-          }
-        }
+        drain_dkv(tmem + lane_base + TM_DKV, 0, inf, lst, j, lane, quarter, p, BN, c);      // keys 0..15
+        if (j == inf.tiles - 1) mbar_arrive(&c->list_free[is]);
       }
       g += inf.tiles;
       // dQ^T [dim, head]: de-rotate the last 64 dims at -t, store bf16
