@@ -43,7 +43,10 @@ Readings of points the pages leave open (each is listed in the design doc):
     softmax denominator only;
   * the attention backward is the exact gradient of this forward (the pages
     give its kernels, not its formulas): entry gradients are w.r.t. the stored
-    rotated entries, window gradients w.r.t. the un-rotated latent.
+    rotated entries, window gradients w.r.t. the un-rotated latent;
+  * the opt-in E4M3 indexer scales every query-head row and every key row by
+    its absolute maximum (the pages name the format, not the scaling), and
+    takes the quantisation decision in float32 as the kernel does.
 """
 from __future__ import annotations
 
@@ -320,6 +323,82 @@ def indexer_topk(iq, ikey, w, inv_freq, ratio, k, store_bf16=False, rows=None,
     qp = np.asarray(iq, dtype=F64) if prepared else indexer_query_prep(iq, inv_freq, store_bf16,
                                                                        positions=rows_)
     sc = indexer_scores(qp, ikey, w, ratio, rows_, rows_only=True)
+    B, T, N = sc.shape
+    idx = np.full((B, T, k), -1, dtype=np.int32)
+    isc = np.full((B, T, k), -np.inf, dtype=F64)
+    for b in range(B):
+        for i, t in enumerate(rows_):
+            idx[b, i], isc[b, i] = topk_select(sc[b, i], min(n_visible(int(t), ratio), N), k)
+    return {"idx": idx, "iscore": isc, "scores": sc}
+
+
+# ---------------------------------------------------------------------------
+# Opt-in E4M3 indexer QK  ([PR] item 4: the indexer QK stays in high
+# precision by default, FP8 only behind its own switch, because quantisation
+# error changes the selection; [BLOG] closing section: an E4M3 path for the
+# indexer QK ships)
+# ---------------------------------------------------------------------------
+E4M3_MAX = 448.0
+
+
+def round_to_e4m3(x):
+    """Nearest E4M3 ("FN": no infinities) value, ties to even, saturating.
+
+    E4M3 has 1 sign, 4 exponent (bias 7) and 3 mantissa bits.  Normal values
+    are (1 + m/8) * 2**(e-7) for e = 1..15, except that e = 15 with m = 7 is
+    NaN, so the largest finite value is 1.75 * 2**8 = 448; subnormals are
+    m/8 * 2**-6.  Hence for |x| >= 2**-6 the spacing is 2**(floor(log2|x|) - 3)
+    and below 2**-6 it is 2**-9.  Rounding to the nearest multiple of the
+    spacing with numpy's ``rint`` sends halfway cases to the even significand;
+    magnitudes beyond 448 saturate to 448 (the "satfinite" conversion).
+    Result kept in float64.
+    """
+    x = np.asarray(x, dtype=F64)
+    a = np.abs(x)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))      # a = m * 2**ex, 0.5 <= m < 1
+    e = np.maximum(ex - 1, -6)                      # floor(log2 a), clamped to the subnormal range
+    q = np.ldexp(1.0, e - 3)
+    r = np.minimum(np.rint(a / q) * q, E4M3_MAX)
+    return np.copysign(r, x)
+
+
+def quantize_e4m3_rows(x):
+    """Per-row absolute-maximum scaling of x [..., dim] to E4M3.
+
+    The plainest reading of an E4M3 QK (the pages name the format, not the
+    scaling): each row (one query head, one key) gets scale = amax / 448 and
+    code = e4m3(x * (448 / amax)), so that x ~= code * scale.  The code is an
+    integer-like decision taken in float32 as the kernel takes it: amax is
+    exact (x holds bf16 values), 448 / amax and amax / 448 are float32
+    divisions and x * inv a float32 product, each rounded to nearest.  An
+    all-zero row has scale 0 and zero codes.
+    Returns (codes [..., dim] float64 values of E4M3 numbers, scales [...]).
+    """
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x32), axis=-1)
+    pos = amax > 0
+    one = np.float32(E4M3_MAX)
+    safe = np.where(pos, amax, np.float32(1.0)).astype(np.float32)
+    inv = np.where(pos, one / safe, np.float32(0.0)).astype(np.float32)
+    scale = np.where(pos, safe / one, np.float32(0.0)).astype(np.float32)
+    prod = (x32 * inv[..., None]).astype(np.float32)
+    return round_to_e4m3(prod.astype(F64)), scale.astype(F64)
+
+
+def indexer_scores_e4m3(q_codes, q_scales, k_codes, k_scales, w, ratio, rows=None, rows_only=False):
+    """Indexer scores of quantised operands: q~[t,h] = q_codes * q_scales[t,h]
+    and k[s] = k_codes * k_scales[s] dequantised exactly (float64), then the
+    scores of ``indexer_scores``.  Same arguments and result shape."""
+    qd = np.asarray(q_codes, dtype=F64) * np.asarray(q_scales, dtype=F64)[..., None]
+    kd = np.asarray(k_codes, dtype=F64) * np.asarray(k_scales, dtype=F64)[..., None]
+    return indexer_scores(qd, kd, w, ratio, rows, rows_only)
+
+
+def indexer_topk_e4m3(q_codes, q_scales, k_codes, k_scales, w, ratio, k, rows=None, rows_only=False):
+    """Top-k selection of the E4M3 scores (same rules as ``indexer_topk``)."""
+    S = np.asarray(q_codes).shape[1]
+    rows_ = np.arange(S) if rows is None else np.asarray(rows)
+    sc = indexer_scores_e4m3(q_codes, q_scales, k_codes, k_scales, w, ratio, rows_, rows_only)
     B, T, N = sc.shape
     idx = np.full((B, T, k), -1, dtype=np.int32)
     isc = np.full((B, T, k), -np.inf, dtype=F64)

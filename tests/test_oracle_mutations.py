@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 
 from oracle import v4_oracle as O
+import tests.test_oracle_fp8_pins as F
 import tests.test_oracle_pins as P
 
 _rope = O.rope_rotate
@@ -63,6 +64,47 @@ def _rotate_at_entry_index(ckv, cscore, ape, g, f, r, ov, eps, hadamard=False, s
     return O.maybe_bf16(e, store_bf16)
 
 
+_e4m3 = O.round_to_e4m3
+_quant = O.quantize_e4m3_rows
+
+
+def _e4m3_two_mantissa_bits(x):
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))
+    q = np.ldexp(1.0, np.maximum(ex - 1, -6) - 2)
+    return np.copysign(np.minimum(np.rint(a / q) * q, 448.0), x)
+
+
+def _e4m3_half_up(x):
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))
+    q = np.ldexp(1.0, np.maximum(ex - 1, -6) - 3)
+    return np.copysign(np.minimum(np.floor(a / q + 0.5) * q, 448.0), x)
+
+
+def _e4m3_no_saturation(x):
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))
+    q = np.ldexp(1.0, np.maximum(ex - 1, -6) - 3)
+    return np.copysign(np.rint(a / q) * q, x)
+
+
+def _quant_inverted_scale(x):
+    codes, scales = _quant(x)
+    return codes, np.where(scales > 0, 1.0 / np.where(scales > 0, scales, 1.0), 0.0)
+
+
+def _quant_tensor_scale(x):
+    x = np.asarray(x, dtype=np.float64)
+    amax = np.abs(x).max()
+    s = amax / 448.0 if amax > 0 else 0.0
+    codes = _e4m3(x / s) if s > 0 else np.zeros_like(x)
+    return codes, np.full(x.shape[:-1], s)
+
+
 MUTATIONS = [
     ("rope_rotate", _flip_sign, P.test_rope_is_complex_multiplication),
     ("sparse_mqa", _inflated_scale, P.test_softmax_scale_is_head_dim_power),
@@ -71,10 +113,15 @@ MUTATIONS = [
     ("window_range", _window_off_by_one, P.test_hca_equals_dense_masked_sdpa),
     ("hadamard_matrix", _unnormalised_hadamard, P.test_indexer_scores_invariant_under_hadamard),
     ("compress", _rotate_at_entry_index, P.test_constant_score_gives_mean_of_members),
+    ("round_to_e4m3", _e4m3_two_mantissa_bits, F.test_e4m3_code_points_and_range),
+    ("round_to_e4m3", _e4m3_half_up, F.test_e4m3_matches_library_cast_in_range),
+    ("round_to_e4m3", _e4m3_no_saturation, F.test_e4m3_saturates),
+    ("quantize_e4m3_rows", _quant_inverted_scale, F.test_quantizer_error_within_half_spacing),
+    ("quantize_e4m3_rows", _quant_tensor_scale, F.test_quantizer_row_maximum_lands_on_448),
 ]
 
 
-@pytest.mark.parametrize("name,mutant,pin", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+@pytest.mark.parametrize("name,mutant,pin", MUTATIONS, ids=["%s-%s" % (m[0], m[1].__name__) for m in MUTATIONS])
 def test_pin_catches_planted_mistake(monkeypatch, name, mutant, pin):
     monkeypatch.setattr(O, name, mutant)
     with pytest.raises(AssertionError):
