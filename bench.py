@@ -201,7 +201,7 @@ def barrier():
 # ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
-def make_layer(name, S, device, seed, **over):
+def make_layer(name, S, device, seed, indexer_fp8=0, **over):
     import torch
 
     import seeded_inputs as SI
@@ -212,7 +212,7 @@ def make_layer(name, S, device, seed, **over):
     f = V.v4_rope_inv_freq(p["theta"], p["R"], yarn, SI.YARN_ORIGINAL_LEN if yarn > 1 else 0,
                            SI.YARN_BETA_FAST, SI.YARN_BETA_SLOW).to(device)
     x["inv_freq"] = f
-    cfg = V.config_from_preset(p)
+    cfg = V.config_from_preset(p, indexer_fp8=int(indexer_fp8) if p["K"] > 0 else 0)
     B, H = p["B"], p["H"]
     outs = {"o": torch.empty_like(x["q"]), "lse": torch.empty(B, S, H, device=device)}
     if p["K"] > 0:
@@ -496,12 +496,13 @@ def run_workload(args):
               "B=%d, S=%d, H=64, D=512, R=64, bf16" % (B, S))
     else:
         B = 1
-        order = [make_layer("csa_bf16_16k", S, dev, seed=3000)]
+        order = [make_layer("csa_bf16_16k", S, dev, seed=3000, indexer_fp8=args.indexer_fp8)]
         for L in order:
             L["name"] = "csa"
         metric = "CSA layer fwd tokens/s at S=%d" % S
-        wl = ("DeepSeek-V4-Flash CSA layer fwd (ratio 4 overlapped, indexer 64x128 fp32 scoring, top-512, "
-              "window 128), B=1, S=%d, H=64, D=512, R=64, bf16" % S)
+        scoring = "E4M3 operands, per-row scales" if args.indexer_fp8 else "bf16 operands"
+        wl = ("DeepSeek-V4-Flash CSA layer fwd (ratio 4 overlapped, indexer 64x128 %s, fp32 scoring, top-512, "
+              "window 128), B=1, S=%d, H=64, D=512, R=64, bf16" % (scoring, S))
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
         for L in order:
@@ -555,9 +556,13 @@ def run_workload(args):
     if isc:
         a_ms = sum(isc) / len(isc)
         tf = wk["idx_flops"] / (a_ms / 1e3) / 1e12
-        other.append({"kernel": "csa indexer scores", "bound": "tensor", "achieved": round(tf, 2),
-                      "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": round(tf / peaks["bf16"], 4),
-                      "flops_per_launch": wk["idx_flops"], "avg_launch_ms": round(a_ms, 4)})
+        fp8 = bool(csa["cfg"].indexer_fp8)
+        # E4M3 products: the measured bf16 peak times the nominal e4m3/bf16 ratio (4.5 / 2.25)
+        pk = peaks["bf16"] * (2.0 if fp8 else 1.0)
+        other.append({"kernel": "csa indexer scores" + (" (E4M3)" if fp8 else ""), "bound": "tensor",
+                      "achieved": round(tf, 2), "peak": round(pk, 1), "unit": "TFLOP/s",
+                      "frac": round(tf / pk, 4), "flops_per_launch": wk["idx_flops"],
+                      "avg_launch_ms": round(a_ms, 4)})
     op = [t for (n, k), v in per.items() if k == "o_proj" for t in v]
     if op:
         a_ms = sum(op) / len(op)
@@ -707,6 +712,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=6)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager calls instead of a captured step")
+    ap.add_argument("--indexer-fp8", type=int, choices=[0, 1], default=0,
+                    help="--workload csa: opt-in E4M3 indexer QK (the default keeps bf16 operands)")
     ap.add_argument("--workload", choices=["pair", "stack", "csa", "pro"], default="pair",
                     help="pair: the CSA + HCA layer pair (the reported line); stack: the 43-layer "
                          "Flash stack with grouped wo_a at B=2; csa: one CSA layer (e.g. --seq 65536); "

@@ -82,6 +82,8 @@ typedef struct v4_config {
   float rms_eps;          /* entry RMSNorm epsilon (1e-6) */
   int32_t dtype;          /* v4_dtype: storage dtype */
   int32_t path;           /* v4_path */
+  int32_t indexer_fp8;    /* 1 = opt-in E4M3 indexer QK (see v4_indexer_topk_e4m3);
+                             0 = bf16 operands, fp32 scoring (the default [PR] item 4 asks for) */
 } v4_config;
 
 /* ----------------------------------------------------------------------
@@ -162,6 +164,40 @@ v4_status v4_indexer_topk(const v4_config* cfg, const void* iq, int32_t iq_prepa
                           const void* ikey, const float* w, const float* inv_freq,
                           int32_t* idx, float* iscore, void* workspace,
                           size_t ws_bytes, void* stream);
+
+/* ----------------------------------------------------------------------
+ * Opt-in E4M3 indexer.  [PR] item 4 keeps the indexer QK in high precision
+ * by default, because quantisation error there changes which entries are
+ * selected, and puts FP8 behind its own switch; [BLOG] closing section: an
+ * E4M3 path for the indexer QK ships.  The pages name the format, not the
+ * scaling: here every row (one prepared query head, one indexer key) is
+ * scaled by its absolute maximum.
+ *
+ * v4_quantize_e4m3: x [rows, dim] bf16 -> codes [rows, dim] (E4M3 bytes,
+ *   OCP "FN" encoding) and scales [rows] fp32 with x ~= code * scale:
+ *   scale = amax / 448, code = E4M3(x * (448 / amax)), every step in fp32
+ *   rounded to nearest (the conversion saturates at +-448); an all-zero row
+ *   gets scale 0 and zero codes.  dim is 128, 256, 512 or 1024; rows >= 0.
+ *
+ * v4_indexer_topk_e4m3: the selection of v4_indexer_topk from quantised
+ *   operands (cfg as for the tensor-core indexer: bf16, Hi = 64, Di = 128):
+ *     q_codes [B, S, Hi, Di] with q_scales [B, S, Hi]  (prepared queries),
+ *     k_codes [B, N, Di]     with k_scales [B, N]      (indexer keys),
+ *     I[t,s] = sum_h w[t,h] (Hi*Di)^-1/2 max(0, (q_code q_scale) . (k_code k_scale)),
+ *   E4M3 tensor-core products with fp32 accumulation and fp32 scoring; idx,
+ *   iscore, tie rule and workspace as v4_indexer_topk.  Other shapes return
+ *   V4_ERR_UNSUPPORTED.
+ *
+ * With cfg->indexer_fp8 = 1, v4_indexer_topk and v4_attn_layer_fwd prepare
+ * the queries in bf16 as before, quantise queries and keys into the
+ * workspace with v4_quantize_e4m3's rule and select from the E4M3 scores.
+ * --------------------------------------------------------------------*/
+v4_status v4_quantize_e4m3(const void* x, int64_t rows, int32_t dim, uint8_t* codes, float* scales,
+                           void* stream);
+v4_status v4_indexer_topk_e4m3(const v4_config* cfg, const uint8_t* q_codes, const float* q_scales,
+                               const uint8_t* k_codes, const float* k_scales, const float* w,
+                               int32_t* idx, float* iscore, void* workspace, size_t ws_bytes,
+                               void* stream);
 
 /* ----------------------------------------------------------------------
  * Sparse / dense multi-query attention with sliding window, sink and
@@ -322,7 +358,8 @@ uint64_t v4_launch_count(void);
  * stop event.  kind: 0 compressor, 1 window-key rotation, 2 indexer query
  * prep, 3 indexer scores, 4 top-k, 5 attention, 6 output projection,
  * 7 backward prep (clears, tables, key rotation, query/gradient rotation and
- * delta), 8 attention backward, 9 window-gradient de-rotation.
+ * delta), 8 attention backward, 9 window-gradient de-rotation, 10 E4M3
+ * quantisation of the indexer operands.
  * --------------------------------------------------------------------*/
 v4_status v4_profile_enable(int32_t on);
 int32_t v4_profile_count(void);

@@ -27,9 +27,10 @@ EXPORTS = ["v4_rope_inv_freq", "v4_workspace_size", "v4_compress", "v4_indexer_p
            "v4_indexer_topk", "v4_sparse_mqa_fwd", "v4_grouped_o_proj", "v4_attn_layer_fwd",
            "v4_last_error", "v4_get_device_status", "v4_reset_device_status", "v4_launch_count",
            "v4_profile_enable", "v4_profile_count", "v4_profile_get", "v4_sparse_mqa_fwd_noalloc",
-           "v4_bwd_workspace_size", "v4_sparse_mqa_bwd"]
+           "v4_bwd_workspace_size", "v4_sparse_mqa_bwd", "v4_quantize_e4m3", "v4_indexer_topk_e4m3"]
 PROFILE_KINDS = {0: "compress", 1: "window_rotate", 2: "indexer_prep", 3: "indexer_scores", 4: "topk",
-                 5: "attention", 6: "o_proj", 7: "bwd_prep", 8: "bwd_attention", 9: "bwd_derotate"}
+                 5: "attention", 6: "o_proj", 7: "bwd_prep", 8: "bwd_attention", 9: "bwd_derotate",
+                 10: "indexer_quant"}
 
 
 class V4Error(RuntimeError):
@@ -42,7 +43,8 @@ class v4_config(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "batch", "seqlen", "n_heads", "head_dim", "rope_dim", "ratio", "overlap", "window", "topk",
         "idx_heads", "idx_dim", "o_groups", "o_rank")] + [
-        ("softmax_scale", C.c_float), ("rms_eps", C.c_float), ("dtype", C.c_int32), ("path", C.c_int32)]
+        ("softmax_scale", C.c_float), ("rms_eps", C.c_float), ("dtype", C.c_int32), ("path", C.c_int32),
+        ("indexer_fp8", C.c_int32)]
 
 
 class v4_layer_inputs(C.Structure):
@@ -76,6 +78,8 @@ def lib(path=None):
         "v4_compress": [cfgp, vp, vp, vp, vp, vp, i32, i32, vp, vp],
         "v4_indexer_prep": [cfgp, vp, vp, vp, vp],
         "v4_indexer_topk": [cfgp, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp],
+        "v4_quantize_e4m3": [vp, C.c_int64, i32, vp, vp, vp],
+        "v4_indexer_topk_e4m3": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
         "v4_sparse_mqa_fwd": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
         "v4_sparse_mqa_fwd_noalloc": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
         "v4_grouped_o_proj": [cfgp, vp, vp, vp, vp],
@@ -107,9 +111,10 @@ def _check(status):
 
 
 def make_config(B, S, H, D, R, ratio=0, overlap=0, window=128, topk=0, Hi=64, Di=128,
-                o_groups=8, o_rank=1024, scale=0.0, eps=1e-6, dtype="bf16", path=V4_PATH_AUTO):
+                o_groups=8, o_rank=1024, scale=0.0, eps=1e-6, dtype="bf16", path=V4_PATH_AUTO,
+                indexer_fp8=0):
     return v4_config(B, S, H, D, R, ratio, overlap, window, topk, Hi, Di, o_groups, o_rank,
-                     scale, eps, V4_BF16 if dtype == "bf16" else V4_F32, path)
+                     scale, eps, V4_BF16 if dtype == "bf16" else V4_F32, path, int(indexer_fp8))
 
 
 def config_from_preset(p, **over):
@@ -117,7 +122,8 @@ def config_from_preset(p, **over):
     q.update(over)
     return make_config(q["B"], q["S"], q["H"], q["D"], q["R"], q["ratio"], q["overlap"], q["W"],
                        q["K"], q["Hi"], q["Di"], dtype=q["dtype"], path=q.get("path", V4_PATH_AUTO),
-                       eps=q.get("eps", 1e-6), scale=q.get("scale", 0.0))
+                       eps=q.get("eps", 1e-6), scale=q.get("scale", 0.0),
+                       indexer_fp8=q.get("indexer_fp8", 0))
 
 
 def _storage(cfg):
@@ -189,6 +195,27 @@ def v4_indexer_topk(cfg, iq, iq_prepared, ikey, w, inv_freq, idx, iscore, worksp
                                  _ptr(iscore, "iscore", torch.float32, optional=True),
                                  _ptr(workspace, "workspace", torch.uint8), workspace.numel(),
                                  _stream(stream)))
+    return idx
+
+
+def v4_quantize_e4m3(x, codes, scales, stream=None):
+    """x [..., dim] bf16 -> codes [..., dim] uint8 (E4M3 bytes), scales [...] fp32."""
+    dim = x.shape[-1]
+    rows = x.numel() // dim if dim else 0
+    _check(lib().v4_quantize_e4m3(_ptr(x, "x", torch.bfloat16), rows, dim, _ptr(codes, "codes", torch.uint8),
+                                  _ptr(scales, "scales", torch.float32), _stream(stream)))
+    return codes, scales
+
+
+def v4_indexer_topk_e4m3(cfg, q_codes, q_scales, k_codes, k_scales, w, idx, iscore, workspace, stream=None):
+    _check(lib().v4_indexer_topk_e4m3(C.byref(cfg), _ptr(q_codes, "q_codes", torch.uint8),
+                                      _ptr(q_scales, "q_scales", torch.float32),
+                                      _ptr(k_codes, "k_codes", torch.uint8, optional=True),
+                                      _ptr(k_scales, "k_scales", torch.float32, optional=True),
+                                      _ptr(w, "w", torch.float32), _ptr(idx, "idx", torch.int32),
+                                      _ptr(iscore, "iscore", torch.float32, optional=True),
+                                      _ptr(workspace, "workspace", torch.uint8), workspace.numel(),
+                                      _stream(stream)))
     return idx
 
 

@@ -64,7 +64,7 @@ static bool g_prof_on = false;
 static std::vector<ProfRec> g_prof;
 
 enum { K_COMPRESS = 0, K_ROTATE = 1, K_IDX_PREP = 2, K_IDX_SCORE = 3, K_TOPK = 4, K_ATTN = 5,
-       K_OPROJ = 6, K_BWD_PREP = 7, K_BWD_ATTN = 8, K_BWD_FIN = 9 };
+       K_OPROJ = 6, K_BWD_PREP = 7, K_BWD_ATTN = 8, K_BWD_FIN = 9, K_IDX_QUANT = 10 };
 
 struct ProfScope {
   bool on = false;
@@ -123,6 +123,11 @@ Workspace plan_workspace(const v4_config& c) {
   // redo list: one entry per (query, 64-head slice) at most
   take(w.counters, w.counters_bytes, (2 + B * S * (size_t)(c.n_heads > 64 ? (c.n_heads + 63) / 64 : 1)) * 4);
   take(w.rope, w.rope_bytes, S * (size_t)(c.rope_dim / 2) * 8);
+  const bool e4m3 = sel && c.indexer_fp8 == 1;
+  take(w.qc8, w.qc8_bytes, e4m3 ? B * S * c.idx_heads * c.idx_dim : 0);
+  take(w.qs8, w.qs8_bytes, e4m3 ? B * S * c.idx_heads * 4 : 0);
+  take(w.kc8, w.kc8_bytes, e4m3 ? B * N * c.idx_dim : 0);
+  take(w.ks8, w.ks8_bytes, e4m3 ? B * N * 4 : 0);
   w.total = off;
   return w;
 }
@@ -179,6 +184,7 @@ static v4_status check_cfg(const v4_config* c) {
   if (c->dtype != V4_F32 && c->dtype != V4_BF16) return fail(V4_ERR_INVALID_ARG, "unknown dtype");
   if (c->path < V4_PATH_AUTO || c->path > V4_PATH_TC) return fail(V4_ERR_INVALID_ARG, "unknown path");
   if (!(c->rms_eps >= 0.f)) return fail(V4_ERR_INVALID_ARG, "rms_eps must be >= 0");
+  if (c->indexer_fp8 != 0 && c->indexer_fp8 != 1) return fail(V4_ERR_INVALID_ARG, "indexer_fp8 must be 0 or 1");
   return V4_OK;
 }
 
@@ -240,7 +246,26 @@ static v4_status do_indexer(const v4_config& c, const void* iq, int prepared, co
     iqp = ws + plan.iqp;
   }
   float* scores = (float*)(ws + plan.scores);
-  {
+  if (c.indexer_fp8) {
+    // opt-in E4M3: quantise the prepared queries and the keys per row
+    uint8_t* qc = (uint8_t*)(ws + plan.qc8);
+    float* qs = (float*)(ws + plan.qs8);
+    uint8_t* kc = (uint8_t*)(ws + plan.kc8);
+    float* ks = (float*)(ws + plan.ks8);
+    const long long N = c.seqlen / c.ratio;
+    {
+      ProfScope ps(K_IDX_QUANT, st);
+      CU(launch_quant_e4m3(iqp, (long long)c.batch * c.seqlen * c.idx_heads, c.idx_dim, qc, qs, st),
+         "E4M3 query quantisation kernel");
+      CU(launch_quant_e4m3(ikey, (long long)c.batch * N, c.idx_dim, kc, ks, st), "E4M3 key quantisation kernel");
+    }
+    int* status = status_ptr();
+    if (!status) return fail(V4_ERR_CUDA, "device status word unavailable");
+    {
+      ProfScope ps(K_IDX_SCORE, st);
+      CU(launch_indexer_scores_e4m3(c, qc, qs, kc, ks, w, scores, status, st), "E4M3 indexer kernel");
+    }
+  } else {
     ProfScope ps(K_IDX_SCORE, st);
     if (c.path != V4_PATH_SIMT && indexer_tc_supported(c)) {
       int* status = status_ptr();
@@ -393,10 +418,62 @@ v4_status v4_indexer_topk(const v4_config* cfg, const void* iq, int32_t iq_prepa
   if (!iq_prepared && cfg->rope_dim > 0) REQ(inv_freq, "inv_freq");
   if (cfg->path == V4_PATH_TC && !indexer_tc_supported(*cfg))
     return fail(V4_ERR_UNSUPPORTED, "tensor-core indexer needs bf16, idx_heads 64, idx_dim 128");
+  if (cfg->indexer_fp8 && (cfg->path == V4_PATH_SIMT || !indexer_e4m3_supported(*cfg)))
+    return fail(V4_ERR_UNSUPPORTED, "E4M3 indexer needs the tensor-core shapes: bf16, idx_heads 64, idx_dim 128");
   s = check_ws(*cfg, workspace, ws_bytes);
   if (s != V4_OK) return s;
   return do_indexer(*cfg, iq, iq_prepared ? 1 : 0, ikey, w, inv_freq, idx, iscore, (char*)workspace,
                     (cudaStream_t)stream, false);
+}
+
+v4_status v4_quantize_e4m3(const void* x, int64_t rows, int32_t dim, uint8_t* codes, float* scales,
+                           void* stream) {
+  if (rows < 0) return fail(V4_ERR_INVALID_ARG, "rows must be >= 0");
+  if (dim != 128 && dim != 256 && dim != 512 && dim != 1024)
+    return fail(V4_ERR_INVALID_ARG, "dim must be 128, 256, 512 or 1024");
+  if (rows == 0) return V4_OK;
+  REQ(x, "x");
+  REQ(codes, "codes");
+  REQ(scales, "scales");
+  CU(launch_quant_e4m3(x, (long long)rows, dim, codes, scales, (cudaStream_t)stream), "E4M3 quantisation kernel");
+  return V4_OK;
+}
+
+v4_status v4_indexer_topk_e4m3(const v4_config* cfg, const uint8_t* q_codes, const float* q_scales,
+                               const uint8_t* k_codes, const float* k_scales, const float* w, int32_t* idx,
+                               float* iscore, void* workspace, size_t ws_bytes, void* stream) {
+  v4_status s = check_cfg(cfg);
+  if (s != V4_OK) return s;
+  if (cfg->topk < 1) return fail(V4_ERR_INVALID_ARG, "indexer needs topk >= 1");
+  if (!indexer_e4m3_supported(*cfg) || cfg->path == V4_PATH_SIMT)
+    return fail(V4_ERR_UNSUPPORTED, "E4M3 indexer needs the tensor-core shapes: bf16, idx_heads 64, idx_dim 128");
+  REQ(q_codes, "q_codes");
+  REQ(q_scales, "q_scales");
+  REQ(w, "w");
+  REQ(idx, "idx");
+  OPT(iscore, "iscore");
+  if (cfg->seqlen / cfg->ratio > 0) {
+    REQ(k_codes, "k_codes");
+    REQ(k_scales, "k_scales");
+  }
+  s = check_ws(*cfg, workspace, ws_bytes);
+  if (s != V4_OK) return s;
+  const Workspace plan = plan_workspace(*cfg);
+  cudaStream_t st = (cudaStream_t)stream;
+  char* ws = (char*)workspace;
+  float* scores = (float*)(ws + plan.scores);
+  int* status = status_ptr();
+  if (!status) return fail(V4_ERR_CUDA, "device status word unavailable");
+  {
+    ProfScope ps(K_IDX_SCORE, st);
+    CU(launch_indexer_scores_e4m3(*cfg, q_codes, q_scales, k_codes, k_scales, w, scores, status, st),
+       "E4M3 indexer kernel");
+  }
+  {
+    ProfScope ps(K_TOPK, st);
+    CU(launch_topk(*cfg, scores, idx, iscore, st), "top-k kernel");
+  }
+  return V4_OK;
 }
 
 v4_status v4_sparse_mqa_fwd(const v4_config* cfg, const void* q, const void* kv, const void* ent,
@@ -567,6 +644,8 @@ v4_status v4_attn_layer_fwd(const v4_config* cfg, const v4_layer_inputs* in, v4_
   }
   if (c.path == V4_PATH_TC && !mqa_tc_supported(c))
     return fail(V4_ERR_UNSUPPORTED, "tensor-core attention needs bf16, H a multiple of 64 up to 512, D=512, R=64, 1 <= W <= 128, K <= 1024");
+  if (sel && c.indexer_fp8 && (c.path == V4_PATH_SIMT || !indexer_e4m3_supported(c)))
+    return fail(V4_ERR_UNSUPPORTED, "E4M3 indexer needs the tensor-core shapes: bf16, idx_heads 64, idx_dim 128");
   s = check_ws(c, workspace, ws_bytes);
   if (s != V4_OK) return s;
   char* ws = (char*)workspace;

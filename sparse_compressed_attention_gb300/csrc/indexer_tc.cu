@@ -22,7 +22,18 @@
 // owner, warps 2-9 epilogue (two per TMEM lane quarter, each summing two of
 // the four queries: one warp per quarter could not keep up with the MMAs).  Groups are handed out round-robin, heaviest
 // (largest t) first.  Flash shapes only: Hi = 64, Di = 128, bf16.
+//
+// The opt-in E4M3 variant (same kernel, kE4M3 = true) takes per-row scaled
+// E4M3 codes of the prepared queries and of the keys: one 128-byte K-block
+// per row instead of two, kind::f8f6f4 MMAs (K = 32), twice the stages.
+// With x ~= code * scale per row and positive scales,
+//   I[t, s] = kscale[s] * sum_h (w'[t,h] * qscale[t,h]) * max(acc[s,(t,h)], 0),
+// so the query scales fold into the head weights and the key scale is one
+// product after the head sum.  A quantisation kernel (one warp per row,
+// absolute maximum by shuffles, scale = amax / 448, codes = satfinite e4m3
+// of x * (448 / amax) rounded to nearest) makes the codes from bf16 rows.
 #include <cuda.h>
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -39,15 +50,23 @@ constexpr int kHi = 64, kDi = 128;
 constexpr int kQG = 4;                                // queries per group
 constexpr int kThreads = 320;
 constexpr int kEpiThreads = 256;
-constexpr int kStages = 3;
-constexpr uint32_t kABlock = 128 * 128;               // 128 entries x 64 dims x 2 B
-constexpr uint32_t kAStage = 2 * kABlock;             // both K-blocks of a tile
-constexpr uint32_t kBBlock = 256 * 128;               // 256 rows x 64 dims x 2 B
-constexpr uint32_t OFF_B = 0;                         // 2 buffers x 2 K-blocks: 131072
-constexpr uint32_t OFF_A = 4 * kBBlock;               // stages: 3 x 32768
-constexpr uint32_t OFF_W = OFF_A + kStages * kAStage; // 229376: w' [2][4][64] fp32
-constexpr uint32_t OFF_CTL = OFF_W + 2 * kQG * kHi * 4;   // 231424
+constexpr uint32_t kABlock = 128 * 128;               // 128 entries x 128 bytes (64 bf16 / 128 e4m3 dims)
+constexpr uint32_t kBBlock = 256 * 128;               // 256 query rows x 128 bytes
 
+// Shared-memory plan of one variant: two query-row buffers, the entry-tile
+// ring, the scaled head weights and the barriers.
+template <bool kE4M3>
+struct Shape {
+  static constexpr int kKB = kE4M3 ? 1 : 2;           // 128-byte K-blocks per row (Di = 128)
+  static constexpr int kStages = kE4M3 ? 8 : 3;
+  static constexpr uint32_t kAStage = kKB * kABlock;
+  static constexpr uint32_t OFF_B = 0;
+  static constexpr uint32_t OFF_A = 2 * kKB * kBBlock;
+  static constexpr uint32_t OFF_W = OFF_A + kStages * kAStage;   // w' [2][4][64] fp32
+  static constexpr uint32_t OFF_CTL = OFF_W + 2 * kQG * kHi * 4;
+};
+
+template <int kStages>
 struct Ctl {
   uint64_t a_full[kStages], a_empty[kStages];
   uint64_t b_full[2], b_empty[2];
@@ -56,16 +75,32 @@ struct Ctl {
   uint32_t tmem_base;
   int abort;
 };
-constexpr uint32_t kSmemBytes = OFF_CTL + sizeof(Ctl);
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+template <bool kE4M3>
+constexpr uint32_t smem_bytes() {
+  return Shape<kE4M3>::OFF_CTL + sizeof(Ctl<Shape<kE4M3>::kStages>);
+}
+static_assert(smem_bytes<false>() <= 232448 && smem_bytes<true>() <= 232448, "shared memory budget");
 
 struct Params {
   const float* w;          // [B,S,64] unscaled weights
+  const float* qscale;     // [B,S,64] query-row scales (E4M3 only)
+  const float* kscale;     // [B,N] key-row scales (E4M3 only)
   float* scores;           // [B,S,N]
   int* status;
   int B, S, N, ratio;
   float wscale;
 };
+
+// (a0, a1) += (w0 * max(x0, 0), w1 * max(x1, 0)): one paired fp32 FMA
+// (fma.rn.f32x2, two round-to-nearest FMAs) after the two ReLUs.
+__device__ __forceinline__ void fma2_relu(float& a0, float& a1, float w0, float w1, float x0, float x1) {
+  const float r0 = fmaxf(x0, 0.f), r1 = fmaxf(x1, 0.f);
+  asm("{\n\t.reg .b64 wv, rv, av;\n\t"
+      "mov.b64 wv, {%2, %3};\n\tmov.b64 rv, {%4, %5};\n\tmov.b64 av, {%0, %1};\n\t"
+      "fma.rn.f32x2 av, wv, rv, av;\n\tmov.b64 {%0, %1}, av;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(w0), "f"(w1), "f"(r0), "f"(r1));
+}
 
 __device__ __forceinline__ void group_of(int gi, const Params& p, int groups_per_b, int& b, int& t0,
                                          int& tiles) {
@@ -77,12 +112,17 @@ __device__ __forceinline__ void group_of(int gi, const Params& p, int groups_per
   tiles = (nv + 127) / 128;
 }
 
+template <bool kE4M3>
 __global__ void __launch_bounds__(kThreads, 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const Params p) {
+  using Sh = Shape<kE4M3>;
+  constexpr int kStages = Sh::kStages, kKB = Sh::kKB;
+  constexpr uint32_t kAStage = Sh::kAStage, OFF_A = Sh::OFF_A, OFF_B = Sh::OFF_B;
+  constexpr int kXStep = kE4M3 ? 128 : 64;              // elements per 128-byte K-block
   extern __shared__ __align__(1024) uint8_t smem[];
-  Ctl* c = reinterpret_cast<Ctl*>(smem + OFF_CTL);
-  float* s_w = reinterpret_cast<float*>(smem + OFF_W);
+  Ctl<kStages>* c = reinterpret_cast<Ctl<kStages>*>(smem + Sh::OFF_CTL);
+  float* s_w = reinterpret_cast<float*>(smem + Sh::OFF_W);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if ((smem_u32(smem) & 1023u) != 0) {
     if (threadIdx.x == 0) set_status(p.status, V4_ERR_UNSUPPORTED);
@@ -123,16 +163,16 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         const int bb = gq & 1;
         if (gq >= 2) ok = mbar_wait(&c->b_empty[bb], ((gq >> 1) - 1) & 1, &c->abort, p.status);
         if (!ok) break;
-        mbar_expect_tx(&c->b_full[bb], 2 * kBBlock);
-        for (int kb = 0; kb < 2; ++kb)
-          tma_load_2d(smem + OFF_B + (2 * bb + kb) * kBBlock, &map_q, 64 * kb, (b * p.S + t0) * kHi,
+        mbar_expect_tx(&c->b_full[bb], kKB * kBBlock);
+        for (int kb = 0; kb < kKB; ++kb)
+          tma_load_2d(smem + OFF_B + (kKB * bb + kb) * kBBlock, &map_q, kXStep * kb, (b * p.S + t0) * kHi,
                       &c->b_full[bb]);
         for (int j = 0; j < tiles && ok; ++j) {
           if (use >= kStages) ok = mbar_wait(&c->a_empty[st], ((use / kStages) - 1) & 1, &c->abort, p.status);
           if (!ok) break;
           mbar_expect_tx(&c->a_full[st], kAStage);
-          for (int kb = 0; kb < 2; ++kb)
-            tma_load_2d(smem + OFF_A + st * kAStage + kb * kABlock, &map_k, 64 * kb, b * p.N + 128 * j,
+          for (int kb = 0; kb < kKB; ++kb)
+            tma_load_2d(smem + OFF_A + st * kAStage + kb * kABlock, &map_k, kXStep * kb, b * p.N + 128 * j,
                         &c->a_full[st]);
           ++use;
           st = (st + 1) % kStages;
@@ -144,7 +184,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(128, 256, 0, 0);
+      const uint32_t idesc = kE4M3 ? idesc_e4m3_f32(128, 256) : idesc_bf16_f32(128, 256, 0, 0);
       const uint64_t dA0 = smem_desc(smem_u32(smem + OFF_A), 16, 1024, kLayoutSW128);
       const uint64_t dB0 = smem_desc(smem_u32(smem + OFF_B), 16, 1024, kLayoutSW128);
       int gq = 0, st = 0, use = 0, tile_ct = 0;
@@ -155,7 +195,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         if (tiles == 0) continue;
         const int bb = gq & 1;
         ok = mbar_wait(&c->b_full[bb], (gq >> 1) & 1, &c->abort, p.status);
-        const uint64_t dB = dB0 + (uint64_t)((2 * bb * kBBlock) >> 4);
+        const uint64_t dB = dB0 + (uint64_t)((kKB * bb * kBBlock) >> 4);
         for (int j = 0; j < tiles && ok; ++j) {
           const int ab = tile_ct & 1;
           ok = mbar_wait(&c->a_full[st], (use / kStages) & 1, &c->abort, p.status);
@@ -165,11 +205,16 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           const uint32_t d = tmem + 256 * ab;
           const uint64_t dA = dA0 + (uint64_t)((st * kAStage) >> 4);
 #pragma unroll
-          for (int kb = 0; kb < 2; ++kb) {
+          for (int kb = 0; kb < kKB; ++kb) {
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              umma_f16_ss(d, dA + (uint64_t)((kb * kABlock + 32 * ks) >> 4),
-                          dB + (uint64_t)((kb * kBBlock + 32 * ks) >> 4), idesc, (kb | ks) != 0);
+            for (int ks = 0; ks < 4; ++ks) {           // 32 bytes of K per instruction
+              const uint64_t da = dA + (uint64_t)((kb * kABlock + 32 * ks) >> 4);
+              const uint64_t db = dB + (uint64_t)((kb * kBBlock + 32 * ks) >> 4);
+              if constexpr (kE4M3)
+                umma_e4m3_ss(d, da, db, idesc, (kb | ks) != 0);
+              else
+                umma_f16_ss(d, da, db, idesc, (kb | ks) != 0);
+            }
           }
           umma_commit(&c->a_empty[st]);
           umma_commit(&c->acc_full[ab]);
@@ -199,7 +244,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       if (g >= total) return 0.f;
       group_of(g, p, groups_per_b, bg, tg, tl);
       const int t = tg + ts / kHi;
-      return t < p.S ? p.w[((size_t)bg * p.S + t) * kHi + (ts % kHi)] * p.wscale : 0.f;
+      if (t >= p.S) return 0.f;
+      const size_t wi = ((size_t)bg * p.S + t) * kHi + (ts % kHi);
+      if constexpr (kE4M3)
+        return p.w[wi] * p.wscale * p.qscale[wi];
+      else
+        return p.w[wi] * p.wscale;
     };
     pf_w = fetch_w(blockIdx.x);
     pf_gi = blockIdx.x;
@@ -218,27 +268,34 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       pf_gi = gi + gridDim.x;
       for (int j = 0; j < tiles; ++j) {
         const int ab = tile_ct & 1;
+        const int s = 128 * j + krow;
+        float ksc = 1.f;                         // key-row scale, loaded before the wait
+        if constexpr (kE4M3) ksc = s < p.N ? p.kscale[(size_t)b * p.N + s] : 0.f;
         mbar_wait(&c->acc_full[ab], (tile_ct >> 1) & 1, &c->abort, p.status);
         tc_fence_after();
-        const int s = 128 * j + krow;
         float sc[2];
 #pragma unroll
         for (int qq = 0; qq < 2; ++qq) {
           const int q = q0 + qq;
           const float* wq = sw + q * kHi;
-          float acc = 0.f;
+          // both halves of the query's 64 heads in one wait; four partial
+          // sums (heads h mod 4), two of them per paired fp32 FMA
+          float v[64];
+          tmem_ld32(tmem + lane_base + 256 * ab + 64 * q, v);
+          tmem_ld32(tmem + lane_base + 256 * ab + 64 * q + 32, v + 32);
+          tmem_wait_ld();
+          float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {       // heads in order 0..63
-            float v[32];
-            tmem_ld32(tmem + lane_base + 256 * ab + 64 * q + 32 * half, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int h = 0; h < 32; ++h) acc = fmaf(wq[32 * half + h], fmaxf(v[h], 0.f), acc);
-          }
-          sc[qq] = acc;
+          for (int h = 0; h < kHi; h += 2)
+            fma2_relu(a[h & 3], a[(h & 3) + 1], wq[h], wq[h + 1], v[h], v[h + 1]);
+          sc[qq] = (a[0] + a[1]) + (a[2] + a[3]);
         }
         tc_fence_before();
         mbar_arrive(&c->acc_empty[ab]);
+        if constexpr (kE4M3) {
+          sc[0] *= ksc;
+          sc[1] *= ksc;
+        }
 #pragma unroll
         for (int qq = 0; qq < 2; ++qq) {
           const int t = t0 + q0 + qq;
@@ -264,6 +321,40 @@ bool indexer_tc_supported(const v4_config& c) {
   return c.dtype == V4_BF16 && c.idx_heads == kHi && c.idx_dim == kDi && c.ratio >= 1;
 }
 
+bool indexer_e4m3_supported(const v4_config& c) { return indexer_tc_supported(c); }
+
+template <bool kE4M3>
+static cudaError_t launch_scores(const v4_config& cfg, const CUtensorMap& mq, const CUtensorMap& mk,
+                                 const Params& prm, cudaStream_t st) {
+  const uint32_t bytes = smem_bytes<kE4M3>();
+  cudaError_t err = cudaFuncSetAttribute(indexer_tc_kernel<kE4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)bytes);
+  if (err != cudaSuccess) return err;
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int total = cfg.batch * ((cfg.seqlen + kQG - 1) / kQG);
+  const int grid = total < sms ? total : sms;
+  indexer_tc_kernel<kE4M3><<<grid, kThreads, bytes, st>>>(mq, mk, prm);
+  note_launch();
+  return cudaGetLastError();
+}
+
+static Params make_params(const v4_config& cfg, const float* w, float* scores, int* status) {
+  Params prm;
+  prm.w = w;
+  prm.qscale = nullptr;
+  prm.kscale = nullptr;
+  prm.scores = scores;
+  prm.status = status;
+  prm.B = cfg.batch;
+  prm.S = cfg.seqlen;
+  prm.N = cfg.seqlen / cfg.ratio;
+  prm.ratio = cfg.ratio;
+  prm.wscale = 1.0f / sqrtf((float)kHi) / sqrtf((float)kDi);
+  return prm;
+}
+
 cudaError_t launch_indexer_scores_tc(const v4_config& cfg, const void* iqp, const void* ikey, const float* w,
                                      float* scores, int* status, cudaStream_t st) {
   const int B = cfg.batch, S = cfg.seqlen;
@@ -274,24 +365,85 @@ cudaError_t launch_indexer_scores_tc(const v4_config& cfg, const void* iqp, cons
   e |= make_tmap_bf16_2d(&mq, iqp, kDi, (uint64_t)B * S * kHi, 64, 256, true);
   e |= make_tmap_bf16_2d(&mk, ikey, kDi, (uint64_t)B * N, 64, 128, true);
   if (e) return cudaErrorInvalidValue;
-  Params prm;
-  prm.w = w;
-  prm.scores = scores;
-  prm.status = status;
-  prm.B = B;
-  prm.S = S;
-  prm.N = N;
-  prm.ratio = cfg.ratio;
-  prm.wscale = 1.0f / sqrtf((float)kHi) / sqrtf((float)kDi);
-  cudaError_t err = cudaFuncSetAttribute(indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-  if (err != cudaSuccess) return err;
+  return launch_scores<false>(cfg, mq, mk, make_params(cfg, w, scores, status), st);
+}
+
+cudaError_t launch_indexer_scores_e4m3(const v4_config& cfg, const uint8_t* qc, const float* qs, const uint8_t* kc,
+                                       const float* ks, const float* w, float* scores, int* status,
+                                       cudaStream_t st) {
+  const int B = cfg.batch, S = cfg.seqlen;
+  const int N = S / cfg.ratio;
+  if (N == 0) return cudaSuccess;
+  CUtensorMap mq, mk;
+  int e = 0;
+  e |= make_tmap_u8_2d(&mq, qc, kDi, (uint64_t)B * S * kHi, 128, 256, true);
+  e |= make_tmap_u8_2d(&mk, kc, kDi, (uint64_t)B * N, 128, 128, true);
+  if (e) return cudaErrorInvalidValue;
+  Params prm = make_params(cfg, w, scores, status);
+  prm.qscale = qs;
+  prm.kscale = ks;
+  return launch_scores<true>(cfg, mq, mk, prm, st);
+}
+
+// ---------------------------------------------------------------------------
+// E4M3 quantisation of bf16 rows: one warp per row, lane l holds the 4-value
+// chunks l, l + 32, ... (dim / 128 of them); absolute maximum by shuffles.
+// ---------------------------------------------------------------------------
+template <int kChunks>
+__global__ void __launch_bounds__(256)
+quant_e4m3_kernel(const bf16* __restrict__ x, long long rows, uint8_t* __restrict__ codes,
+                  float* __restrict__ scales) {
+  constexpr int dim = 128 * kChunks;
+  const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+  const int lane = threadIdx.x & 31;
+  for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
+    const bf16* xr = x + r * dim;
+    float v[4 * kChunks];
+    float amax = 0.f;
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      const uint2 u = *reinterpret_cast<const uint2*>(xr + 4 * (32 * c + lane));
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+      const float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]);
+      v[4 * c] = a.x;
+      v[4 * c + 1] = a.y;
+      v[4 * c + 2] = b.x;
+      v[4 * c + 3] = b.y;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(v[4 * c + i]));
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float inv = amax > 0.f ? 448.0f / amax : 0.f;
+    if (lane == 0) scales[r] = amax > 0.f ? amax / 448.0f : 0.f;
+    uint8_t* cr = codes + r * dim;
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      const __nv_fp8x2_storage_t lo =
+          __nv_cvt_float2_to_fp8x2(make_float2(v[4 * c] * inv, v[4 * c + 1] * inv), __NV_SATFINITE, __NV_E4M3);
+      const __nv_fp8x2_storage_t hi =
+          __nv_cvt_float2_to_fp8x2(make_float2(v[4 * c + 2] * inv, v[4 * c + 3] * inv), __NV_SATFINITE, __NV_E4M3);
+      *reinterpret_cast<uint32_t*>(cr + 4 * (32 * c + lane)) = (uint32_t)lo | ((uint32_t)hi << 16);
+    }
+  }
+}
+
+cudaError_t launch_quant_e4m3(const void* x, long long rows, int dim, uint8_t* codes, float* scales,
+                              cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
   int sms = 0, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int total = B * ((S + kQG - 1) / kQG);
-  const int grid = total < sms ? total : sms;
-  indexer_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mq, mk, prm);
+  const long long want = (rows + 7) / 8;
+  const int grid = (int)(want < 8LL * sms ? want : 8LL * sms);
+  const bf16* xb = (const bf16*)x;
+  switch (dim / 128) {
+    case 1: quant_e4m3_kernel<1><<<grid, 256, 0, st>>>(xb, rows, codes, scales); break;
+    case 2: quant_e4m3_kernel<2><<<grid, 256, 0, st>>>(xb, rows, codes, scales); break;
+    case 4: quant_e4m3_kernel<4><<<grid, 256, 0, st>>>(xb, rows, codes, scales); break;
+    case 8: quant_e4m3_kernel<8><<<grid, 256, 0, st>>>(xb, rows, codes, scales); break;
+    default: return cudaErrorInvalidValue;
+  }
   note_launch();
   return cudaGetLastError();
 }

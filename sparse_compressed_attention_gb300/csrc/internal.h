@@ -30,6 +30,10 @@ struct Workspace {
   size_t knorm = 0, knorm_bytes = 0;       // key-row norms [B*S + B*N] (tensor-core attention)
   size_t counters = 0, counters_bytes = 0; // work counter, redo count, redo list [2 + B*S]
   size_t rope = 0, rope_bytes = 0;         // cos/sin table [S][R/2] float2
+  size_t qc8 = 0, qc8_bytes = 0;           // E4M3 indexer: query codes [B,S,Hi,Di] u8
+  size_t qs8 = 0, qs8_bytes = 0;           //   query scales [B,S,Hi] fp32
+  size_t kc8 = 0, kc8_bytes = 0;           //   key codes [B,N,Di] u8
+  size_t ks8 = 0, ks8_bytes = 0;           //   key scales [B,N] fp32
   size_t total = 0;
 };
 Workspace plan_workspace(const v4_config& c);
@@ -61,6 +65,8 @@ cudaError_t launch_rope_table(const v4_config& c, const float* inv_freq, float2*
 // ---- TMA descriptors (tma_host.cu); returns 0 on success
 int make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
                       uint32_t box_rows, bool swizzle128);
+int make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                    uint32_t box_rows, bool swizzle128);
 // cs_table may be null (angles are then computed in the kernel from inv_freq)
 cudaError_t launch_indexer_prep(const v4_config& c, const void* iq, const float2* cs_table,
                                 const float* inv_freq, void* iqp, cudaStream_t st);
@@ -71,6 +77,16 @@ cudaError_t launch_indexer_scores_simt(const v4_config& c, const void* iqp, cons
 bool indexer_tc_supported(const v4_config& c);
 cudaError_t launch_indexer_scores_tc(const v4_config& c, const void* iqp, const void* ikey, const float* w,
                                      float* scores, int* status, cudaStream_t st);
+// Opt-in E4M3 indexer (indexer_tc.cu): per-row absmax quantisation of bf16
+// rows (dim a multiple of 128, <= 1024) and the scores of quantised
+// operands (Hi = 64, Di = 128): q codes [B,S,64,128] with scales [B,S,64],
+// key codes [B,N,128] with scales [B,N].
+cudaError_t launch_quant_e4m3(const void* x, long long rows, int dim, uint8_t* codes, float* scales,
+                              cudaStream_t st);
+bool indexer_e4m3_supported(const v4_config& c);
+cudaError_t launch_indexer_scores_e4m3(const v4_config& c, const uint8_t* qc, const float* qs, const uint8_t* kc,
+                                       const float* ks, const float* w, float* scores, int* status,
+                                       cudaStream_t st);
 cudaError_t launch_topk(const v4_config& c, const float* scores, int32_t* idx, float* iscore,
                         cudaStream_t st);
 

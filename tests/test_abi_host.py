@@ -67,7 +67,8 @@ def _status(fn, *args):
 @pytest.mark.parametrize("field,value,msg", [
     ("head_dim", 40, "head_dim"), ("rope_dim", 12, "rope_dim"), ("ratio", -1, "ratio"),
     ("overlap", 2, "overlap"), ("window", -2, "window"), ("topk", -1, "topk"),
-    ("idx_dim", 96, "idx_dim"), ("dtype", 7, "dtype"), ("batch", 0, "batch")])
+    ("idx_dim", 96, "idx_dim"), ("dtype", 7, "dtype"), ("batch", 0, "batch"),
+    ("indexer_fp8", 2, "indexer_fp8")])
 def test_invalid_config_is_rejected_on_host(lib, field, value, msg):
     cfg = L.config_from_preset(SI.preset("csa_bf16_4k"))
     setattr(cfg, field, value)
@@ -97,6 +98,30 @@ def test_topk_without_ratio_is_rejected(lib):
     cfg = L.make_config(1, 64, 4, 64, 16, ratio=0, topk=8, Hi=2, Di=32)
     st = lib.v4_indexer_topk(C.byref(cfg), 16, 0, 16, 16, 16, 16, None, 256, 1 << 20, None)
     assert st == L.V4_ERR_INVALID_ARG and "ratio" in lib.v4_last_error().decode()
+
+
+def test_e4m3_indexer_host_checks(lib):
+    # workspace grows by the codes and scales of both operands
+    p = SI.preset("csa_bf16_4k")
+    n0 = L.v4_workspace_size(L.config_from_preset(p))
+    n1 = L.v4_workspace_size(L.config_from_preset(p, indexer_fp8=1))
+    S, N = p["S"], p["S"] // p["ratio"]
+    assert n1 >= n0 + S * 64 * 128 + S * 64 * 4 + N * 128 + N * 4
+    # shapes outside the tensor-core indexer are refused before any launch
+    cfg = L.config_from_preset(SI.preset("tiny_csa_f32"), indexer_fp8=1)
+    st = lib.v4_indexer_topk_e4m3(C.byref(cfg), 16, 16, 16, 16, 16, 16, None, 256, 1 << 20, None)
+    assert st == L.V4_ERR_UNSUPPORTED and "E4M3" in lib.v4_last_error().decode()
+    st = lib.v4_indexer_topk(C.byref(cfg), 16, 0, 16, 16, 16, 16, None, 256, 1 << 20, None)
+    assert st == L.V4_ERR_UNSUPPORTED and "E4M3" in lib.v4_last_error().decode()
+    cfg = L.config_from_preset(p, indexer_fp8=1, path=L.V4_PATH_SIMT)
+    st = lib.v4_indexer_topk(C.byref(cfg), 16, 0, 16, 16, 16, 16, None, 256, 1 << 30, None)
+    assert st == L.V4_ERR_UNSUPPORTED
+    # the quantiser's own argument checks
+    st = lib.v4_quantize_e4m3(16, 4, 100, 16, 16, None)
+    assert st == L.V4_ERR_INVALID_ARG and "dim" in lib.v4_last_error().decode()
+    st = lib.v4_quantize_e4m3(None, 4, 128, 16, 16, None)
+    assert st == L.V4_ERR_INVALID_ARG and "x" in lib.v4_last_error().decode()
+    assert lib.v4_quantize_e4m3(None, 0, 128, None, None, None) == L.V4_OK
 
 
 def test_error_text_is_per_thread(lib):
