@@ -586,6 +586,36 @@ def grouped_wo_a(o, wo_a, store_bf16=False):
 
 
 # ---------------------------------------------------------------------------
+# Query projections  ([BLOG] "The DeepSeek-V4-Flash architecture": queries
+# arrive through a low-rank path of rank 1024 that the indexer shares)
+# ---------------------------------------------------------------------------
+def q_projection(qlat, wq, n_heads, head_dim, norm=True, eps=0.0, norm_w=None, store_bf16=False):
+    """Attention queries from the shared rank-r latent.
+
+    qlat [B,T,r], wq [r, H*D]; y = qlat @ wq viewed as [B,T,H,D].  With
+    ``norm`` every head is RMS-normalised over its D dims (the reading the
+    benchmark inputs use: unit-RMS heads), y / sqrt(mean(y^2) + eps) * g,
+    g = norm_w [D] or ones.  Returns [B,T,H,D].
+    """
+    qlat = np.asarray(qlat, dtype=F64)
+    B, T, r = qlat.shape
+    y = (qlat.reshape(B * T, r) @ np.asarray(wq, dtype=F64)).reshape(B, T, n_heads, head_dim)
+    if norm:
+        y = y / np.sqrt(np.mean(y * y, axis=-1, keepdims=True) + eps)
+        if norm_w is not None:
+            y = y * np.asarray(norm_w, dtype=F64)
+    return maybe_bf16(y, store_bf16)
+
+
+def indexer_q_projection(qlat, wiq, idx_heads, idx_dim, store_bf16=False):
+    """Indexer queries from the same latent: qlat @ wiq viewed as [B,T,Hi,Di]."""
+    qlat = np.asarray(qlat, dtype=F64)
+    B, T, r = qlat.shape
+    y = (qlat.reshape(B * T, r) @ np.asarray(wiq, dtype=F64)).reshape(B, T, idx_heads, idx_dim)
+    return maybe_bf16(y, store_bf16)
+
+
+# ---------------------------------------------------------------------------
 # One attention layer
 # ---------------------------------------------------------------------------
 def attn_layer(cfg, x, rows=None):

@@ -105,6 +105,24 @@ def _quant_tensor_scale(x):
     return codes, np.full(x.shape[:-1], s)
 
 
+_qproj = O.q_projection
+
+
+def _qproj_whole_row_norm(qlat, wq, n_heads, head_dim, norm=True, eps=0.0, norm_w=None, store_bf16=False):
+    y = _qproj(qlat, wq, n_heads, head_dim, norm=False)
+    B, T = y.shape[:2]
+    f = y.reshape(B, T, -1)
+    f = f / np.sqrt(np.mean(f * f, axis=-1, keepdims=True) + eps)
+    return f.reshape(y.shape)
+
+
+def _qproj_transposed_weight(qlat, wq, n_heads, head_dim, norm=True, eps=0.0, norm_w=None, store_bf16=False):
+    # the [r][H*D] weight read as if it were stored [H*D][r]
+    r = np.asarray(qlat).shape[-1]
+    w = np.asarray(wq).reshape(n_heads * head_dim, r).T
+    return _qproj(qlat, w, n_heads, head_dim, norm, eps, norm_w, store_bf16)
+
+
 MUTATIONS = [
     ("rope_rotate", _flip_sign, P.test_rope_is_complex_multiplication),
     ("sparse_mqa", _inflated_scale, P.test_softmax_scale_is_head_dim_power),
@@ -118,6 +136,8 @@ MUTATIONS = [
     ("round_to_e4m3", _e4m3_no_saturation, F.test_e4m3_saturates),
     ("quantize_e4m3_rows", _quant_inverted_scale, F.test_quantizer_error_within_half_spacing),
     ("quantize_e4m3_rows", _quant_tensor_scale, F.test_quantizer_row_maximum_lands_on_448),
+    ("q_projection", _qproj_whole_row_norm, P.test_q_projection_heads_have_unit_rms_and_ignore_scale),
+    ("q_projection", _qproj_transposed_weight, P.test_q_projection_matches_explicit_sums),
 ]
 
 

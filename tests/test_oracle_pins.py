@@ -481,3 +481,45 @@ def test_flash_layer_mix():
     assert len(ratios) == g["decoder_layers"]
     assert ratios.count(0) == g["swa"] and ratios.count(4) == g["csa"] and ratios.count(128) == g["hca"]
     assert ratios[-1] == 4 and ratios[:2] == [0, 0]
+
+
+# ---------------------------------------------------------------------------
+# Query projections from the shared rank-r latent
+# ---------------------------------------------------------------------------
+def _qproj_case(seed=0, B=2, T=5, r=16, H=3, D=8):
+    rng = np.random.default_rng(seed)
+    return rng.normal(0, 1, (B, T, r)), rng.normal(0, 0.3, (r, H * D)), H, D
+
+
+def test_q_projection_matches_explicit_sums():
+    qlat, wq, H, D = _qproj_case()
+    y = O.q_projection(qlat, wq, H, D, norm=False)
+    for (b, t, h, d) in ((0, 0, 0, 0), (1, 4, 2, 7), (0, 3, 1, 5)):
+        ref = sum(qlat[b, t, k] * wq[k, h * D + d] for k in range(qlat.shape[-1]))
+        assert abs(y[b, t, h, d] - ref) < 1e-12
+    g = np.random.default_rng(1).normal(0, 1, D)
+    yn = O.q_projection(qlat, wq, H, D, norm=True, eps=1e-6, norm_w=g)
+    for (b, t, h) in ((0, 0, 0), (1, 4, 2)):
+        v = y[b, t, h]
+        ref = v / math.sqrt(sum(x * x for x in v) / D + 1e-6) * g
+        np.testing.assert_allclose(yn[b, t, h], ref, rtol=1e-12, atol=1e-14)
+
+
+def test_q_projection_heads_have_unit_rms_and_ignore_scale():
+    qlat, wq, H, D = _qproj_case(2)
+    y = O.q_projection(qlat, wq, H, D, norm=True)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=-1)), 1.0, rtol=1e-12)
+    # each head is normalised on its own: scaling one head's weight columns
+    # leaves every head unchanged
+    w2 = wq.copy()
+    w2[:, D:2 * D] *= 7.0
+    np.testing.assert_allclose(O.q_projection(qlat, w2, H, D, norm=True), y, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(O.q_projection(3.0 * qlat, wq, H, D, norm=True), y, rtol=1e-12, atol=1e-14)
+
+
+def test_indexer_q_projection_shares_the_latent():
+    qlat, _, _, _ = _qproj_case(3)
+    wiq = np.random.default_rng(4).normal(0, 0.3, (qlat.shape[-1], 2 * 4))
+    y = O.indexer_q_projection(qlat, wiq, 2, 4)
+    np.testing.assert_allclose(y.reshape(2, 5, 8), np.einsum("btk,kn->btn", qlat, wiq), rtol=1e-12)
+    assert y.shape == (2, 5, 2, 4)
