@@ -468,6 +468,60 @@ def make_stack_layer(kind, B, S, device, seed):
     return dict(name=kind, p=p, x=x, outs=outs, cfg=cfg, ws=V.alloc_workspace(cfg, device))
 
 
+def run_qproj(args):
+    """--workload qproj: the query projections of the rank-1024 latent (q with
+    per-head RMSNorm, and the indexer queries) for B=1, S tokens."""
+    import torch
+
+    import seeded_inputs as SI
+    import sparse_compressed_attention_gb300 as V
+    from sparse_compressed_attention_gb300 import build as Bld
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    Bld.build()
+    V.lib()
+    S = args.seq
+    p = SI.preset("csa_bf16_16k", S=S)
+    H, D, Hi, Di, rank = p["H"], p["D"], p["Hi"], p["Di"], SI.Q_RANK
+    g = torch.Generator(device=dev).manual_seed(5000)
+    qlat = torch.randn(1, S, rank, generator=g, device=dev).to(torch.bfloat16)
+    wq = (torch.randn(rank, H * D, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    wiq = (torch.randn(rank, Hi * Di, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    q = torch.empty(1, S, H, D, dtype=torch.bfloat16, device=dev)
+    iq = torch.empty(1, S, Hi, Di, dtype=torch.bfloat16, device=dev)
+    cfg = V.config_from_preset(p)
+    for _ in range(args.warmup):
+        V.v4_q_proj(cfg, qlat, wq, q, 1, None, wiq, iq)
+    torch.cuda.synchronize(dev)
+    clk = ClockSampler(smi_index(0))
+    clk.start()
+    stream = torch.cuda.current_stream(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = V.v4_launch_count()
+    t0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        V.v4_q_proj(cfg, qlat, wq, q, 1, None, wiq, iq)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    clk.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    flops = 2.0 * S * rank * (H * D + Hi * Di)
+    tf = flops / (ms / 1e3) / 1e12
+    peaks = load_peaks()
+    line = {"metric": "query projection tokens/s at S=%d (rank-1024 latent -> 64x512 q, 64x128 iq)" % S,
+            "value": round(S / (ms / 1e3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) latent, N(0,0.02) weights)",
+            "config": {"workload": "q and indexer-q projections of the rank-1024 latent, per-head RMSNorm on q, "
+                                   "B=1, S=%d" % S, "global_batch": 1, "seq_len": S},
+            "clocks": clk.summary(t0, t1), "gpu_launches": V.v4_launch_count() - launches0,
+            "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16"], "unit": "TFLOP/s",
+                         "frac": round(tf / peaks["bf16"], 4), "traffic": None, "flops_per_launch": flops}}
+    print(json.dumps(line), flush=True)
+
+
 def run_workload(args):
     """--workload stack | csa: one JSON line for that workload (1 GPU)."""
     import torch
@@ -714,13 +768,15 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="time eager calls instead of a captured step")
     ap.add_argument("--indexer-fp8", type=int, choices=[0, 1], default=0,
                     help="--workload csa: opt-in E4M3 indexer QK (the default keeps bf16 operands)")
-    ap.add_argument("--workload", choices=["pair", "stack", "csa", "pro"], default="pair",
+    ap.add_argument("--workload", choices=["pair", "stack", "csa", "pro", "qproj"], default="pair",
                     help="pair: the CSA + HCA layer pair (the reported line); stack: the 43-layer "
                          "Flash stack with grouped wo_a at B=2; csa: one CSA layer (e.g. --seq 65536); "
-                         "pro: the pair with 128 heads and top-1024")
+                         "pro: the pair with 128 heads and top-1024; qproj: the rank-1024 query projections")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "qproj":
+        run_qproj(args)
     elif args.workload != "pair":
         run_workload(args)
     else:

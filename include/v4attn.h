@@ -288,6 +288,25 @@ v4_status v4_sparse_mqa_bwd(const v4_config* cfg, const void* q, const void* kv,
                             float* dsink, void* workspace, size_t ws_bytes, void* stream);
 
 /* ----------------------------------------------------------------------
+ * Query projections of the rank-r latent.  [BLOG] "The DeepSeek-V4-Flash
+ * architecture": queries arrive through a low-rank path of rank 1024 that
+ * the sparse-selection indexer shares.
+ *   qlat : [B, S, rank] bf16, the shared latent.
+ *   wq   : [rank, H*D] bf16 (row k holds the weights of latent dim k).
+ *   q    : [B, S, H, D] out: qlat . wq, and with q_norm = 1 every head
+ *          RMS-normalised over its D dims, q / sqrt(mean(q^2) + cfg->rms_eps)
+ *          * g with g = q_norm_w [D] fp32 (NULL = ones).
+ *   wiq  : [rank, Hi*Di] bf16, nullable; iq : [B, S, Hi, Di] out (required
+ *          iff wiq): qlat . wiq.
+ * bf16 storage only, fp32 accumulation, one rounding to bf16; rank a
+ * multiple of 64 (at most 65536), H*D and Hi*Di multiples of 256, and D =
+ * 512 when q_norm = 1; other shapes return V4_ERR_UNSUPPORTED.
+ * --------------------------------------------------------------------*/
+v4_status v4_q_proj(const v4_config* cfg, const void* qlat, int32_t rank, const void* wq,
+                    int32_t q_norm, const float* q_norm_w, const void* wiq, void* q, void* iq,
+                    void* stream);
+
+/* ----------------------------------------------------------------------
  * Grouped low-rank output projection.  [BLOG] "The DeepSeek-V4-Flash
  * architecture": the 64 x 512 output splits into o_groups groups, each
  * through an o_rank bottleneck.  Group g holds heads g*H/G .. (g+1)*H/G-1
@@ -359,7 +378,7 @@ uint64_t v4_launch_count(void);
  * prep, 3 indexer scores, 4 top-k, 5 attention, 6 output projection,
  * 7 backward prep (clears, tables, key rotation, query/gradient rotation and
  * delta), 8 attention backward, 9 window-gradient de-rotation, 10 E4M3
- * quantisation of the indexer operands.
+ * quantisation of the indexer operands, 11 query projections.
  * --------------------------------------------------------------------*/
 v4_status v4_profile_enable(int32_t on);
 int32_t v4_profile_count(void);

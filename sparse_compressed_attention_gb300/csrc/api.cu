@@ -64,7 +64,8 @@ static bool g_prof_on = false;
 static std::vector<ProfRec> g_prof;
 
 enum { K_COMPRESS = 0, K_ROTATE = 1, K_IDX_PREP = 2, K_IDX_SCORE = 3, K_TOPK = 4, K_ATTN = 5,
-       K_OPROJ = 6, K_BWD_PREP = 7, K_BWD_ATTN = 8, K_BWD_FIN = 9, K_IDX_QUANT = 10 };
+       K_OPROJ = 6, K_BWD_PREP = 7, K_BWD_ATTN = 8, K_BWD_FIN = 9, K_IDX_QUANT = 10,
+       K_QPROJ = 11 };
 
 struct ProfScope {
   bool on = false;
@@ -600,6 +601,37 @@ v4_status v4_grouped_o_proj(const v4_config* cfg, const void* o, const void* wo_
   REQ(wo_a, "wo_a");
   REQ(y, "y");
   return do_oproj(*cfg, o, wo_a, y, (cudaStream_t)stream);
+}
+
+v4_status v4_q_proj(const v4_config* cfg, const void* qlat, int32_t rank, const void* wq, int32_t q_norm,
+                    const float* q_norm_w, const void* wiq, void* q, void* iq, void* stream) {
+  v4_status s = check_cfg(cfg);
+  if (s != V4_OK) return s;
+  const v4_config& c = *cfg;
+  if (q_norm != 0 && q_norm != 1) return fail(V4_ERR_INVALID_ARG, "q_norm must be 0 or 1");
+  if (rank < 1) return fail(V4_ERR_INVALID_ARG, "rank must be >= 1");
+  const long long nq = (long long)c.n_heads * c.head_dim;
+  const long long ni = (long long)c.idx_heads * c.idx_dim;
+  if (c.dtype != V4_BF16 || rank % 64 || rank > 65536 || nq % 256 || (q_norm && c.head_dim != 512) ||
+      (wiq && (c.idx_heads < 1 || ni % 256)))
+    return fail(V4_ERR_UNSUPPORTED, "query projections need bf16, rank a multiple of 64, H*D and Hi*Di multiples "
+                                    "of 256, D = 512 with q_norm");
+  REQ(qlat, "qlat");
+  REQ(wq, "wq");
+  REQ(q, "q");
+  OPT(q_norm_w, "q_norm_w");
+  OPT(wiq, "wiq");
+  if (wiq) REQ(iq, "iq");
+  int* status = status_ptr();
+  if (!status) return fail(V4_ERR_CUDA, "device status word unavailable");
+  cudaStream_t st = (cudaStream_t)stream;
+  const long long T = (long long)c.batch * c.seqlen;
+  ProfScope ps(K_QPROJ, st);
+  CU(launch_qproj_tc(T, rank, qlat, wq, (int)nq, q, q_norm, c.rms_eps, q_norm ? q_norm_w : nullptr, status, st),
+     "query projection kernel");
+  if (wiq) CU(launch_qproj_tc(T, rank, qlat, wiq, (int)ni, iq, 0, 0.f, nullptr, status, st),
+              "indexer query projection kernel");
+  return V4_OK;
 }
 
 v4_status v4_attn_layer_fwd(const v4_config* cfg, const v4_layer_inputs* in, v4_layer_outputs* out,

@@ -103,6 +103,11 @@ bool mqa_tc_supported(const v4_config& c);
 bool oproj_tc_supported(const v4_config& c);
 cudaError_t launch_oproj_tc(const v4_config& c, const void* o, const void* wo_a, void* y, int* status,
                             cudaStream_t st);
+// Query projection y[T, N] = x[T, rank] . w[rank, N] (bf16, fp32 accumulate);
+// norm = 1 RMS-normalises every 512-wide column block (N % 512 == 0),
+// weight norm_w [512] or ones.  rank % 64 == 0, N % 256 == 0.
+cudaError_t launch_qproj_tc(long long T, int rank, const void* x, const void* w, int N, void* y, int norm,
+                            float eps, const float* norm_w, int* status, cudaStream_t st);
 cudaError_t launch_mqa_tc(const v4_config& c, const void* q, const void* kv_rot, const void* ent,
                           const int32_t* idx, const float* sink, const float2* cs_table,
                           const float* wmax, const float* emax, void* o, float* lse,

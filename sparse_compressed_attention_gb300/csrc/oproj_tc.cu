@@ -15,6 +15,13 @@
 // K=16) accumulate in TMEM, double-buffered (2 x 256 columns) so the
 // epilogue of one tile (one thread per token row: fp32 -> bf16, 16-byte
 // stores) overlaps the next tile's MMAs.  Persistent CTAs walk the tiles.
+//
+// The same kernel runs the query projections of the rank-1024 path (one
+// group: y = qlat . W).  With per-head normalisation a CTA takes the two
+// 256-column tiles of a 512-wide head back to back, into the two TMEM
+// buffers; the epilogue sums the squares of both halves, then scales and
+// stores them (y / sqrt(mean(y^2) + eps) * g), releasing each buffer as it
+// is written so the next head's first half can start.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -47,9 +54,19 @@ constexpr uint32_t kSmemBytes = OFF_CTL + sizeof(Ctl);
 
 struct Params {
   bf16* y;             // [T, G*N]
+  const float* norm_w; // [512] RMSNorm weight of a head (pair_norm), null = ones
   int* status;
   int T, G, N, Kg;     // tokens, groups, outputs per group, inputs per group
+  int pair_norm;       // 1: RMS-normalise each pair of consecutive 256-column tiles (a 512-wide head)
+  float eps;
 };
+
+// The k-th tile of this CTA (tiles in tile_of order).  With pair_norm the
+// CTA owns pairs: tiles 2i and 2i+1 hold the two halves of one head.
+__device__ __forceinline__ int my_tile(int k, const Params& p) {
+  if (p.pair_norm) return 2 * (blockIdx.x + (k >> 1) * gridDim.x) + (k & 1);
+  return blockIdx.x + k * gridDim.x;
+}
 
 __device__ __forceinline__ void tile_of(int tile, const Params& p, int& g, int& m0, int& n0) {
   const int nt = p.N / kBN;
@@ -96,7 +113,7 @@ oproj_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant
     if (lane == 0) {
       int use = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      for (int k = 0, tile = my_tile(0, p); tile < tiles && ok; tile = my_tile(++k, p)) {
         int g, m0, n0;
         tile_of(tile, p, g, m0, n0);
         for (int kb = 0; kb < kblocks; ++kb) {
@@ -121,7 +138,7 @@ oproj_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant
       const uint64_t dB0 = smem_desc(smem_u32(smem + kABytes), kBBlock, 1024, kLayoutSW128);
       int use = 0, tc = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      for (int k = 0, tile = my_tile(0, p); tile < tiles && ok; tile = my_tile(++k, p)) {
         const int ab = tc & 1;
         if (tc >= 2) ok = mbar_wait(&c->acc_empty[ab], ((tc >> 1) - 1) & 1, &c->abort, p.status);
         tc_fence_after();
@@ -151,27 +168,73 @@ oproj_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant
     const int row = 32 * quarter + lane;
     const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
     int tc = 0;
-    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-      int g, m0, n0;
-      tile_of(tile, p, g, m0, n0);
-      const int ab = tc & 1;
-      mbar_wait(&c->acc_full[ab], (tc >> 1) & 1, &c->abort, p.status);
-      tc_fence_after();
-      const int t = m0 + row;
-      bf16* yrow = p.y + (size_t)t * p.G * p.N + (size_t)g * p.N + n0;
+    if (!p.pair_norm) {
+      for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        int g, m0, n0;
+        tile_of(tile, p, g, m0, n0);
+        const int ab = tc & 1;
+        mbar_wait(&c->acc_full[ab], (tc >> 1) & 1, &c->abort, p.status);
+        tc_fence_after();
+        const int t = m0 + row;
+        bf16* yrow = p.y + (size_t)t * p.G * p.N + (size_t)g * p.N + n0;
 #pragma unroll 1
-      for (int cb = 0; cb < kBN / 32; ++cb) {
-        float v[32];
-        tmem_ld32(tmem + lane_base + 256 * ab + 32 * cb, v);
-        tmem_wait_ld();
-        if (t < p.T) {
+        for (int cb = 0; cb < kBN / 32; ++cb) {
+          float v[32];
+          tmem_ld32(tmem + lane_base + 256 * ab + 32 * cb, v);
+          tmem_wait_ld();
+          if (t < p.T) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) store8(yrow + 32 * cb + 8 * q, v + 8 * q);
+            for (int q = 0; q < 4; ++q) store8(yrow + 32 * cb + 8 * q, v + 8 * q);
+          }
         }
+        tc_fence_before();
+        mbar_arrive(&c->acc_empty[ab]);
+        ++tc;
       }
-      tc_fence_before();
-      mbar_arrive(&c->acc_empty[ab]);
-      ++tc;
+    } else {
+      // one 512-wide head per pair: halves in buffers 0 and 1
+      for (int k = 0, tile = my_tile(0, p); tile < tiles; k += 2, tile = my_tile(k, p)) {
+        int g, m0, n0;
+        tile_of(tile, p, g, m0, n0);
+        const uint32_t ph = (tc >> 1) & 1;
+        float ss[4] = {0.f, 0.f, 0.f, 0.f};
+        // squares of the first half while the second half's products run
+#pragma unroll 1
+        for (int ab = 0; ab < 2; ++ab) {
+          mbar_wait(&c->acc_full[ab], ph, &c->abort, p.status);
+          tc_fence_after();
+#pragma unroll 1
+          for (int cb = 0; cb < kBN / 32; ++cb) {
+            float v[32];
+            tmem_ld32(tmem + lane_base + 256 * ab + 32 * cb, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ss[i & 3] = fmaf(v[i], v[i], ss[i & 3]);
+          }
+        }
+        const float rs = 1.0f / sqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) / (float)(2 * kBN) + p.eps);
+        const int t = m0 + row;
+        bf16* yrow = p.y + (size_t)t * p.G * p.N + (size_t)g * p.N + n0;
+#pragma unroll 1
+        for (int ab = 0; ab < 2; ++ab) {
+#pragma unroll 1
+          for (int cb = 0; cb < kBN / 32; ++cb) {
+            float v[32];
+            tmem_ld32(tmem + lane_base + 256 * ab + 32 * cb, v);
+            tmem_wait_ld();
+            const int c0 = kBN * ab + 32 * cb;            // column within the head
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= p.norm_w ? rs * p.norm_w[c0 + i] : rs;
+            if (t < p.T) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) store8(yrow + c0 + 8 * q, v + 8 * q);
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(&c->acc_empty[ab]);
+        }
+        tc += 2;
+      }
     }
   }
 
@@ -203,11 +266,14 @@ cudaError_t launch_oproj_tc(const v4_config& cfg, const void* o, const void* wo_
   if (e) return cudaErrorInvalidValue;
   Params prm;
   prm.y = (bf16*)y;
+  prm.norm_w = nullptr;
   prm.status = status;
   prm.T = (int)T;
   prm.G = G;
   prm.N = N;
   prm.Kg = Kg;
+  prm.pair_norm = 0;
+  prm.eps = 0.f;
   cudaError_t err = cudaFuncSetAttribute(oproj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
   if (err != cudaSuccess) return err;
@@ -217,6 +283,38 @@ cudaError_t launch_oproj_tc(const v4_config& cfg, const void* o, const void* wo_
   const long long tiles = (long long)G * ((T + kBM - 1) / kBM) * (N / kBN);
   const int grid = (int)(tiles < sms ? tiles : sms);
   if (grid == 0) return cudaSuccess;
+  oproj_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mx, mw, prm);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_qproj_tc(long long T, int rank, const void* x, const void* w, int N, void* y, int norm,
+                            float eps, const float* norm_w, int* status, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  CUtensorMap mx, mw;
+  int e = 0;
+  e |= make_tmap_bf16_2d(&mx, x, (uint64_t)rank, (uint64_t)T, kBK, kBM, true);
+  e |= make_tmap_bf16_2d(&mw, w, (uint64_t)N, (uint64_t)rank, 64, kBK, true);
+  if (e) return cudaErrorInvalidValue;
+  Params prm;
+  prm.y = (bf16*)y;
+  prm.norm_w = norm_w;
+  prm.status = status;
+  prm.T = (int)T;
+  prm.G = 1;
+  prm.N = N;
+  prm.Kg = rank;
+  prm.pair_norm = norm ? 1 : 0;
+  prm.eps = eps;
+  cudaError_t err = cudaFuncSetAttribute(oproj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+  if (err != cudaSuccess) return err;
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long tiles = ((T + kBM - 1) / kBM) * (N / kBN);
+  const long long units = norm ? tiles / 2 : tiles;
+  const int grid = (int)(units < sms ? units : sms);
   oproj_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mx, mw, prm);
   note_launch();
   return cudaGetLastError();

@@ -124,6 +124,19 @@ def test_e4m3_indexer_host_checks(lib):
     assert lib.v4_quantize_e4m3(None, 0, 128, None, None, None) == L.V4_OK
 
 
+def test_q_projection_host_checks(lib):
+    cfg = L.config_from_preset(SI.preset("tiny_csa_f32"))
+    st = lib.v4_q_proj(C.byref(cfg), 16, 1024, 16, 1, None, None, 16, None, None)
+    assert st == L.V4_ERR_UNSUPPORTED and "bf16" in lib.v4_last_error().decode()
+    cfg = L.config_from_preset(SI.preset("csa_bf16_4k"))
+    st = lib.v4_q_proj(C.byref(cfg), 16, 1000, 16, 1, None, None, 16, None, None)
+    assert st == L.V4_ERR_UNSUPPORTED
+    st = lib.v4_q_proj(C.byref(cfg), 16, 1024, 16, 2, None, None, 16, None, None)
+    assert st == L.V4_ERR_INVALID_ARG and "q_norm" in lib.v4_last_error().decode()
+    st = lib.v4_q_proj(C.byref(cfg), 16, 1024, 16, 1, None, 16, 16, None, None)
+    assert st == L.V4_ERR_INVALID_ARG and "iq" in lib.v4_last_error().decode()
+
+
 def test_error_text_is_per_thread(lib):
     import threading
     cfg = L.config_from_preset(SI.preset("csa_bf16_4k"))
