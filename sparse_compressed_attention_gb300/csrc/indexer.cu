@@ -96,7 +96,7 @@ topk_kernel(const float* __restrict__ scores, int32_t* __restrict__ idx, float* 
   extern __shared__ uint32_t skeys[];
   __shared__ int s_hist[kTopkWarps][256];
   __shared__ uint32_t s_prefix, s_mask;
-  __shared__ int s_krem;
+  __shared__ int s_krem, s_done;
   const int t = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int nv = min(n_visible(t, ratio), N);
@@ -113,9 +113,9 @@ topk_kernel(const float* __restrict__ scores, int32_t* __restrict__ idx, float* 
   const bool in_smem = nv <= smem_cap;
   if (in_smem)
     for (int s = tid; s < nv; s += kTopkThreads) skeys[s] = ordered_key(row[s]);
-  if (tid == 0) { s_prefix = 0u; s_mask = 0u; s_krem = K; }
+  if (tid == 0) { s_prefix = 0u; s_mask = 0u; s_krem = K; s_done = 0; }
   __syncthreads();
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  for (int shift = 24; shift >= 0 && !s_done; shift -= 8) {
     for (int i = tid; i < kTopkWarps * 256; i += kTopkThreads) (&s_hist[0][0])[i] = 0;
     __syncthreads();
     const uint32_t prefix = s_prefix, mask = s_mask;
@@ -126,9 +126,12 @@ topk_kernel(const float* __restrict__ scores, int32_t* __restrict__ idx, float* 
         const uint32_t u = row_key(row, skeys, in_smem, s);
         if ((u & mask) == prefix) bin = (int)((u >> shift) & 0xFFu);
       }
-      // lanes of the warp with the same bin add once
-      const unsigned peers = __match_any_sync(0xffffffffu, bin);
-      if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_hist[wid][bin], __popc(peers));
+      // lanes of the warp with the same bin add once (after the first pass
+      // most keys no longer match the prefix: skip warps with none)
+      if (shift == 24 || __any_sync(0xffffffffu, bin >= 0)) {
+        const unsigned peers = __match_any_sync(0xffffffffu, bin);
+        if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_hist[wid][bin], __popc(peers));
+      }
     }
     __syncthreads();
     // totals per digit
@@ -167,11 +170,17 @@ topk_kernel(const float* __restrict__ scores, int32_t* __restrict__ idx, float* 
         s_krem = krem - acc;
         s_prefix = prefix | ((uint32_t)dsel << shift);
         s_mask = mask | (0xFFu << shift);
+        // every key of the digit is taken: the prefix already separates the
+        // selection, the remaining digits need no pass
+        if (s_hist[0][dsel] == krem - acc) s_done = 1;
       }
     }
     __syncthreads();
   }
-  const uint32_t kth = s_prefix;
+  // the k-th key's resolved digits; keys compare on those digits only (all
+  // 32 bits unless the selection was separated earlier, in which case every
+  // key equal to kth on them is taken)
+  const uint32_t kth = s_prefix, kmask = s_mask;
   const int ties_needed = s_krem;      // keys equal to kth that are taken
   // Compaction: warp w owns the contiguous index range [lo, hi).  Counts of
   // keys above kth and equal to kth per warp give every warp its first
@@ -182,7 +191,7 @@ topk_kernel(const float* __restrict__ scores, int32_t* __restrict__ idx, float* 
   int gt = 0, eq = 0;
   for (int s0 = lo; s0 < hi; s0 += 32) {
     const int s = s0 + lane;
-    const uint32_t u = s < hi ? row_key(row, skeys, in_smem, s) : 0u;
+    const uint32_t u = s < hi ? row_key(row, skeys, in_smem, s) & kmask : 0u;
     gt += __popc(__ballot_sync(0xffffffffu, s < hi && u > kth));
     eq += __popc(__ballot_sync(0xffffffffu, s < hi && u == kth));
   }
@@ -197,7 +206,7 @@ topk_kernel(const float* __restrict__ scores, int32_t* __restrict__ idx, float* 
   const unsigned below = (1u << lane) - 1u;
   for (int s0 = lo; s0 < hi; s0 += 32) {
     const int s = s0 + lane;
-    const uint32_t u = s < hi ? row_key(row, skeys, in_smem, s) : 0u;
+    const uint32_t u = s < hi ? row_key(row, skeys, in_smem, s) & kmask : 0u;
     const unsigned tie_bits = __ballot_sync(0xffffffffu, s < hi && u == kth);
     const int my_tie = tie_rank + __popc(tie_bits & below);
     const bool take = s < hi && (u > kth || (u == kth && my_tie < ties_needed));
