@@ -70,7 +70,7 @@ def layer_work(p):
 NCU_TRAFFIC = {
     "csa_attention": ("mqa_tc.cu", "9d14665343ab875b9a9c974edb5cd0a8594cd8a6f8a360ca40ded6bfa03ef2ff", 2162648832),
     "hca_attention": ("mqa_tc.cu", "9d14665343ab875b9a9c974edb5cd0a8594cd8a6f8a360ca40ded6bfa03ef2ff", 2121747968),
-    "csa_indexer": ("indexer_tc.cu", "ecff08a0aaf63cfbe4cb2a13b428f4d1b048212bf3642ec0a93bc2a95ab9a281", 395698432),
+    "csa_indexer": ("indexer_tc.cu", "f649d2ee00405a246972c64eaac6e25974ae18b5f9dabc20e18c441ef48084c2", 398966784),
 }
 
 

@@ -113,11 +113,12 @@ topk_kernel(const float* __restrict__ scores, int32_t* __restrict__ idx, float* 
   const bool in_smem = nv <= smem_cap;
   if (in_smem)
     for (int s = tid; s < nv; s += kTopkThreads) skeys[s] = ordered_key(row[s]);
+  for (int i = tid; i < kTopkWarps * 256; i += kTopkThreads) (&s_hist[0][0])[i] = 0;
   if (tid == 0) { s_prefix = 0u; s_mask = 0u; s_krem = K; s_done = 0; }
   __syncthreads();
   for (int shift = 24; shift >= 0 && !s_done; shift -= 8) {
-    for (int i = tid; i < kTopkWarps * 256; i += kTopkThreads) (&s_hist[0][0])[i] = 0;
-    __syncthreads();
+    // histograms are zero here: cleared before the first pass, and by the
+    // select phase of the previous one
     const uint32_t prefix = s_prefix, mask = s_mask;
     for (int s0 = 0; s0 < nv; s0 += kTopkThreads) {
       const int s = s0 + tid;
@@ -161,10 +162,10 @@ topk_kernel(const float* __restrict__ scores, int32_t* __restrict__ idx, float* 
       const int before = incl - local;
       const bool mine = before < krem && incl >= krem;
       if (mine) {
-        int acc = before, dsel = 0;
+        int acc = before, dsel = 0, csel = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          if (acc + cnt[i] >= krem) { dsel = 255 - 8 * lane - i; break; }
+          if (acc + cnt[i] >= krem) { dsel = 255 - 8 * lane - i; csel = cnt[i]; break; }
           acc += cnt[i];
         }
         s_krem = krem - acc;
@@ -172,8 +173,12 @@ topk_kernel(const float* __restrict__ scores, int32_t* __restrict__ idx, float* 
         s_mask = mask | (0xFFu << shift);
         // every key of the digit is taken: the prefix already separates the
         // selection, the remaining digits need no pass
-        if (s_hist[0][dsel] == krem - acc) s_done = 1;
+        if (csel == krem - acc) s_done = 1;
       }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s_hist[0][255 - 8 * lane - i] = 0;     // this lane's digits, read above
+    } else {
+      for (int i = lane; i < 256; i += 32) s_hist[wid][i] = 0;            // per-warp counts, summed above
     }
     __syncthreads();
   }
