@@ -405,11 +405,8 @@ def run_e2e(args, layers, dev):
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     done = [None] * len(layers)       # compute of layer i finished (inputs free)
     read = [None] * len(layers)       # read-back of layer i's o finished (o free)
-    torch.cuda.synchronize(dev)
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(comp)
-    for _ in range(n):
+
+    def step():
         for i, (L, (hx, ho)) in enumerate(zip(layers, hosts)):
             with torch.cuda.stream(s_in):
                 if done[i] is not None:
@@ -430,6 +427,20 @@ def run_e2e(args, layers, dev):
                 ho.copy_(L["outs"]["o"], non_blocking=True)
                 read[i] = torch.cuda.Event()
                 read[i].record(s_out)
+
+    # one untimed pass through the same pipeline (first use of the pinned
+    # buffers), then n timed steps starting from an empty pipeline
+    step()
+    comp.wait_stream(s_in)
+    comp.wait_stream(s_out)
+    torch.cuda.synchronize(dev)
+    done = [None] * len(layers)
+    read = [None] * len(layers)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(comp)
+    for _ in range(n):
+        step()
     comp.wait_stream(s_in)
     comp.wait_stream(s_out)
     e1.record(comp)
@@ -760,7 +771,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--seq", type=int, default=16384)
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-rows", type=int, default=64)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-rows", type=int, default=6)
