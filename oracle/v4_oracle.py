@@ -485,6 +485,71 @@ def sparse_mqa(q, kv, ent, idx, sink, inv_freq, ratio, window, scale=None,
 
 
 # ---------------------------------------------------------------------------
+# Sparse indexer distillation target  ([PR] item 5: KL(attention || indexer)
+# over the selected entries, the sparse top-k variant kept in [B, S, K];
+# item 11: the target branch is detached, head-summed inside the loop)
+# ---------------------------------------------------------------------------
+def indexer_kl_target(q, kv, ent, idx, sink, inv_freq, ratio, window, iscore=None, scale=None,
+                      rows=None, rows_only=False):
+    """Target distribution of the indexer and the KL loss, per query t.
+
+    A_h = the main attention's probabilities of head h over all of t's keys
+    (selected entries, window tokens, sink in the denominator), as in
+    ``sparse_mqa``.  The target over t's selection slots is the head sum of
+    A on the selected entries, L1-normalised over the slots:
+        p[t, k] = sum_h A_h[idx[t,k]] / sum_k' sum_h A_h[idx[t,k']]
+    (0 on padding slots, and everywhere when the entries carry no mass).
+    With ``iscore`` (the indexer's scores of the slots) the indexer's
+    distribution is qd = softmax over the valid slots, the loss is
+    KL(p || qd) = sum_k p (log p - log qd) (0 log 0 = 0) and its gradient
+    with respect to iscore is qd - p.
+    Returns dict(target [B,T,K], loss [B,T] or None, dscore [B,T,K] or None).
+    """
+    q = np.asarray(q, dtype=F64)
+    B, S, H, D = q.shape
+    scale = D ** -0.5 if (scale is None or scale <= 0) else scale
+    rows = np.arange(S) if rows is None else np.asarray(rows)
+    idx = np.asarray(idx)
+    K = idx.shape[-1]
+    z = None if sink is None else np.asarray(sink, dtype=F64)
+    target = np.zeros((B, len(rows), K), dtype=F64)
+    loss = np.zeros((B, len(rows)), dtype=F64) if iscore is not None else None
+    dscore = np.zeros((B, len(rows), K), dtype=F64) if iscore is not None else None
+    for b in range(B):
+        for i, t in enumerate(rows):
+            t = int(t)
+            r = i if rows_only else t
+            slots = np.nonzero(idx[b, r] >= 0)[0]
+            if len(slots) == 0:
+                continue
+            keys = attention_keys(0, 0, kv[b:b + 1], ent[b:b + 1], idx[b:b + 1, r:r + 1], inv_freq,
+                                  ratio, window, t=t)
+            qr = rope_rotate(q[b, r], t, inv_freq)
+            logits = scale * (qr @ keys.T)                      # [H, nk]; entries first, in slot order
+            m = logits.max(axis=1)
+            if z is not None:
+                m = np.maximum(m, z)
+            e = np.exp(logits - m[:, None])
+            den = e.sum(axis=1)
+            if z is not None:
+                den = den + np.exp(z - m)
+            A = e / den[:, None]
+            raw = A[:, :len(slots)].sum(axis=0)
+            tot = raw.sum()
+            pk = raw / tot if tot > 0 else np.zeros_like(raw)
+            target[b, i, slots] = pk
+            if iscore is not None:
+                sc = np.asarray(iscore, dtype=F64)[b, r, slots]
+                lq = sc - sc.max()
+                lq = lq - np.log(np.exp(lq).sum())
+                qd = np.exp(lq)
+                nz = pk > 0
+                loss[b, i] = float(np.sum(pk[nz] * (np.log(pk[nz]) - lq[nz])))
+                dscore[b, i, slots] = qd - pk
+    return {"target": target, "loss": loss, "dscore": dscore}
+
+
+# ---------------------------------------------------------------------------
 # Attention backward  ([BLOG] "Attention kernels for the three layer types",
 # backward: the gradient of the same forward, split there into dQ, a
 # head-dimension contraction ("interm") and the delta rowsum(O * dO))

@@ -10,6 +10,7 @@ import pytest
 
 from oracle import v4_oracle as O
 import tests.test_oracle_fp8_pins as F
+import tests.test_oracle_kl_pins as KL
 import tests.test_oracle_pins as P
 
 _rope = O.rope_rotate
@@ -123,6 +124,44 @@ def _qproj_transposed_weight(qlat, wq, n_heads, head_dim, norm=True, eps=0.0, no
     return _qproj(qlat, w, n_heads, head_dim, norm, eps, norm_w, store_bf16)
 
 
+_klt = O.indexer_kl_target
+
+
+def _kl_sum_before_normalising(q, kv, ent, idx, sink, inv_freq, ratio, window, iscore=None, scale=None,
+                               rows=None, rows_only=False):
+    # heads summed as raw exponentials (one shared shift), normalised once
+    q = np.asarray(q, dtype=np.float64)
+    B, S, H, D = q.shape
+    sc = D ** -0.5
+    rows_ = np.arange(S) if rows is None else np.asarray(rows)
+    out = _klt(q, kv, ent, idx, sink, inv_freq, ratio, window, iscore, scale, rows, rows_only)
+    for b in range(B):
+        for i, t in enumerate(rows_):
+            slots = np.nonzero(np.asarray(idx)[b, t] >= 0)[0]
+            if not len(slots):
+                continue
+            keys = O.attention_keys(0, 0, kv[b:b + 1], ent[b:b + 1], np.asarray(idx)[b:b + 1, t:t + 1], inv_freq,
+                                    ratio, window, t=int(t))
+            lg = sc * (O.rope_rotate(q[b, t], int(t), inv_freq) @ keys.T)
+            e = np.exp(lg - lg.max()).sum(axis=0)[:len(slots)]
+            out["target"][b, i, slots] = e / e.sum()
+    return out
+
+
+def _kl_entries_only(q, kv, ent, idx, sink, inv_freq, ratio, window, iscore=None, scale=None,
+                     rows=None, rows_only=False):
+    # per-head softmax over the selected entries alone (window, sink dropped)
+    return _klt(q, kv, ent, idx, None, inv_freq, ratio, 0, iscore, scale, rows, rows_only)
+
+
+def _kl_gradient_sign(q, kv, ent, idx, sink, inv_freq, ratio, window, iscore=None, scale=None,
+                      rows=None, rows_only=False):
+    out = _klt(q, kv, ent, idx, sink, inv_freq, ratio, window, iscore, scale, rows, rows_only)
+    if out["dscore"] is not None:
+        out["dscore"] = -out["dscore"]
+    return out
+
+
 MUTATIONS = [
     ("rope_rotate", _flip_sign, P.test_rope_is_complex_multiplication),
     ("sparse_mqa", _inflated_scale, P.test_softmax_scale_is_head_dim_power),
@@ -138,6 +177,9 @@ MUTATIONS = [
     ("quantize_e4m3_rows", _quant_tensor_scale, F.test_quantizer_row_maximum_lands_on_448),
     ("q_projection", _qproj_whole_row_norm, P.test_q_projection_heads_have_unit_rms_and_ignore_scale),
     ("q_projection", _qproj_transposed_weight, P.test_q_projection_matches_explicit_sums),
+    ("indexer_kl_target", _kl_sum_before_normalising, KL.test_two_heads_without_window),
+    ("indexer_kl_target", _kl_entries_only, KL.test_two_heads_with_window_mass),
+    ("indexer_kl_target", _kl_gradient_sign, KL.test_loss_gradient_matches_central_differences),
 ]
 
 
