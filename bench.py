@@ -533,6 +533,65 @@ def run_qproj(args):
     print(json.dumps(line), flush=True)
 
 
+def run_kl(args):
+    """--workload kl: the sparse indexer distillation target (target, KL loss
+    and its gradient) of the CSA layer at B=1, S tokens, after one forward of
+    the layer has produced the selections, their scores, the entries and lse."""
+    import torch
+
+    import sparse_compressed_attention_gb300 as V
+    from sparse_compressed_attention_gb300 import build as Bld
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    Bld.build()
+    V.lib()
+    S = args.seq
+    L = make_layer("csa_bf16_16k", S, dev, seed=6000)
+    p, x, outs = L["p"], L["x"], L["outs"]
+    B, H, K = p["B"], p["H"], p["K"]
+    outs["ent"] = torch.empty(B, S // p["ratio"], p["D"], dtype=torch.bfloat16, device=dev)
+    outs["iscore"] = torch.empty(B, S, K, device=dev)
+    run_layer(L)
+    target = torch.empty(B, S, K, device=dev)
+    loss = torch.empty(B, S, device=dev)
+    dscore = torch.empty(B, S, K, device=dev)
+    args_ = (L["cfg"], x["q"], outs["ent"], outs["idx"], outs["lse"], outs["iscore"], x["inv_freq"], target, loss,
+             dscore, L["ws"])
+    for _ in range(args.warmup):
+        V.v4_indexer_kl_target(*args_)
+    torch.cuda.synchronize(dev)
+    clk = ClockSampler(smi_index(0))
+    clk.start()
+    stream = torch.cuda.current_stream(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = V.v4_launch_count()
+    t0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        V.v4_indexer_kl_target(*args_)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    clk.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    pairs = int((outs["idx"] >= 0).sum().item())
+    flops = 2.0 * H * p["D"] * pairs                 # the logits of every (query, selected entry)
+    tf = flops / (ms / 1e3) / 1e12
+    peaks = load_peaks()
+    line = {"metric": "indexer distillation target tokens/s at S=%d (CSA, top-%d)" % (S, K),
+            "value": round(B * S / (ms / 1e3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; the layer's own selections)",
+            "config": {"workload": "sparse indexer KL target, loss and gradient of one CSA layer, B=1, S=%d, "
+                                   "H=64, D=512, top-%d" % (S, K), "global_batch": B, "seq_len": S,
+                       "selected_pairs": pairs},
+            "clocks": clk.summary(t0, t1), "gpu_launches": V.v4_launch_count() - launches0,
+            "device_status": V.v4_get_device_status(),
+            "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16"], "unit": "TFLOP/s",
+                         "frac": round(tf / peaks["bf16"], 4), "traffic": None, "flops_per_launch": flops}}
+    print(json.dumps(line), flush=True)
+
+
 def run_workload(args):
     """--workload stack | csa: one JSON line for that workload (1 GPU)."""
     import torch
@@ -779,15 +838,18 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="time eager calls instead of a captured step")
     ap.add_argument("--indexer-fp8", type=int, choices=[0, 1], default=0,
                     help="--workload csa: opt-in E4M3 indexer QK (the default keeps bf16 operands)")
-    ap.add_argument("--workload", choices=["pair", "stack", "csa", "pro", "qproj"], default="pair",
+    ap.add_argument("--workload", choices=["pair", "stack", "csa", "pro", "qproj", "kl"], default="pair",
                     help="pair: the CSA + HCA layer pair (the reported line); stack: the 43-layer "
                          "Flash stack with grouped wo_a at B=2; csa: one CSA layer (e.g. --seq 65536); "
-                         "pro: the pair with 128 heads and top-1024; qproj: the rank-1024 query projections")
+                         "pro: the pair with 128 heads and top-1024; qproj: the rank-1024 query projections; "
+                         "kl: the indexer distillation target of the CSA layer")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
     elif args.workload == "qproj":
         run_qproj(args)
+    elif args.workload == "kl":
+        run_kl(args)
     elif args.workload != "pair":
         run_workload(args)
     else:

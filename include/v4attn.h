@@ -307,6 +307,33 @@ v4_status v4_q_proj(const v4_config* cfg, const void* qlat, int32_t rank, const 
                     void* stream);
 
 /* ----------------------------------------------------------------------
+ * Sparse indexer distillation target.  [PR] item 5: KL(attention ||
+ * indexer) over the selected entries, the sparse top-k variant that stays
+ * in [B, S, K]; item 11: the target branch is detached and its heads are
+ * summed inside the loop, so [B, H, S, K] never exists.
+ *
+ * With A_h the attention probabilities of v4_sparse_mqa_fwd for head h
+ * (window and sink included in the normalisation, given by lse):
+ *   target[t,k] = sum_h A_h[idx[t,k]] / sum_k' sum_h A_h[idx[t,k']]
+ * over the valid slots (0 on padding and on rows without selections).  With
+ * iscore (the indexer scores of the slots, as v4_indexer_topk returns
+ * them) and qd = softmax of iscore over the valid slots:
+ *   loss[t]     = sum_k target (log target - log qd)     (nullable)
+ *   dscore[t,k] = qd - target, the gradient of sum_t loss[t] with respect
+ *                 to iscore (0 on padding)                 (nullable)
+ *   q    : [B, S, H, D] un-rotated queries.   ent : [B, N, D] rotated entries.
+ *   idx  : [B, S, K] selections.              lse : [B, S, H] of the forward.
+ * Tensor-core shapes only (bf16, H a multiple of 64 up to 512, D = 512,
+ * R = 64, K <= 1024, N <= 65536); others return V4_ERR_UNSUPPORTED.
+ * Heads and slices are summed with fp32 atomics (not bitwise reproducible).
+ * workspace : at least v4_workspace_size bytes.
+ * --------------------------------------------------------------------*/
+v4_status v4_indexer_kl_target(const v4_config* cfg, const void* q, const void* ent,
+                               const int32_t* idx, const float* lse, const float* iscore,
+                               const float* inv_freq, float* target, float* loss, float* dscore,
+                               void* workspace, size_t ws_bytes, void* stream);
+
+/* ----------------------------------------------------------------------
  * Grouped low-rank output projection.  [BLOG] "The DeepSeek-V4-Flash
  * architecture": the 64 x 512 output splits into o_groups groups, each
  * through an o_rank bottleneck.  Group g holds heads g*H/G .. (g+1)*H/G-1
@@ -378,7 +405,8 @@ uint64_t v4_launch_count(void);
  * prep, 3 indexer scores, 4 top-k, 5 attention, 6 output projection,
  * 7 backward prep (clears, tables, key rotation, query/gradient rotation and
  * delta), 8 attention backward, 9 window-gradient de-rotation, 10 E4M3
- * quantisation of the indexer operands, 11 query projections.
+ * quantisation of the indexer operands, 11 query projections, 12 indexer
+ * distillation target.
  * --------------------------------------------------------------------*/
 v4_status v4_profile_enable(int32_t on);
 int32_t v4_profile_count(void);

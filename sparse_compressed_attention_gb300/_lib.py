@@ -28,10 +28,10 @@ EXPORTS = ["v4_rope_inv_freq", "v4_workspace_size", "v4_compress", "v4_indexer_p
            "v4_last_error", "v4_get_device_status", "v4_reset_device_status", "v4_launch_count",
            "v4_profile_enable", "v4_profile_count", "v4_profile_get", "v4_sparse_mqa_fwd_noalloc",
            "v4_bwd_workspace_size", "v4_sparse_mqa_bwd", "v4_quantize_e4m3", "v4_indexer_topk_e4m3",
-           "v4_q_proj"]
+           "v4_q_proj", "v4_indexer_kl_target"]
 PROFILE_KINDS = {0: "compress", 1: "window_rotate", 2: "indexer_prep", 3: "indexer_scores", 4: "topk",
                  5: "attention", 6: "o_proj", 7: "bwd_prep", 8: "bwd_attention", 9: "bwd_derotate",
-                 10: "indexer_quant", 11: "q_proj"}
+                 10: "indexer_quant", 11: "q_proj", 12: "kl_target"}
 
 
 class V4Error(RuntimeError):
@@ -85,6 +85,7 @@ def lib(path=None):
         "v4_sparse_mqa_fwd_noalloc": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
         "v4_grouped_o_proj": [cfgp, vp, vp, vp, vp],
         "v4_q_proj": [cfgp, vp, i32, vp, i32, vp, vp, vp, vp, vp],
+        "v4_indexer_kl_target": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
         "v4_bwd_workspace_size": [cfgp, C.POINTER(sz)],
         "v4_sparse_mqa_bwd": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
         "v4_attn_layer_fwd": [cfgp, C.POINTER(v4_layer_inputs), C.POINTER(v4_layer_outputs), vp, sz, vp],
@@ -283,6 +284,20 @@ def v4_q_proj(cfg, qlat, wq, q, q_norm=1, q_norm_w=None, wiq=None, iq=None, stre
                            _ptr(wiq, "wiq", torch.bfloat16, optional=True), _ptr(q, "q", torch.bfloat16),
                            _ptr(iq, "iq", torch.bfloat16, optional=True), _stream(stream)))
     return q, iq
+
+
+def v4_indexer_kl_target(cfg, q, ent, idx, lse, iscore, inv_freq, target, loss, dscore, workspace, stream=None):
+    """Distillation target of the indexer (and, with iscore, the KL loss and its gradient)."""
+    dt = _storage(cfg)
+    _check(lib().v4_indexer_kl_target(C.byref(cfg), _ptr(q, "q", dt), _ptr(ent, "ent", dt, optional=True),
+                                      _ptr(idx, "idx", torch.int32), _ptr(lse, "lse", torch.float32),
+                                      _ptr(iscore, "iscore", torch.float32, optional=True),
+                                      _ptr(inv_freq, "inv_freq", torch.float32, optional=True),
+                                      _ptr(target, "target", torch.float32),
+                                      _ptr(loss, "loss", torch.float32, optional=True),
+                                      _ptr(dscore, "dscore", torch.float32, optional=True),
+                                      _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)))
+    return target
 
 
 def v4_grouped_o_proj(cfg, o, wo_a, y, stream=None):

@@ -65,7 +65,7 @@ static std::vector<ProfRec> g_prof;
 
 enum { K_COMPRESS = 0, K_ROTATE = 1, K_IDX_PREP = 2, K_IDX_SCORE = 3, K_TOPK = 4, K_ATTN = 5,
        K_OPROJ = 6, K_BWD_PREP = 7, K_BWD_ATTN = 8, K_BWD_FIN = 9, K_IDX_QUANT = 10,
-       K_QPROJ = 11 };
+       K_QPROJ = 11, K_KL_TARGET = 12 };
 
 struct ProfScope {
   bool on = false;
@@ -601,6 +601,41 @@ v4_status v4_grouped_o_proj(const v4_config* cfg, const void* o, const void* wo_
   REQ(wo_a, "wo_a");
   REQ(y, "y");
   return do_oproj(*cfg, o, wo_a, y, (cudaStream_t)stream);
+}
+
+v4_status v4_indexer_kl_target(const v4_config* cfg, const void* q, const void* ent, const int32_t* idx,
+                               const float* lse, const float* iscore, const float* inv_freq, float* target,
+                               float* loss, float* dscore, void* workspace, size_t ws_bytes, void* stream) {
+  v4_status s = check_cfg(cfg);
+  if (s != V4_OK) return s;
+  const v4_config& c = *cfg;
+  if (c.topk < 1 || c.ratio < 1) return fail(V4_ERR_INVALID_ARG, "the target needs a selection (topk >= 1, ratio >= 1)");
+  if (!kl_target_tc_supported(c))
+    return fail(V4_ERR_UNSUPPORTED, "the distillation target needs bf16, H a multiple of 64 up to 512, D=512, R=64, "
+                                    "K <= 1024");
+  REQ(q, "q");
+  REQ(idx, "idx");
+  REQ(lse, "lse");
+  REQ(target, "target");
+  if (c.seqlen / c.ratio > 0) REQ(ent, "ent");
+  if (c.rope_dim > 0) REQ(inv_freq, "inv_freq");
+  OPT(iscore, "iscore");
+  OPT(loss, "loss");
+  OPT(dscore, "dscore");
+  if ((loss || dscore) && !iscore) return fail(V4_ERR_INVALID_ARG, "loss and dscore need iscore");
+  s = check_ws(c, workspace, ws_bytes);
+  if (s != V4_OK) return s;
+  int* status = status_ptr();
+  if (!status) return fail(V4_ERR_CUDA, "device status word unavailable");
+  cudaStream_t st = (cudaStream_t)stream;
+  char* ws = (char*)workspace;
+  s = do_rope_table(c, inv_freq, ws, st);
+  if (s != V4_OK) return s;
+  const Workspace plan = plan_workspace(c);
+  ProfScope ps(K_KL_TARGET, st);
+  CU(launch_kl_target(c, q, ent, idx, lse, iscore, (const float2*)(ws + plan.rope), target, loss, dscore, status, st),
+     "distillation target kernel");
+  return V4_OK;
 }
 
 v4_status v4_q_proj(const v4_config* cfg, const void* qlat, int32_t rank, const void* wq, int32_t q_norm,

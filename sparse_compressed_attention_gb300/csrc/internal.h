@@ -113,6 +113,13 @@ cudaError_t launch_mqa_tc(const v4_config& c, const void* q, const void* kv_rot,
                           const float* wmax, const float* emax, void* o, float* lse,
                           int* counters, int* status, cudaStream_t st);
 
+// ---- sparse indexer distillation target (kl_target_tc.cu)
+bool kl_target_tc_supported(const v4_config& c);
+// target [B,S,K] (written), loss [B,S] and dscore [B,S,K] nullable (need iscore)
+cudaError_t launch_kl_target(const v4_config& c, const void* q, const void* ent, const int32_t* idx,
+                             const float* lse, const float* iscore, const float2* cs_table, float* target,
+                             float* loss, float* dscore, int* status, cudaStream_t st);
+
 // ---- attention backward (mqa_bwd_tc.cu)
 bool mqa_bwd_tc_supported(const v4_config& c);
 // qr = rot(q, t), dor = rot(dout, t) (storage dtype), delta = dout . o per
