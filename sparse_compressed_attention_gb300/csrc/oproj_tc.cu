@@ -58,6 +58,7 @@ struct Params {
   int* status;
   int T, G, N, Kg;     // tokens, groups, outputs per group, inputs per group
   int pair_norm;       // 1: RMS-normalise each pair of consecutive 256-column tiles (a 512-wide head)
+  int m_fast;          // 1: token tiles vary fastest (each weight block is read once from DRAM)
   float eps;
 };
 
@@ -73,8 +74,17 @@ __device__ __forceinline__ void tile_of(int tile, const Params& p, int& g, int& 
   const int mt = (p.T + kBM - 1) / kBM;
   g = tile / (mt * nt);
   const int r = tile % (mt * nt);
-  m0 = (r / nt) * kBM;
-  n0 = (r % nt) * kBN;
+  if (!p.m_fast) {               // grouped projection: a token tile's outputs side by side
+    m0 = (r / nt) * kBM;
+    n0 = (r % nt) * kBN;
+  } else if (p.pair_norm) {      // (head, token tile) pairs, token tiles fastest
+    const int pr = r >> 1;
+    m0 = (pr % mt) * kBM;
+    n0 = (pr / mt) * 2 * kBN + (r & 1) * kBN;
+  } else {
+    m0 = (r % mt) * kBM;
+    n0 = (r / mt) * kBN;
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -273,6 +283,7 @@ cudaError_t launch_oproj_tc(const v4_config& cfg, const void* o, const void* wo_
   prm.N = N;
   prm.Kg = Kg;
   prm.pair_norm = 0;
+  prm.m_fast = 0;
   prm.eps = 0.f;
   cudaError_t err = cudaFuncSetAttribute(oproj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
@@ -305,6 +316,7 @@ cudaError_t launch_qproj_tc(long long T, int rank, const void* x, const void* w,
   prm.N = N;
   prm.Kg = rank;
   prm.pair_norm = norm ? 1 : 0;
+  prm.m_fast = 1;
   prm.eps = eps;
   cudaError_t err = cudaFuncSetAttribute(oproj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
