@@ -1,5 +1,6 @@
-"""CPU oracle for the DeepSeek-V4-Flash compressed attention forward and the
-gradient of its attention step.
+"""CPU oracle for the DeepSeek-V4-Flash compressed attention forward, its query
+and output projections, the gradient of its attention step and the indexer's
+distillation target.
 
 TEST INFRASTRUCTURE ONLY. This module is the slow, plain, float64 statement of
 what the attention path computes. Only the tests, ``__graft_entry__.smoke()``
@@ -46,7 +47,10 @@ Readings of points the pages leave open (each is listed in the design doc):
     rotated entries, window gradients w.r.t. the un-rotated latent;
   * the opt-in E4M3 indexer scales every query-head row and every key row by
     its absolute maximum (the pages name the format, not the scaling), and
-    takes the quantisation decision in float32 as the kernel does.
+    takes the quantisation decision in float32 as the kernel does;
+  * the indexer distillation target sums the heads' attention probabilities
+    (each normalised over all of its keys, window and sink included) on the
+    selected entries and renormalises the sum over the selection slots.
 """
 from __future__ import annotations
 
