@@ -117,7 +117,8 @@ Workspace plan_workspace(const v4_config& c) {
   take(w.kv_rot, w.kv_rot_bytes, B * S * D * es);
   take(w.ent, w.ent_bytes, B * N * D * es);
   take(w.ikey, w.ikey_bytes, sel ? B * N * c.idx_dim * es : 0);
-  take(w.iqp, w.iqp_bytes, sel ? B * S * c.idx_heads * c.idx_dim * es : 0);
+  // bf16 prepared queries (the E4M3 path writes codes instead)
+  take(w.iqp, w.iqp_bytes, sel && !c.indexer_fp8 ? B * S * c.idx_heads * c.idx_dim * es : 0);
   take(w.scores, w.scores_bytes, sel ? B * S * N * 4 : 0);
   take(w.idx, w.idx_bytes, sel ? B * S * c.topk * 4 : 0);
   take(w.knorm, w.knorm_bytes, key_norm_floats(c) * 4);
@@ -236,28 +237,28 @@ static v4_status do_indexer(const v4_config& c, const void* iq, int prepared, co
                             const float* w, const float* f, int32_t* idx, float* iscore,
                             char* ws, cudaStream_t st, bool table_ready) {
   const Workspace plan = plan_workspace(c);
-  const void* iqp = iq;
-  if (!prepared) {
-    if (!table_ready) {
-      v4_status s = do_rope_table(c, f, ws, st);
-      if (s != V4_OK) return s;
-    }
-    ProfScope ps(K_IDX_PREP, st);
-    CU(launch_indexer_prep(c, iq, (const float2*)(ws + plan.rope), f, ws + plan.iqp, st), "indexer prep kernel");
-    iqp = ws + plan.iqp;
+  if (!prepared && !table_ready) {
+    v4_status s = do_rope_table(c, f, ws, st);
+    if (s != V4_OK) return s;
   }
+  const float2* table = (const float2*)(ws + plan.rope);
   float* scores = (float*)(ws + plan.scores);
   if (c.indexer_fp8) {
-    // opt-in E4M3: quantise the prepared queries and the keys per row
+    // opt-in E4M3: queries prepared and quantised in one kernel (or, when the
+    // caller prepared them, quantised alone), keys quantised per row
     uint8_t* qc = (uint8_t*)(ws + plan.qc8);
     float* qs = (float*)(ws + plan.qs8);
     uint8_t* kc = (uint8_t*)(ws + plan.kc8);
     float* ks = (float*)(ws + plan.ks8);
     const long long N = c.seqlen / c.ratio;
+    const long long qrows = (long long)c.batch * c.seqlen * c.idx_heads;
+    if (!prepared) {
+      ProfScope ps(K_IDX_PREP, st);
+      CU(launch_indexer_prep_e4m3(c, iq, table, f, qc, qs, st), "indexer prep kernel (E4M3)");
+    }
     {
       ProfScope ps(K_IDX_QUANT, st);
-      CU(launch_quant_e4m3(iqp, (long long)c.batch * c.seqlen * c.idx_heads, c.idx_dim, qc, qs, st),
-         "E4M3 query quantisation kernel");
+      if (prepared) CU(launch_quant_e4m3(iq, qrows, c.idx_dim, qc, qs, st), "E4M3 query quantisation kernel");
       CU(launch_quant_e4m3(ikey, (long long)c.batch * N, c.idx_dim, kc, ks, st), "E4M3 key quantisation kernel");
     }
     int* status = status_ptr();
@@ -267,6 +268,12 @@ static v4_status do_indexer(const v4_config& c, const void* iq, int prepared, co
       CU(launch_indexer_scores_e4m3(c, qc, qs, kc, ks, w, scores, status, st), "E4M3 indexer kernel");
     }
   } else {
+    const void* iqp = iq;
+    if (!prepared) {
+      ProfScope ps(K_IDX_PREP, st);
+      CU(launch_indexer_prep(c, iq, table, f, ws + plan.iqp, st), "indexer prep kernel");
+      iqp = ws + plan.iqp;
+    }
     ProfScope ps(K_IDX_SCORE, st);
     if (c.path != V4_PATH_SIMT && indexer_tc_supported(c)) {
       int* status = status_ptr();

@@ -8,6 +8,7 @@
 // the window of 8 or 128, weighted reduce, all in fp32, one kernel).  Entry
 // RMSNorm and the rotation at r*s follow Primus PR #930 items 1 and 2; the
 // indexer-key Hadamard follows item 6e.
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -388,11 +389,16 @@ __global__ void indexer_prep_kernel(const T* __restrict__ iq, const float2* __re
 // consecutive elements, so five butterfly stages run inside the thread and
 // only two cross lanes (a quarter of the shuffles of the kernel above), and
 // each thread has 64 bytes (bf16) in flight.
-template <typename T>
+// With kCodes (bf16 only) the prepared row is not stored: its bf16 values are
+// quantised to E4M3 by the row's absolute maximum (the rule of the
+// standalone quantiser: scale = amax / 448, codes of x * (448 / amax) in fp32,
+// round to nearest, saturating), and only the codes and the scale are written.
+template <typename T, bool kCodes = false>
 __global__ void __launch_bounds__(256)
 indexer_prep_d128_kernel(const T* __restrict__ iq, const float2* __restrict__ cs_table,
                          const float* __restrict__ inv_freq, T* __restrict__ out,
-                         long long rows, int S, int Hi, int R) {
+                         long long rows, int S, int Hi, int R, uint8_t* __restrict__ codes = nullptr,
+                         float* __restrict__ scales = nullptr) {
   constexpr int Di = 128, kLanes = 4, kPer = 32;
   const long long gt = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   const long long row = gt / kLanes;
@@ -452,9 +458,36 @@ indexer_prep_d128_kernel(const T* __restrict__ iq, const float2* __restrict__ cs
   const float hs = 1.0f / sqrtf((float)Di);
 #pragma unroll
   for (int k = 0; k < kPer; ++k) e[k] *= hs;
-  if (live) {
+  if constexpr (kCodes) {
+    float amax = 0.f;
 #pragma unroll
-    for (int q = 0; q < kPer / 8; ++q) store8(out + row * Di + c0 + 8 * q, e + 8 * q);
+    for (int k = 0; k < kPer; ++k) {
+      e[k] = __bfloat162float(__float2bfloat16_rn(e[k]));
+      amax = fmaxf(amax, fabsf(e[k]));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));     // the row's four lanes
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const float inv = amax > 0.f ? 448.0f / amax : 0.f;
+    if (live) {
+      if (lane == 0) scales[row] = amax > 0.f ? amax / 448.0f : 0.f;
+      uint32_t wv[kPer / 4];
+#pragma unroll
+      for (int q = 0; q < kPer / 4; ++q) {
+        const __nv_fp8x2_storage_t lo =
+            __nv_cvt_float2_to_fp8x2(make_float2(e[4 * q] * inv, e[4 * q + 1] * inv), __NV_SATFINITE, __NV_E4M3);
+        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+            make_float2(e[4 * q + 2] * inv, e[4 * q + 3] * inv), __NV_SATFINITE, __NV_E4M3);
+        wv[q] = (uint32_t)lo | ((uint32_t)hi << 16);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(codes + row * Di + c0);
+      dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+    }
+  } else {
+    if (live) {
+#pragma unroll
+      for (int q = 0; q < kPer / 8; ++q) store8(out + row * Di + c0 + 8 * q, e + 8 * q);
+    }
   }
 }
 
@@ -672,6 +705,18 @@ cudaError_t launch_key_prep(const v4_config& c, const void* kv, const void* ent,
   const int wblocks = (int)((kv_rows + kBoundThreads - 1) / kBoundThreads);
   key_bounds_kernel<<<wblocks + (c.ratio > 0 ? c.batch : 0), kBoundThreads, 0, st>>>(
       kv_norm, ent_rows > 0 ? ent_norm : nullptr, wmax, emax, c.batch, c.seqlen, N, c.window, wblocks);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_indexer_prep_e4m3(const v4_config& c, const void* iq, const float2* cs_table,
+                                     const float* inv_freq, uint8_t* codes, float* scales, cudaStream_t st) {
+  if (c.idx_dim != 128 || c.dtype != V4_BF16) return cudaErrorInvalidValue;
+  const long long rows = (long long)c.batch * c.seqlen * c.idx_heads;
+  const int threads = 256;
+  const long long blocks = (rows * 4 + threads - 1) / threads;
+  indexer_prep_d128_kernel<bf16, true><<<(unsigned)blocks, threads, 0, st>>>(
+      (const bf16*)iq, cs_table, inv_freq, nullptr, rows, c.seqlen, c.idx_heads, c.rope_dim, codes, scales);
   note_launch();
   return cudaGetLastError();
 }

@@ -70,6 +70,10 @@ int make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t 
 // cs_table may be null (angles are then computed in the kernel from inv_freq)
 cudaError_t launch_indexer_prep(const v4_config& c, const void* iq, const float2* cs_table,
                                 const float* inv_freq, void* iqp, cudaStream_t st);
+// The same preparation quantised to E4M3 rows in the kernel (bf16, Di = 128):
+// codes [B,S,Hi,128] and scales [B,S,Hi] instead of the bf16 rows.
+cudaError_t launch_indexer_prep_e4m3(const v4_config& c, const void* iq, const float2* cs_table,
+                                     const float* inv_freq, uint8_t* codes, float* scales, cudaStream_t st);
 
 // ---- indexer (indexer.cu)
 cudaError_t launch_indexer_scores_simt(const v4_config& c, const void* iqp, const void* ikey,

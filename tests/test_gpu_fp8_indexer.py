@@ -114,6 +114,24 @@ def test_e4m3_indexer_topk_stagewise(name, p):
     assert swaps <= max(2, B * S * K // 10000)
 
 
+def test_prepared_queries_quantised_by_the_library():
+    # v4_indexer_topk with E4M3 on queries the caller prepared (bf16, made by
+    # the oracle): the library quantises them with the standalone rule
+    p = SI.preset("csa_bf16_4k", S=1500, q_mode="direct")
+    x = SI.make_layer_inputs(p, "cpu", seed=2)
+    f = inv_freq_for(p)
+    ikey, iqp, qc, qs, kc, ks = _oracle_operands(p, x, f)
+    cfg = V.config_from_preset(p, indexer_fp8=1)
+    B, S, K = p["B"], p["S"], p["K"]
+    idx = torch.empty(B, S, K, dtype=torch.int32, device="cuda")
+    V.v4_indexer_topk(cfg, torch.from_numpy(iqp).to(torch.bfloat16).cuda(), 1,
+                      torch.from_numpy(ikey).to(torch.bfloat16).cuda(), x["w"].cuda(),
+                      torch.from_numpy(f).cuda(), idx, None, V.alloc_workspace(cfg))
+    torch.cuda.synchronize()
+    sel = O.indexer_topk_e4m3(qc, qs, kc, ks, np64(x["w"]), p["ratio"], K)["idx"]
+    assert _overlap(idx.cpu().numpy(), sel) >= 0.995
+
+
 def _layer(p, x, f, fp8):
     xd = dict(to_dev(x), inv_freq=torch.from_numpy(f).cuda())
     cfg = V.config_from_preset(p, indexer_fp8=fp8)
