@@ -1,0 +1,34 @@
+"""The benchmark's algorithmic work counts against the oracle's definitions
+(CPU only): the keys every query attends to (selected or visible entries
+plus its window), the indexer's visible (query, entry) pairs, and the FLOP
+totals the roofline fractions divide by at the benchmark sizes."""
+import numpy as np
+import pytest
+
+import bench
+import seeded_inputs as SI
+from oracle import v4_oracle as O
+
+
+@pytest.mark.parametrize("S,r,K,W", [(300, 4, 16, 16), (1000, 4, 64, 128), (700, 128, 0, 128), (257, 0, 0, 37),
+                                     (90, 1, 0, -1), (50, 4, 0, 0)])
+def test_attention_keys_match_the_oracle(S, r, K, W):
+    brute = sum(O.keys_read(t, r, W, K) for t in range(S))
+    assert bench.attention_keys_total(S, r, K, W) == brute
+
+
+def test_indexer_pairs_match_visibility():
+    p = SI.preset("csa_bf16_4k", S=999)
+    brute = sum(min(O.n_visible(t, p["ratio"]), p["S"] // p["ratio"]) for t in range(p["S"]))
+    assert bench.layer_work(p)["idx_pairs"] == brute
+
+
+def test_flop_totals_at_the_benchmark_sizes():
+    csa = bench.layer_work(SI.preset("csa_bf16_16k"))
+    hca = bench.layer_work(SI.preset("hca_bf16_16k"))
+    H, D = 64, 512
+    assert csa["attn_flops"] == 4.0 * H * D * csa["attn_keys"]
+    assert abs(csa["attn_flops"] / 1e12 - 1.3045) < 1e-3        # 1.305 TFLOP per CSA attention launch
+    assert abs(hca["attn_flops"] / 1e12 - 0.4092) < 1e-3
+    assert abs(csa["idx_flops"] / 1e12 - 0.5497) < 1e-3         # 0.550 TFLOP per indexer launch
+    assert csa["attn_bytes"] == hca["attn_bytes"] == 2 * 16384 * H * D * 2
