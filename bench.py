@@ -85,6 +85,16 @@ def ncu_traffic(key, seq):
     return val if (cur == sha and seq == 16384) else None
 
 
+def indexer_unit(flops, scores_ms, topk_ms, peak):
+    """The indexer as one unit: the score products' FLOPs over the time of
+    the score kernel and the top-k selection that follows it."""
+    ms = scores_ms + topk_ms
+    tf = flops / (ms / 1e3) / 1e12
+    return {"kernel": "csa indexer unit (scores + top-k)", "bound": "tensor", "achieved": round(tf, 2),
+            "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(tf / peak, 4), "flops": flops,
+            "scores_ms": round(scores_ms, 4), "topk_ms": round(topk_ms, 4)}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -358,6 +368,10 @@ def run_ours(args):
                             "traffic": ncu_traffic("csa_indexer", S),
                             "flops_per_launch": work["csa_bf16_16k"]["idx_flops"],
                             "avg_launch_ms": round(a_ms, 4)})
+        tk = per.get(("csa_bf16_16k", "topk"), [])
+        if tk:
+            extra_roofs.append(indexer_unit(work["csa_bf16_16k"]["idx_flops"], a_ms, sum(tk) / len(tk),
+                                            peaks["bf16"]))
 
     e2e = run_e2e(args, layers, dev) if args.e2e_steps > 0 else None
 
@@ -687,6 +701,9 @@ def run_workload(args):
                       "achieved": round(tf, 2), "peak": round(pk, 1), "unit": "TFLOP/s",
                       "frac": round(tf / pk, 4), "flops_per_launch": wk["idx_flops"],
                       "avg_launch_ms": round(a_ms, 4)})
+        tk = per.get(("csa", "topk"), [])
+        if tk:
+            other.append(indexer_unit(wk["idx_flops"], a_ms, sum(tk) / len(tk), pk))
     op = [t for (n, k), v in per.items() if k == "o_proj" for t in v]
     if op:
         a_ms = sum(op) / len(op)

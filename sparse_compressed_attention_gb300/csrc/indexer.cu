@@ -76,24 +76,63 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
 constexpr int kTopkThreads = 256;
 
 // One block per (t, b): exact top-K of the row's n_vis scores.  The row is
-// loaded once into shared memory as order-preserving 32-bit keys; a 4-pass
-// MSB-first radix select (8 bits per pass) finds the K-th key: each pass
-// builds per-warp 256-bin histograms (lanes that hit the same bin combine
-// their increments first), sums them, and one warp locates the digit with a
-// suffix scan.  The compaction keeps every key above the K-th key plus the
-// lowest-index keys equal to it.  Output in ascending index
-// order, -1 padded.  Rows longer than the shared-memory capacity fall back to
-// reading the keys from global memory on every pass.
+// held in shared memory as order-preserving 32-bit keys; a 4-pass MSB-first
+// radix select (8 bits per pass) finds the K-th key, and a compaction keeps
+// every key above it plus the lowest-index keys equal to it.  Output in
+// ascending index order, -1 padded.
+//
+// The kernel is bound by instruction issue, so each thread takes four
+// consecutive keys per shared-memory load.  Each pass builds per-warp
+// 256-bin histograms: in the first pass (sign and exponent bits) the scores
+// crowd a few bins, so lanes that hit the same bin combine their increments
+// before one shared-memory add, and that pass runs while the keys are
+// loaded; later digits spread over the bins and each matching key adds
+// directly.  One warp locates the digit with a scan.  The select stops once
+// every key of the located digit is taken.  In the compaction each warp owns
+// a contiguous range; per-warp counts give its first output slot and one
+// packed lane scan per 128 keys orders its writes.  Rows longer than the
+// shared-memory capacity read their keys from global memory on every pass.
 constexpr int kTopkWarps = kTopkThreads / 32;
 
-__device__ __forceinline__ uint32_t row_key(const float* row, const uint32_t* skeys, bool in_smem, int s) {
-  return in_smem ? skeys[s] : ordered_key(row[s]);
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-__global__ void __launch_bounds__(kTopkThreads)
+// keys 4c .. 4c+3 of the row (entries at or past nv are unspecified)
+__device__ __forceinline__ uint4 row_key4(const float* row, const uint4* skeys4, bool in_smem, bool vec, int c,
+                                          int nv) {
+  if (in_smem) return skeys4[c];
+  const int s = 4 * c;
+  if (vec && s + 3 < nv) {
+    const float4 f = __ldg(reinterpret_cast<const float4*>(row) + c);
+    return make_uint4(ordered_key(f.x), ordered_key(f.y), ordered_key(f.z), ordered_key(f.w));
+  }
+  return make_uint4(s < nv ? ordered_key(row[s]) : 0u, s + 1 < nv ? ordered_key(row[s + 1]) : 0u,
+                    s + 2 < nv ? ordered_key(row[s + 2]) : 0u, s + 3 < nv ? ordered_key(row[s + 3]) : 0u);
+}
+
+// the four keys' contributions to this warp's histogram of digit `shift`
+template <bool kFirst>
+__device__ __forceinline__ void hist_add4(int* whist, uint4 k4, int s, int nv, uint32_t prefix, uint32_t mask,
+                                          int shift, int lane) {
+  const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    int bin = -1;
+    if (s + j < nv && (kk[j] & mask) == prefix) bin = (int)((kk[j] >> shift) & 0xFFu);
+    if (kFirst) {
+      const unsigned peers = __match_any_sync(0xffffffffu, bin);
+      if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&whist[bin], __popc(peers));
+    } else if (bin >= 0) {
+      atomicAdd(&whist[bin], 1);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kTopkThreads, 8)
 topk_kernel(const float* __restrict__ scores, int32_t* __restrict__ idx, float* __restrict__ iscore,
             int S, int N, int K, int ratio, int smem_cap) {
-  extern __shared__ uint32_t skeys[];
+  extern __shared__ uint4 skeys4[];
   __shared__ int s_hist[kTopkWarps][256];
   __shared__ uint32_t s_prefix, s_mask;
   __shared__ int s_krem, s_done;
@@ -111,30 +150,37 @@ topk_kernel(const float* __restrict__ scores, int32_t* __restrict__ idx, float* 
     return;
   }
   const bool in_smem = nv <= smem_cap;
+  const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+  const int nc = (nv + 3) >> 2;                        // 4-key chunks
+  int* whist = s_hist[wid];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) whist[lane + 32 * i] = 0;  // each warp adds to its own row only
+  __syncwarp();
   if (in_smem)
-    for (int s = tid; s < nv; s += kTopkThreads) skeys[s] = ordered_key(row[s]);
-  for (int i = tid; i < kTopkWarps * 256; i += kTopkThreads) (&s_hist[0][0])[i] = 0;
+    for (int c0 = 0; c0 < nc; c0 += kTopkThreads) {   // load, with the first pass's histogram
+      const int c = c0 + tid;
+      uint4 k4 = make_uint4(0u, 0u, 0u, 0u);
+      if (c < nc) {
+        k4 = row_key4(row, skeys4, false, vec, c, nv);
+        skeys4[c] = k4;
+      }
+      hist_add4<true>(whist, k4, 4 * c, nv, 0u, 0u, 24, lane);
+    }
   if (tid == 0) { s_prefix = 0u; s_mask = 0u; s_krem = K; s_done = 0; }
   __syncthreads();
   for (int shift = 24; shift >= 0 && !s_done; shift -= 8) {
     // histograms are zero here: cleared before the first pass, and by the
     // select phase of the previous one
     const uint32_t prefix = s_prefix, mask = s_mask;
-    for (int s0 = 0; s0 < nv; s0 += kTopkThreads) {
-      const int s = s0 + tid;
-      int bin = -1;
-      if (s < nv) {
-        const uint32_t u = row_key(row, skeys, in_smem, s);
-        if ((u & mask) == prefix) bin = (int)((u >> shift) & 0xFFu);
+    if (shift != 24 || !in_smem) {
+      for (int c0 = 0; c0 < nc; c0 += kTopkThreads) {
+        const int c = c0 + tid;
+        const uint4 k4 = c < nc ? row_key4(row, skeys4, in_smem, vec, c, nv) : make_uint4(0u, 0u, 0u, 0u);
+        if (shift == 24) hist_add4<true>(whist, k4, 4 * c, nv, prefix, mask, shift, lane);
+        else hist_add4<false>(whist, k4, 4 * c, nv, prefix, mask, shift, lane);
       }
-      // lanes of the warp with the same bin add once (after the first pass
-      // most keys no longer match the prefix: skip warps with none)
-      if (shift == 24 || __any_sync(0xffffffffu, bin >= 0)) {
-        const unsigned peers = __match_any_sync(0xffffffffu, bin);
-        if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_hist[wid][bin], __popc(peers));
-      }
+      __syncthreads();
     }
-    __syncthreads();
     // totals per digit
     {
       const int d = tid;                       // kTopkThreads == 256 digits
@@ -187,42 +233,83 @@ topk_kernel(const float* __restrict__ scores, int32_t* __restrict__ idx, float* 
   // key equal to kth on them is taken)
   const uint32_t kth = s_prefix, kmask = s_mask;
   const int ties_needed = s_krem;      // keys equal to kth that are taken
-  // Compaction: warp w owns the contiguous index range [lo, hi).  Counts of
-  // keys above kth and equal to kth per warp give every warp its first
-  // output slot and its first tie rank; each warp then writes its range in
-  // index order.
-  const int span = ((nv + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
-  const int lo = min(wid * span, nv), hi = min(lo + span, nv);
+  // warp w owns the chunks [lo, hi), in index order
+  const int span = ((nc + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
+  const int lo = min(wid * span, nc), hi = min(lo + span, nc);
   int gt = 0, eq = 0;
-  for (int s0 = lo; s0 < hi; s0 += 32) {
-    const int s = s0 + lane;
-    const uint32_t u = s < hi ? row_key(row, skeys, in_smem, s) & kmask : 0u;
-    gt += __popc(__ballot_sync(0xffffffffu, s < hi && u > kth));
-    eq += __popc(__ballot_sync(0xffffffffu, s < hi && u == kth));
+  for (int c0 = lo; c0 < hi; c0 += 32) {
+    const int c = c0 + lane;
+    if (c < hi) {
+      const uint4 k4 = row_key4(row, skeys4, in_smem, vec, c, nv);
+      const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t u = kk[j] & kmask;
+        const bool v = 4 * c + j < nv;
+        gt += (v && u > kth) ? 1 : 0;
+        eq += (v && u == kth) ? 1 : 0;
+      }
+    }
   }
+  gt = __reduce_add_sync(0xffffffffu, gt);
+  eq = __reduce_add_sync(0xffffffffu, eq);
   if (lane == 0) { s_hist[1][wid] = gt; s_hist[2][wid] = eq; }
   __syncthreads();
+  // first output slot and first tie rank of this warp's range
   int out_pos = 0, tie_rank = 0;
   for (int w = 0; w < wid; ++w) {
     const int e = s_hist[2][w];
     out_pos += s_hist[1][w] + max(0, min(e, ties_needed - tie_rank));
     tie_rank += e;
   }
-  const unsigned below = (1u << lane) - 1u;
-  for (int s0 = lo; s0 < hi; s0 += 32) {
-    const int s = s0 + lane;
-    const uint32_t u = s < hi ? row_key(row, skeys, in_smem, s) & kmask : 0u;
-    const unsigned tie_bits = __ballot_sync(0xffffffffu, s < hi && u == kth);
-    const int my_tie = tie_rank + __popc(tie_bits & below);
-    const bool take = s < hi && (u > kth || (u == kth && my_tie < ties_needed));
-    const unsigned take_bits = __ballot_sync(0xffffffffu, take);
-    if (take) {
-      const int pos = out_pos + __popc(take_bits & below);
-      orow[pos] = s;
-      if (srow) srow[pos] = row[s];
+  for (int c0 = lo; c0 < hi; c0 += 32) {
+    const int c = c0 + lane;
+    uint32_t kk[4] = {0u, 0u, 0u, 0u};
+    int n_gt = 0, n_eq = 0;
+    if (c < hi) {
+      const uint4 k4 = row_key4(row, skeys4, in_smem, vec, c, nv);
+      kk[0] = k4.x; kk[1] = k4.y; kk[2] = k4.z; kk[3] = k4.w;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t u = kk[j] & kmask;
+        const bool v = 4 * c + j < nv;
+        n_gt += (v && u > kth) ? 1 : 0;
+        n_eq += (v && u == kth) ? 1 : 0;
+      }
     }
-    out_pos += __popc(take_bits);
-    tie_rank += __popc(tie_bits);
+    // exclusive lane scan of (keys above kth, keys equal to it), 16 bits each
+    // (at most 128 per step)
+    const int packed = n_gt | (n_eq << 16);
+    int incl = packed;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int excl = incl - packed;
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    const int gt_lo = excl & 0xFFFF, eq_lo = excl >> 16;
+    int tie_r = tie_rank + eq_lo;                          // rank of this lane's first tie
+    int pos = out_pos + gt_lo + max(0, min(eq_lo, ties_needed - tie_rank));
+    if (c < hi) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t u = kk[j] & kmask;
+        if (4 * c + j < nv) {
+          const bool tie = u == kth;
+          const bool take = u > kth || (tie && tie_r < ties_needed);
+          tie_r += tie ? 1 : 0;
+          if (take && pos < K) {
+            orow[pos] = 4 * c + j;
+            if (srow) srow[pos] = key_to_float(kk[j]);
+            ++pos;
+          }
+        }
+      }
+    }
+    const int tot_eq = total >> 16;
+    out_pos += (total & 0xFFFF) + max(0, min(tot_eq, ties_needed - tie_rank));
+    tie_rank += tot_eq;
   }
   // slots past the selection (only when fewer than K keys exist; nv > K here)
   if (wid == kTopkWarps - 1)
@@ -263,7 +350,7 @@ cudaError_t launch_topk(const v4_config& c, const float* scores, int32_t* idx, f
   // scores from L2 on every pass, which keeps more rows resident per SM
   // (measured faster at 16384 keys than staging 64 KB per row)
   const int cap = N < 4096 ? N : 4096;
-  const size_t smem = (size_t)cap * sizeof(uint32_t);
+  const size_t smem = (size_t)((cap + 3) & ~3) * sizeof(uint32_t);      // whole 4-key chunks
   cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(c.seqlen, c.batch);
