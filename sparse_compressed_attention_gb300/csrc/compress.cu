@@ -386,9 +386,10 @@ __global__ void indexer_prep_kernel(const T* __restrict__ iq, const float2* __re
 }
 
 // The same transform for Di = 128 with four lanes per row: a lane holds 32
-// consecutive elements, so five butterfly stages run inside the thread and
-// only two cross lanes (a quarter of the shuffles of the kernel above), and
-// each thread has 64 bytes (bf16) in flight.
+// elements (chunk `lane` of 8 in each 32-element block), so five butterfly
+// stages run inside the thread and only two cross lanes (a quarter of the
+// shuffles of the kernel above), each load of the row's four lanes covers 64
+// contiguous bytes (bf16), and each thread has 64 bytes in flight.
 // With kCodes (bf16 only) the prepared row is not stored: its bf16 values are
 // quantised to E4M3 by the row's absolute maximum (the rule of the
 // standalone quantiser: scale = amax / 448, codes of x * (448 / amax) in fp32,
@@ -404,21 +405,23 @@ indexer_prep_d128_kernel(const T* __restrict__ iq, const float2* __restrict__ cs
   const long long row = gt / kLanes;
   const int lane = (int)(gt % kLanes);
   const bool live = row < rows;
-  const int c0 = lane * kPer;
+  // e[8q + i] holds dim 32q + 8 lane + i: the row's four lanes read 64
+  // contiguous bytes per load (bf16), and the butterflies over dim bits 1, 2,
+  // 4, 32 and 64 stay in the thread
   float e[kPer];
 #pragma unroll
   for (int q = 0; q < kPer / 8; ++q) {
-    if (live) load8(iq + row * Di + c0 + 8 * q, e + 8 * q);
+    if (live) load8(iq + row * Di + 32 * q + 8 * lane, e + 8 * q);
     else {
 #pragma unroll
       for (int k = 0; k < 8; ++k) e[8 * q + k] = 0.f;
     }
   }
-  if (live && c0 + kPer > Di - R) {
+  if (live) {
     const long long t = (row / Hi) % S;
 #pragma unroll
     for (int k = 0; k < kPer / 2; ++k) {
-      const int c = c0 + 2 * k;
+      const int c = 32 * (k / 4) + 8 * lane + 2 * (k % 4);       // dim of e[2k]
       if (c >= Di - R) {
         const int j = (c - (Di - R)) / 2;
         float cs, sn;
@@ -433,7 +436,7 @@ indexer_prep_d128_kernel(const T* __restrict__ iq, const float2* __restrict__ cs
       }
     }
   }
-  // in-thread butterflies (h = 1 .. 16)
+  // in-thread butterflies (element strides 1 .. 16: dim bits 1, 2, 4, 32, 64)
 #pragma unroll
   for (int h = 1; h < kPer; h <<= 1) {
 #pragma unroll
@@ -445,7 +448,7 @@ indexer_prep_d128_kernel(const T* __restrict__ iq, const float2* __restrict__ cs
       }
     }
   }
-  // cross-lane butterflies (h = 32, 64)
+  // cross-lane butterflies (dim bits 8, 16)
 #pragma unroll
   for (int hl = 1; hl < kLanes; hl <<= 1) {
     const bool upper = (lane & hl) != 0;
@@ -479,14 +482,14 @@ indexer_prep_d128_kernel(const T* __restrict__ iq, const float2* __restrict__ cs
             make_float2(e[4 * q + 2] * inv, e[4 * q + 3] * inv), __NV_SATFINITE, __NV_E4M3);
         wv[q] = (uint32_t)lo | ((uint32_t)hi << 16);
       }
-      uint4* dst = reinterpret_cast<uint4*>(codes + row * Di + c0);
-      dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-      dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+#pragma unroll
+      for (int q = 0; q < kPer / 8; ++q)
+        *reinterpret_cast<uint2*>(codes + row * Di + 32 * q + 8 * lane) = make_uint2(wv[2 * q], wv[2 * q + 1]);
     }
   } else {
     if (live) {
 #pragma unroll
-      for (int q = 0; q < kPer / 8; ++q) store8(out + row * Di + c0 + 8 * q, e + 8 * q);
+      for (int q = 0; q < kPer / 8; ++q) store8(out + row * Di + 32 * q + 8 * lane, e + 8 * q);
     }
   }
 }

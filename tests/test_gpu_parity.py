@@ -194,6 +194,51 @@ def test_topk_ties_and_crowded_bins(pattern):
             assert set(zeros[:need].tolist()) <= kept and not (set(zeros[need:].tolist()) & kept), t
 
 
+@pytest.mark.parametrize("keys", ["random", "all_zero"])
+def test_topk_rows_longer_than_shared_memory(keys):
+    """Rows with more than 4096 visible entries (S = 20004, ratio 4: up to
+    5001 entries) read their scores from global memory on every select pass:
+    16-byte loads where a row starts on a 16-byte boundary, scalar loads
+    otherwise (N = 5001 is odd, so the alignment of consecutive rows cycles).
+    Random prepared queries and keys: set-exact outside the tie band, kept
+    scores within their fp32 band, ascending indices.  All-zero keys: every
+    score is 0 and each long row keeps its K lowest indices."""
+    p = SI.preset("csa_bf16_4k", S=20004, q_mode="direct")
+    B, S, K, r, Hi, Di = p["B"], p["S"], p["K"], p["ratio"], p["Hi"], p["Di"]
+    N = S // r
+    g = torch.Generator().manual_seed(11)
+    iqp = SI._unit_rms(SI._normal((B, S, Hi, Di), g, "cpu")).to(torch.bfloat16)
+    ikey = SI._unit_rms(SI._normal((B, N, Di), g, "cpu")).to(torch.bfloat16)
+    w = SI._normal((B, S, Hi), g, "cpu")
+    if keys == "all_zero":
+        ikey.zero_()
+    cfg = V.config_from_preset(p)
+    idx = torch.empty(B, S, K, dtype=torch.int32, device="cuda")
+    isc = torch.empty(B, S, K, dtype=torch.float32, device="cuda")
+    fd = torch.from_numpy(inv_freq_for(p)).cuda()
+    V.v4_indexer_topk(cfg, iqp.cuda(), 1, ikey.cuda(), w.cuda(), fd, idx, isc, V.alloc_workspace(cfg))
+    torch.cuda.synchronize()
+    gi, gs = idx.cpu().numpy()[0], isc.cpu().numpy()[0]
+    rows = np.unique(np.concatenate([np.linspace(16390, S - 1, 20).round().astype(int),
+                                     [16383, 16384, 16387, 16388, 16391, S - 4, S - 3, S - 2, S - 1]]))
+    assert any(min(O.n_visible(int(t), r), N) > 4096 for t in rows)
+    if keys == "all_zero":
+        for t in rows:
+            assert np.array_equal(gi[t], np.arange(K)), t
+            assert np.all(gs[t] == 0.0), t
+        return
+    q64, k64, w64 = np64(iqp)[0], np64(ikey)[0], np64(w)[0]
+    c = O.indexer_scale(Hi, Di)
+    sc = O.indexer_scores(q64[None, rows], k64[None], w64[None, rows], r, rows=rows, rows_only=True)[0]
+    swaps = check_topk_rows(gi[rows], sc, q64, k64, w64, r, K, rows, c)
+    assert swaps <= 2
+    for i, t in enumerate(rows):
+        kept = gi[t][gi[t] >= 0]
+        assert len(kept) == K and np.all(np.diff(kept) > 0), t
+        band = 4 * (Di + Hi + 4) * 2.0 ** -24 * (np.abs(w64[t]) * c) @ (np.abs(q64[t]) @ np.abs(k64[kept]).T)
+        assert np.all(np.abs(gs[t] - sc[i, kept]) <= band + 1e-30), t
+
+
 def _mqa_case(p, mode, sink, seed=0):
     x, xd, f, fd = _setup(p, seed=seed, sink=sink)
     bf = p["dtype"] == "bf16"
