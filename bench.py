@@ -60,8 +60,28 @@ def layer_work(p):
     t = np.arange(S, dtype=np.int64)
     idx_pairs = int(((t + 1) // r).sum()) if (r > 0 and K > 0) else 0
     idx_flops = 2.0 * B * p["Hi"] * p["Di"] * idx_pairs
+    # the layer's algorithmic HBM bytes: its inputs read once (q, kv, the
+    # compressors' projections and scores, the indexer's queries and weights)
+    # and its outputs written once (o, the selection)
+    G = 1 + p["overlap"] if r > 0 else 0
+    layer_bytes = attn_bytes + B * S * D * 2 + 2 * B * S * G * D * 2
+    if r > 0 and K > 0:
+        Hi, Di = p["Hi"], p["Di"]
+        layer_bytes += B * S * Hi * Di * 2 + 2 * B * S * G * Di * 2 + B * S * Hi * 4 + B * S * K * 4
     return dict(attn_flops=attn_flops, attn_bytes=attn_bytes, attn_keys=keys * B,
-                idx_flops=idx_flops, idx_pairs=idx_pairs * B)
+                idx_flops=idx_flops, idx_pairs=idx_pairs * B,
+                layer_flops=attn_flops + idx_flops, layer_bytes=float(layer_bytes))
+
+
+def layer_roofline(name, w, kernel_ms, peaks):
+    """A whole layer against its roofline: the larger of its tensor time
+    (FLOPs at the bf16 peak) and its HBM time (algorithmic bytes at the copy
+    bandwidth), over the sum of the layer's kernel times."""
+    t_tc = w["layer_flops"] / (peaks["bf16"] * 1e12) * 1e3
+    t_hbm = w["layer_bytes"] / (peaks["hbm"] * 1e9) * 1e3
+    return {"layer": name, "bound": "tensor" if t_tc >= t_hbm else "hbm", "ms": round(kernel_ms, 4),
+            "bound_ms": round(max(t_tc, t_hbm), 4), "frac": round(max(t_tc, t_hbm) / kernel_ms, 4),
+            "flops": w["layer_flops"], "bytes": w["layer_bytes"]}
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch at
@@ -373,6 +393,12 @@ def run_ours(args):
             extra_roofs.append(indexer_unit(work["csa_bf16_16k"]["idx_flops"], a_ms, sum(tk) / len(tk),
                                             peaks["bf16"]))
 
+    layer_roofs = []
+    for name in work:
+        tot = sum(sum(v) for (n, k), v in per.items() if n == name)      # every launch of the profiled steps
+        if tot > 0:
+            layer_roofs.append(layer_roofline(name, work[name], tot / args.steps, peaks))
+
     e2e = run_e2e(args, layers, dev) if args.e2e_steps > 0 else None
 
     line = {
@@ -385,7 +411,7 @@ def run_ours(args):
                    "parallelism": "replicas" if ws_ > 1 else "single",
                    "l2": "no flush: inputs larger than L2 (q and o 1 GiB per layer)"},
         "clocks": clocks, "gpu_launches": launches, "device_status": status,
-        "roofline": roof, "roofline_other": extra_roofs, "kernels": kern,
+        "roofline": roof, "roofline_other": extra_roofs, "roofline_layers": layer_roofs, "kernels": kern,
         "e2e": e2e,
     }
     if graph_note:

@@ -436,31 +436,53 @@ indexer_prep_d128_kernel(const T* __restrict__ iq, const float2* __restrict__ cs
       }
     }
   }
-  // in-thread butterflies (element strides 1 .. 16: dim bits 1, 2, 4, 32, 64)
+  // in-thread butterflies (element strides 1 .. 16: dim bits 1, 2, 4, 32,
+  // 64): stride 1 in scalars, the others on element pairs with paired fp32
+  // adds (x - y as fma(y, -1, x), exact)
 #pragma unroll
-  for (int h = 1; h < kPer; h <<= 1) {
+  for (int k = 0; k < kPer; k += 2) {
+    const float a = e[k], b = e[k + 1];
+    e[k] = a + b;
+    e[k + 1] = a - b;
+  }
+  const float2 neg1 = make_float2(-1.f, -1.f);
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
+  for (int h = 2; h < kPer; h <<= 1) {
+#pragma unroll
+    for (int k = 0; k < kPer; k += 2) {
       if ((k & h) == 0) {
-        const float a = e[k], b = e[k + h];
-        e[k] = a + b;
-        e[k + h] = a - b;
+        const float2 x = make_float2(e[k], e[k + 1]), y = make_float2(e[k + h], e[k + h + 1]);
+        const float2 sum = __fadd2_rn(x, y), dif = __ffma2_rn(y, neg1, x);
+        e[k] = sum.x;
+        e[k + 1] = sum.y;
+        e[k + h] = dif.x;
+        e[k + h + 1] = dif.y;
       }
     }
   }
-  // cross-lane butterflies (dim bits 8, 16)
+  // cross-lane butterflies (dim bits 8, 16): the lower lane keeps a + b, the
+  // upper a - b, both as fma(own, +-1, partner)
 #pragma unroll
   for (int hl = 1; hl < kLanes; hl <<= 1) {
-    const bool upper = (lane & hl) != 0;
+    const float sg = (lane & hl) ? -1.f : 1.f;
+    const float2 sg2 = make_float2(sg, sg);
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const float other = __shfl_xor_sync(0xffffffffu, e[k], hl);
-      e[k] = upper ? (other - e[k]) : (e[k] + other);
+    for (int k = 0; k < kPer; k += 2) {
+      const float2 other = make_float2(__shfl_xor_sync(0xffffffffu, e[k], hl),
+                                       __shfl_xor_sync(0xffffffffu, e[k + 1], hl));
+      const float2 r = __ffma2_rn(make_float2(e[k], e[k + 1]), sg2, other);
+      e[k] = r.x;
+      e[k + 1] = r.y;
     }
   }
   const float hs = 1.0f / sqrtf((float)Di);
+  const float2 hs2 = make_float2(hs, hs);
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) e[k] *= hs;
+  for (int k = 0; k < kPer; k += 2) {
+    const float2 r = __fmul2_rn(make_float2(e[k], e[k + 1]), hs2);
+    e[k] = r.x;
+    e[k + 1] = r.y;
+  }
   if constexpr (kCodes) {
     float amax = 0.f;
 #pragma unroll

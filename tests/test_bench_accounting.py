@@ -32,3 +32,23 @@ def test_flop_totals_at_the_benchmark_sizes():
     assert abs(hca["attn_flops"] / 1e12 - 0.4092) < 1e-3
     assert abs(csa["idx_flops"] / 1e12 - 0.5497) < 1e-3         # 0.550 TFLOP per indexer launch
     assert csa["attn_bytes"] == hca["attn_bytes"] == 2 * 16384 * H * D * 2
+
+
+def test_layer_rooflines_at_the_benchmark_sizes():
+    """The CSA layer is tensor-bound and the HCA layer HBM-bound at S=16384
+    (q + o dominate HCA's bytes: 2.15 GB against 0.41 TFLOP); a layer that
+    runs exactly at its bound reads 1.0."""
+    peaks = {"bf16": 1932.6, "hbm": 6779.0}
+    csa = bench.layer_work(SI.preset("csa_bf16_16k"))
+    hca = bench.layer_work(SI.preset("hca_bf16_16k"))
+    S, H, D, Hi, Di, K = 16384, 64, 512, 64, 128, 512
+    # inputs read once and outputs written once; CSA adds its indexer's
+    assert hca["layer_bytes"] == 2 * S * H * D * 2 + S * D * 2 + 2 * S * D * 2
+    assert csa["layer_bytes"] == (2 * S * H * D * 2 + S * D * 2 + 2 * S * 2 * D * 2
+                                  + S * Hi * Di * 2 + 2 * S * 2 * Di * 2 + S * Hi * 4 + S * K * 4)
+    rc = bench.layer_roofline("csa", csa, 10.0, peaks)
+    rh = bench.layer_roofline("hca", hca, 10.0, peaks)
+    assert rc["bound"] == "tensor" and rh["bound"] == "hbm"
+    assert abs(rc["bound_ms"] - csa["layer_flops"] / 1932.6e12 * 1e3) < 1e-4
+    at_bound = bench.layer_roofline("hca", hca, hca["layer_bytes"] / 6779e9 * 1e3, peaks)
+    assert abs(at_bound["frac"] - 1.0) < 1e-3
