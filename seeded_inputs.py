@@ -147,6 +147,21 @@ def make_entries(p, device="cpu", seed=3):
     return _unit_rms(_normal((p["B"], N, p["D"]), g, device)).to(torch_dtype(p))
 
 
+def make_indexer_operands(p, device="cpu", seed=11):
+    """Stand-in for the prepared indexer queries, the index keys and the head
+    weights when the selection is tested alone: unit-RMS N(0,1) rows
+    iq~ [B,S,Hi,Di] and ikey [B,S//ratio,Di] in the storage dtype, and
+    w ~ N(0,1) [B,S,Hi] in float32, drawn in that order."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    B, S, Hi, Di = p["B"], p["S"], p["Hi"], p["Di"]
+    dt = torch_dtype(p)
+    iqp = _unit_rms(_normal((B, S, Hi, Di), g, device)).to(dt)
+    ikey = _unit_rms(_normal((B, S // p["ratio"], Di), g, device)).to(dt)
+    w = _normal((B, S, Hi), g, device)
+    return iqp, ikey, w
+
+
 def make_output_grad(p, device="cpu", seed=2):
     """Gradient of the attention output for the backward: unit-RMS rows of
     N(0,1), [B,S,H,D] in the preset's storage dtype."""

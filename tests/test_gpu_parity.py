@@ -206,10 +206,7 @@ def test_topk_rows_longer_than_shared_memory(keys):
     p = SI.preset("csa_bf16_4k", S=20004, q_mode="direct")
     B, S, K, r, Hi, Di = p["B"], p["S"], p["K"], p["ratio"], p["Hi"], p["Di"]
     N = S // r
-    g = torch.Generator().manual_seed(11)
-    iqp = SI._unit_rms(SI._normal((B, S, Hi, Di), g, "cpu")).to(torch.bfloat16)
-    ikey = SI._unit_rms(SI._normal((B, N, Di), g, "cpu")).to(torch.bfloat16)
-    w = SI._normal((B, S, Hi), g, "cpu")
+    iqp, ikey, w = SI.make_indexer_operands(p, "cpu", seed=11)
     if keys == "all_zero":
         ikey.zero_()
     cfg = V.config_from_preset(p)
