@@ -4,9 +4,11 @@
 One step = one CSA layer forward plus one HCA layer forward (the repeating
 pair of the Flash stack), B=1, S=16384, 64 heads, 512-d latent, bf16, inputs
 resident in HBM (q and o alone are 1 GiB each per layer, far above the 129 MB
-L2, so no flush is needed).  value = tokens through the pair per second, over
-all ranks; each rank runs its own sequence (weak scaling, no collective on the
-data path).
+L2, so no flush is needed).  value = tokens through the pair per second.
+With N GPUs (``--gpus N``, one rank per GPU) the sequence's query rows are
+split zig-zag across the ranks, balanced by per-row cost; every rank holds the
+whole key/value prefix and computes only its rows (strong scaling, no
+collective on the data path).
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on a
 bounded sample of the same workload instead.
@@ -44,30 +46,38 @@ def n_visible(t, r):
     return (t + 1) // r if r > 0 else 0
 
 
-def attention_keys_total(S, r, K, W):
-    t = np.arange(S, dtype=np.int64)
-    nv = (t + 1) // r if r > 0 else np.zeros(S, dtype=np.int64)
+def attention_keys_total(S, r, K, W, lo=0, hi=None):
+    """Keys read by the query positions lo..hi-1 (default all S)."""
+    t = np.arange(lo, S if hi is None else hi, dtype=np.int64)
+    nv = (t + 1) // r if r > 0 else np.zeros(len(t), dtype=np.int64)
     ne = np.minimum(nv, K) if K > 0 else nv
     nw = np.minimum(t + 1, W) if W >= 0 else t + 1
     return int((ne + nw).sum())
 
 
-def layer_work(p):
+def layer_work(p, chunks=None):
+    """Algorithmic work of one layer over the query positions in `chunks`
+    (a list of [a, b) ranges; default the whole sequence).  A chunk's call
+    reads the sequence side (kv, the compressors' inputs) up to its end."""
     B, S, H, D, r, K, W = p["B"], p["S"], p["H"], p["D"], p["ratio"], p["K"], p["W"]
-    keys = attention_keys_total(S, r, K, W)
+    chunks = [(0, S)] if chunks is None else chunks
+    keys = sum(attention_keys_total(S, r, K, W, a, b) for a, b in chunks)
+    rows = sum(b - a for a, b in chunks)
     attn_flops = 4.0 * B * H * D * keys
-    attn_bytes = 2.0 * B * S * H * D * 2            # q read + o written (bf16)
-    t = np.arange(S, dtype=np.int64)
-    idx_pairs = int(((t + 1) // r).sum()) if (r > 0 and K > 0) else 0
+    attn_bytes = 2.0 * B * rows * H * D * 2          # q read + o written (bf16)
+    idx_pairs = 0
+    if r > 0 and K > 0:
+        idx_pairs = sum(int(((np.arange(a, b, dtype=np.int64) + 1) // r).sum()) for a, b in chunks)
     idx_flops = 2.0 * B * p["Hi"] * p["Di"] * idx_pairs
     # the layer's algorithmic HBM bytes: its inputs read once (q, kv, the
     # compressors' projections and scores, the indexer's queries and weights)
     # and its outputs written once (o, the selection)
     G = 1 + p["overlap"] if r > 0 else 0
-    layer_bytes = attn_bytes + B * S * D * 2 + 2 * B * S * G * D * 2
+    prefix = sum(b for _, b in chunks)               # sequence-side tokens read by the calls
+    layer_bytes = attn_bytes + B * prefix * D * 2 + 2 * B * prefix * G * D * 2
     if r > 0 and K > 0:
         Hi, Di = p["Hi"], p["Di"]
-        layer_bytes += B * S * Hi * Di * 2 + 2 * B * S * G * Di * 2 + B * S * Hi * 4 + B * S * K * 4
+        layer_bytes += B * rows * Hi * Di * 2 + 2 * B * prefix * G * Di * 2 + B * rows * Hi * 4 + B * rows * K * 4
     return dict(attn_flops=attn_flops, attn_bytes=attn_bytes, attn_keys=keys * B,
                 idx_flops=idx_flops, idx_pairs=idx_pairs * B,
                 layer_flops=attn_flops + idx_flops, layer_bytes=float(layer_bytes))
@@ -85,13 +95,18 @@ def layer_roofline(name, w, kernel_ms, peaks):
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch at
-# S=16384, from the ncu capture summarised in profiles/dram_traffic_s16384.md.
-# A figure is reported only while its kernel source is unchanged (sha256).
+# S=16384, from one ncu capture of each kernel.  A figure is reported only
+# while its kernel source is unchanged (sha256).
 NCU_TRAFFIC = {
     "csa_attention": ("mqa_tc.cu", "9d14665343ab875b9a9c974edb5cd0a8594cd8a6f8a360ca40ded6bfa03ef2ff", 2162648832),
     "hca_attention": ("mqa_tc.cu", "9d14665343ab875b9a9c974edb5cd0a8594cd8a6f8a360ca40ded6bfa03ef2ff", 2121747968),
     "csa_indexer": ("indexer_tc.cu", "f649d2ee00405a246972c64eaac6e25974ae18b5f9dabc20e18c441ef48084c2", 398966784),
 }
+
+
+TRAFFIC_SOURCE = ("dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture of the "
+                  "same kernel source at S=16384 (a constant keyed to the source hash, not measured in this run; "
+                  "null when the kernel changed since)")
 
 
 def ncu_traffic(key, seq):
@@ -256,6 +271,63 @@ def run_layer(L, stream=None):
     V.v4_attn_layer_fwd(L["cfg"], L["x"], L["outs"], L["ws"], stream)
 
 
+ROW_INPUTS = ("q", "iq", "w")                           # one row per query position
+SEQ_INPUTS = ("kv", "ckv", "cscore", "ickv", "icscore")  # one row per token of the sequence
+
+
+def slice_layer(L, a, b):
+    """The call of layer L over query positions [a, b): its own copies of
+    the row inputs, the sequence inputs up to token b-1 (causality), its own
+    outputs and workspace.  [0, S) is the layer itself."""
+    import torch
+
+    import sparse_compressed_attention_gb300 as V
+    p = L["p"]
+    if (a, b) == (0, p["S"]):
+        return dict(L, chunk=(a, b))
+    cfg = V.config_from_preset(p, S=b, q_begin=a, indexer_fp8=L["cfg"].indexer_fp8)
+    x = {}
+    for k, v in L["x"].items():
+        if v is not None and k in ROW_INPUTS:
+            x[k] = v[:, a:b].clone()             # own allocation: 16-byte aligned
+        elif v is not None and k in SEQ_INPUTS:
+            x[k] = v[:, :b].contiguous()
+        else:
+            x[k] = v
+    B, H, dev = p["B"], p["H"], x["q"].device
+    outs = {"o": torch.empty(B, b - a, H, p["D"], dtype=x["q"].dtype, device=dev),
+            "lse": torch.empty(B, b - a, H, device=dev)}
+    if p["K"] > 0:
+        outs["idx"] = torch.empty(B, b - a, p["K"], dtype=torch.int32, device=dev)
+    return dict(name=L["name"], p=p, x=x, outs=outs, cfg=cfg, ws=V.alloc_workspace(cfg, dev), chunk=(a, b))
+
+
+def rank_chunks(p, world, rank, split="contiguous"):
+    """This rank's query positions of one layer, balanced by the layer's
+    per-row cost: one contiguous range, or the zig-zag pair of chunks (the
+    whole sequence at N=1)."""
+    from sparse_compressed_attention_gb300 import rows as R
+    cost = R.layer_cost(p["ratio"], p["K"], p["W"], heads=p["H"], dim=p["D"], idx_heads=p["Hi"], idx_dim=p["Di"])
+    if world == 1:
+        return [(0, p["S"])]
+    if split == "zigzag":
+        return R.zigzag_chunks(p["S"], world, rank, cost)
+    return R.contiguous_chunks(p["S"], world, rank, cost)
+
+
+def relaunch_under_torchrun(args):
+    """`--gpus N` without a launcher: start N ranks on this node (one per GPU)
+    with torch.distributed.run and return its exit code."""
+    import socket
+    sock = socket.socket()
+    sock.bind(("127.0.0.1", 0))
+    port = sock.getsockname()[1]
+    sock.close()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=%d" % args.gpus,
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -272,8 +344,20 @@ def run_ours(args):
     barrier()
     V.lib()
     S = args.seq
-    layers = [make_layer("csa_bf16_16k", S, dev, seed=1000 + 2 * rank),
-              make_layer("hca_bf16_16k", S, dev, seed=1001 + 2 * rank)]
+    # one sequence, the same inputs on every rank; each rank computes its
+    # zig-zag share of the query rows of each layer against the whole prefix
+    full = [make_layer("csa_bf16_16k", S, dev, seed=1000), make_layer("hca_bf16_16k", S, dev, seed=1001)]
+    # --shard-of r/n (one process): time rank r's rows of an n-GPU split alone
+    split_world, split_rank = ws_, rank
+    if args.shard_of:
+        split_rank, split_world = (int(v) for v in args.shard_of.split("/"))
+        if ws_ > 1 or not 0 <= split_rank < split_world:
+            raise SystemExit("--shard-of r/n needs one process and 0 <= r < n")
+    chunks_of = {L["name"]: rank_chunks(L["p"], split_world, split_rank, args.split) for L in full}
+    layers = [slice_layer(L, a, b) for L in full for a, b in chunks_of[L["name"]]]
+    if split_world > 1:
+        for L in full:                       # the whole-sequence outputs are not used by a rank
+            L["outs"] = None
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
         for L in layers:
@@ -341,7 +425,8 @@ def run_ours(args):
     status = V.v4_get_device_status()
 
     # per-kernel durations from the live event records (of the timed region
-    # itself when the step runs eagerly)
+    # itself when the step runs eagerly); a kernel's time per step sums its
+    # launches over this rank's row chunks of the layer
     recs = V.v4_profile_records()
     per = {}
     start = 0
@@ -352,46 +437,63 @@ def run_ours(args):
     kern = {"%s/%s" % k: {"launches": len(v), "avg_ms": sum(v) / len(v), "total_ms": sum(v)}
             for k, v in per.items()}
 
-    tokens_rank = sum(L["p"]["B"] * L["p"]["S"] for L in layers[:1])   # tokens through the pair
+    def per_step_ms(key):
+        v = per.get(key, [])
+        return sum(v) / args.steps if v else None
+
+    # tokens through the layer pair: this rank's rows (each layer's chunks
+    # cover the sequence once over all ranks)
+    rows = {n: sum(b - a for a, b in ch) for n, ch in chunks_of.items()}
+    tokens_rank = full[0]["p"]["B"] * (rows["csa_bf16_16k"] + rows["hca_bf16_16k"]) / 2.0
     tokens = sum_over_ranks(tokens_rank * args.steps, dev)
     value = tokens / (ms / 1e3)
 
     peaks = load_peaks()
-    work = {L["name"]: layer_work(L["p"]) for L in layers}
-    csa_attn = per.get(("csa_bf16_16k", "attention"), [])
-    hca_attn = per.get(("hca_bf16_16k", "attention"), [])
+    work = {L["name"]: layer_work(L["p"], chunks_of[L["name"]]) for L in full}
+    nlaunch = {n: len(ch) for n, ch in chunks_of.items()}
     roof = None
-    if csa_attn:
-        a_ms = sum(csa_attn) / len(csa_attn)
+    a_ms = per_step_ms(("csa_bf16_16k", "attention"))
+    if a_ms:
         achieved = work["csa_bf16_16k"]["attn_flops"] / (a_ms / 1e3) / 1e12
         roof = {"kernel": "csa attention (sparse MQA, 64 heads x 512, top-512 + window 128)",
                 "bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16"],
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4),
-                "traffic": ncu_traffic("csa_attention", S),
+                "traffic": ncu_traffic("csa_attention", S) if ws_ == 1 else None,
+                "traffic_source": TRAFFIC_SOURCE,
                 "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % peaks["src"],
-                "flops_per_launch": work["csa_bf16_16k"]["attn_flops"], "avg_launch_ms": round(a_ms, 4)}
+                "flops_per_launch": work["csa_bf16_16k"]["attn_flops"] / nlaunch["csa_bf16_16k"],
+                "avg_launch_ms": round(a_ms / nlaunch["csa_bf16_16k"], 4),
+                "launches_per_step": nlaunch["csa_bf16_16k"]}
     extra_roofs = []
-    if hca_attn:
-        a_ms = sum(hca_attn) / len(hca_attn)
+    a_ms = per_step_ms(("hca_bf16_16k", "attention"))
+    if a_ms:
         gbs = work["hca_bf16_16k"]["attn_bytes"] / (a_ms / 1e3) / 1e9
         extra_roofs.append({"kernel": "hca attention", "bound": "hbm", "achieved": round(gbs, 1),
                             "peak": peaks["hbm"], "unit": "GB/s", "frac": round(gbs / peaks["hbm"], 4),
-                            "traffic": ncu_traffic("hca_attention", S),
-                            "bytes_per_launch": work["hca_bf16_16k"]["attn_bytes"],
-                            "avg_launch_ms": round(a_ms, 4)})
-    isc = per.get(("csa_bf16_16k", "indexer_scores"), [])
-    if isc:
-        a_ms = sum(isc) / len(isc)
-        tf = work["csa_bf16_16k"]["idx_flops"] / (a_ms / 1e3) / 1e12
+                            "traffic": ncu_traffic("hca_attention", S) if ws_ == 1 else None,
+                            "traffic_source": TRAFFIC_SOURCE,
+                            "bytes_per_launch": work["hca_bf16_16k"]["attn_bytes"] / nlaunch["hca_bf16_16k"],
+                            "avg_launch_ms": round(a_ms / nlaunch["hca_bf16_16k"], 4),
+                            "launches_per_step": nlaunch["hca_bf16_16k"]})
+    s_ms = per_step_ms(("csa_bf16_16k", "indexer_scores"))
+    if s_ms:
+        tf = work["csa_bf16_16k"]["idx_flops"] / (s_ms / 1e3) / 1e12
         extra_roofs.append({"kernel": "csa indexer scores", "bound": "tensor", "achieved": round(tf, 2),
                             "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": round(tf / peaks["bf16"], 4),
-                            "traffic": ncu_traffic("csa_indexer", S),
-                            "flops_per_launch": work["csa_bf16_16k"]["idx_flops"],
-                            "avg_launch_ms": round(a_ms, 4)})
-        tk = per.get(("csa_bf16_16k", "topk"), [])
+                            "traffic": ncu_traffic("csa_indexer", S) if ws_ == 1 else None,
+                            "traffic_source": TRAFFIC_SOURCE,
+                            "flops_per_launch": work["csa_bf16_16k"]["idx_flops"] / nlaunch["csa_bf16_16k"],
+                            "avg_launch_ms": round(s_ms / nlaunch["csa_bf16_16k"], 4)})
+        tk = per_step_ms(("csa_bf16_16k", "topk"))
         if tk:
-            extra_roofs.append(indexer_unit(work["csa_bf16_16k"]["idx_flops"], a_ms, sum(tk) / len(tk),
-                                            peaks["bf16"]))
+            extra_roofs.append(indexer_unit(work["csa_bf16_16k"]["idx_flops"], s_ms, tk, peaks["bf16"]))
+            pr = per_step_ms(("csa_bf16_16k", "indexer_prep"))
+            if pr:
+                u = indexer_unit(work["csa_bf16_16k"]["idx_flops"], s_ms + pr, tk, peaks["bf16"])
+                u["kernel"] = "csa indexer unit with its query prep (prep + scores + top-k)"
+                u["prep_ms"] = round(pr, 4)
+                u["scores_ms"] = round(s_ms, 4)
+                extra_roofs.append(u)
 
     layer_roofs = []
     for name in work:
@@ -399,16 +501,19 @@ def run_ours(args):
         if tot > 0:
             layer_roofs.append(layer_roofline(name, work[name], tot / args.steps, peaks))
 
-    e2e = run_e2e(args, layers, dev) if args.e2e_steps > 0 else None
+    e2e = run_e2e(args, layers, dev, tokens_rank) if args.e2e_steps > 0 else None
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws_,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; activations unit-RMS N(0,1), q from a random rank-1024 path)",
-        "config": {"workload": workload(S), "global_batch": ws_, "seq_len": S, "layers_per_step": 2,
+        "config": {"workload": workload(S), "global_batch": 1, "seq_len": S, "layers_per_step": 2,
                    "cuda_graph": graph is not None,
-                   "parallelism": "replicas" if ws_ > 1 else "single",
+                   "parallelism": ("query rows of one sequence split over %d GPUs (%s, cost-balanced), "
+                                   "no collective on the data path" % (ws_, args.split)) if ws_ > 1 else "single",
+                   "rank0_chunks": {n: [list(c) for c in ch] for n, ch in chunks_of.items()},
+                   "shard_of": args.shard_of or None,
                    "l2": "no flush: inputs larger than L2 (q and o 1 GiB per layer)"},
         "clocks": clocks, "gpu_launches": launches, "device_status": status,
         "roofline": roof, "roofline_other": extra_roofs, "roofline_layers": layer_roofs, "kernels": kern,
@@ -417,14 +522,14 @@ def run_ours(args):
     if graph_note:
         line["note"] = graph_note
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args, layers)
+        line["cpu_baseline"] = cpu_baseline(args, full)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws_ > 1:
         dist.destroy_process_group()
 
 
-def run_e2e(args, layers, dev):
+def run_e2e(args, layers, dev, tokens_rank):
     """Same step through the C ABI with inputs in pinned host memory: every
     step copies every input of both layers host->device and each layer's
     output o device->host.  Copies in and out run on their own streams and
@@ -486,7 +591,7 @@ def run_e2e(args, layers, dev):
     e1.record(comp)
     torch.cuda.synchronize(dev)
     ms = max_over_ranks(e0.elapsed_time(e1), dev)
-    tokens = sum_over_ranks(layers[0]["p"]["B"] * layers[0]["p"]["S"] * n, dev)
+    tokens = sum_over_ranks(tokens_rank * n, dev)
     return {"value": round(tokens / (ms / 1e3), 1), "unit": "tokens/s", "steps": n,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "overlap": "copies in and out on their own streams, overlapping the other layer's compute"}
@@ -825,6 +930,11 @@ def cpu_baseline(args, layers):
 # Reference arm: the CPU oracle as the comparison program
 # ---------------------------------------------------------------------------
 def run_reference(args):
+    """The CPU oracle as the comparison program, on the same workload.  One
+    step = the oracle on a bounded sample (the full compressors of both layers
+    and the indexer and attention of --ref-rows evenly spaced query rows per
+    layer, as cpu_baseline samples them); ms_per_step is the measured time of
+    that sample, value the whole-sequence throughput extrapolated from it."""
     import torch
 
     import seeded_inputs as SI
@@ -844,21 +954,24 @@ def run_reference(args):
     inputs = gather_oracle_inputs(layers, args.ref_rows)
     for _ in range(args.warmup):
         oracle_sample(inputs, args.ref_rows)
-    ests = []
-    spent = 0.0
+    ests, spent = [], []
     for _ in range(args.steps):
-        e, s = oracle_sample(inputs, args.ref_rows)
+        e, sp = oracle_sample(inputs, args.ref_rows)
         ests.append(e)
-        spent += s
+        spent.append(sp)
     est = sum(ests) / len(ests)
     value = S / est
+    sample = ("numpy float64 oracle per step: full compressors of both layers + indexer/attention for %d evenly "
+              "spaced query rows per layer (the rows cpu_baseline samples), extrapolated to S=%d"
+              % (args.ref_rows, S))
     cb = {"value": round(value, 2), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-          "sample": "numpy float64 oracle per step: full compressors + indexer/attention for %d query "
-                    "rows per layer, extrapolated to S=%d" % (args.ref_rows, S)}
+          "sample": sample}
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
             "n_gpus": ws_, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(est * 1e3, 1), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "ms_per_step": round(1e3 * sum(spent) / len(spent), 1), "extrapolated": True,
+            "extrapolated_ms_per_step": round(est * 1e3, 1), "sample_rows_per_layer": args.ref_rows,
+            "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
             "config": {"workload": workload(S), "global_batch": 1, "seq_len": S, "layers_per_step": 2},
             "cpu_baseline": cb,
             "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -876,9 +989,13 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-rows", type=int, default=64)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--ref-rows", type=int, default=6)
+    ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager calls instead of a captured step")
+    ap.add_argument("--split", choices=["contiguous", "zigzag"], default="contiguous",
+                    help="N > 1: how the query rows of the sequence are split (both balanced by per-row cost)")
+    ap.add_argument("--shard-of", default="", help="r/n: one process times rank r's query rows of an n-GPU "
+                                                   "split (value then counts only those rows)")
     ap.add_argument("--indexer-fp8", type=int, choices=[0, 1], default=0,
                     help="--workload csa: opt-in E4M3 indexer QK (the default keeps bf16 operands)")
     ap.add_argument("--workload", choices=["pair", "stack", "csa", "pro", "qproj", "kl"], default="pair",
@@ -887,6 +1004,8 @@ def main():
                          "pro: the pair with 128 heads and top-1024; qproj: the rank-1024 query projections; "
                          "kl: the indexer distillation target of the CSA layer")
     args = ap.parse_args()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ and args.impl == "ours" and args.workload == "pair":
+        sys.exit(relaunch_under_torchrun(args))
     if args.impl == "reference":
         run_reference(args)
     elif args.workload == "qproj":

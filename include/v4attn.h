@@ -13,8 +13,10 @@
  * Conventions shared by every entry point
  *   - Tensors are dense, row-major, in device memory owned by the caller.
  *     The library never allocates device memory; scratch space is the
- *     caller's workspace (see v4_workspace_size).  Every device pointer must
- *     be 16-byte aligned.
+ *     caller's workspace (see v4_workspace_size).  One exception:
+ *     v4_sparse_mqa_fwd_noalloc keeps its scratch in a library-owned static
+ *     device array (see its section).  Every device pointer must be 16-byte
+ *     aligned.
  *   - "Storage dtype" (cfg->dtype) is the element type of q, kv, the pooling
  *     projections, entries, indexer keys/queries and the output: V4_F32 or
  *     V4_BF16.  ape, norm weights, indexer weights w, sink, inv_freq, lse
@@ -84,6 +86,18 @@ typedef struct v4_config {
   int32_t path;           /* v4_path */
   int32_t indexer_fp8;    /* 1 = opt-in E4M3 indexer QK (see v4_indexer_topk_e4m3);
                              0 = bf16 operands, fp32 scoring (the default [PR] item 4 asks for) */
+  int32_t q_begin;        /* first query position of the call, 0 <= q_begin < seqlen (0 = all).
+                             The call computes queries q_begin .. seqlen-1 of every sequence
+                             against the whole causal prefix: [BLOG] "Three attention types,
+                             interleaved" gives each query its own keys (selected entries and
+                             window), so query rows are independent given the prefix.  Row
+                             tensors (q, iq, w, o, lse, idx, iscore, y; Sq = seqlen - q_begin
+                             rows per sequence, row i = position q_begin + i) hold only these
+                             rows; sequence tensors (kv, ckv, cscore, ickv, icscore, entries,
+                             indexer keys) hold all seqlen positions.  A chunk [a, b) of a
+                             sequence is the call with seqlen = b and q_begin = a: causality
+                             means it needs no token past b-1.  The backward and the indexer
+                             distillation target take q_begin = 0 only (V4_ERR_UNSUPPORTED). */
 } v4_config;
 
 /* ----------------------------------------------------------------------

@@ -45,7 +45,7 @@ class v4_config(C.Structure):
         "batch", "seqlen", "n_heads", "head_dim", "rope_dim", "ratio", "overlap", "window", "topk",
         "idx_heads", "idx_dim", "o_groups", "o_rank")] + [
         ("softmax_scale", C.c_float), ("rms_eps", C.c_float), ("dtype", C.c_int32), ("path", C.c_int32),
-        ("indexer_fp8", C.c_int32)]
+        ("indexer_fp8", C.c_int32), ("q_begin", C.c_int32)]
 
 
 class v4_layer_inputs(C.Structure):
@@ -115,9 +115,11 @@ def _check(status):
 
 def make_config(B, S, H, D, R, ratio=0, overlap=0, window=128, topk=0, Hi=64, Di=128,
                 o_groups=8, o_rank=1024, scale=0.0, eps=1e-6, dtype="bf16", path=V4_PATH_AUTO,
-                indexer_fp8=0):
+                indexer_fp8=0, q_begin=0):
+    """v4_config; q_begin > 0 restricts the call to query positions q_begin..S-1
+    (row tensors then hold S - q_begin rows per sequence)."""
     return v4_config(B, S, H, D, R, ratio, overlap, window, topk, Hi, Di, o_groups, o_rank,
-                     scale, eps, V4_BF16 if dtype == "bf16" else V4_F32, path, int(indexer_fp8))
+                     scale, eps, V4_BF16 if dtype == "bf16" else V4_F32, path, int(indexer_fp8), int(q_begin))
 
 
 def config_from_preset(p, **over):
@@ -126,7 +128,7 @@ def config_from_preset(p, **over):
     return make_config(q["B"], q["S"], q["H"], q["D"], q["R"], q["ratio"], q["overlap"], q["W"],
                        q["K"], q["Hi"], q["Di"], dtype=q["dtype"], path=q.get("path", V4_PATH_AUTO),
                        eps=q.get("eps", 1e-6), scale=q.get("scale", 0.0),
-                       indexer_fp8=q.get("indexer_fp8", 0))
+                       indexer_fp8=q.get("indexer_fp8", 0), q_begin=q.get("q_begin", 0))
 
 
 def _storage(cfg):
@@ -177,14 +179,14 @@ def v4_compress(cfg, ckv, cscore, ape, norm_w, inv_freq, dim, hadamard, out, str
     _check(lib().v4_compress(C.byref(cfg), _ptr(ckv, "ckv", dt), _ptr(cscore, "cscore", dt),
                              _ptr(ape, "ape", torch.float32),
                              _ptr(norm_w, "norm_w", torch.float32, optional=True),
-                             _ptr(inv_freq, "inv_freq", torch.float32), int(dim), int(hadamard),
+                             _ptr(inv_freq, "inv_freq", torch.float32, optional=cfg.rope_dim == 0), int(dim), int(hadamard),
                              _ptr(out, "out", dt, optional=out is None), _stream(stream)))
     return out
 
 
 def v4_indexer_prep(cfg, iq, inv_freq, iq_prep, stream=None):
     dt = _storage(cfg)
-    _check(lib().v4_indexer_prep(C.byref(cfg), _ptr(iq, "iq", dt), _ptr(inv_freq, "inv_freq", torch.float32),
+    _check(lib().v4_indexer_prep(C.byref(cfg), _ptr(iq, "iq", dt), _ptr(inv_freq, "inv_freq", torch.float32, optional=cfg.rope_dim == 0),
                                  _ptr(iq_prep, "iq_prep", dt), _stream(stream)))
     return iq_prep
 
@@ -228,7 +230,7 @@ def v4_sparse_mqa_fwd(cfg, q, kv, ent, idx, sink, inv_freq, o, lse, workspace, s
                                    _ptr(ent, "ent", dt, optional=True),
                                    _ptr(idx, "idx", torch.int32, optional=True),
                                    _ptr(sink, "sink", torch.float32, optional=True),
-                                   _ptr(inv_freq, "inv_freq", torch.float32),
+                                   _ptr(inv_freq, "inv_freq", torch.float32, optional=cfg.rope_dim == 0),
                                    _ptr(o, "o", dt), _ptr(lse, "lse", torch.float32, optional=True),
                                    _ptr(workspace, "workspace", torch.uint8), workspace.numel(),
                                    _stream(stream)))
@@ -242,7 +244,7 @@ def v4_sparse_mqa_fwd_noalloc(cfg, q, kv, ent, idx, sink, inv_freq, o, lse, stre
                                            _ptr(ent, "ent", dt, optional=True),
                                            _ptr(idx, "idx", torch.int32, optional=True),
                                            _ptr(sink, "sink", torch.float32, optional=True),
-                                           _ptr(inv_freq, "inv_freq", torch.float32),
+                                           _ptr(inv_freq, "inv_freq", torch.float32, optional=cfg.rope_dim == 0),
                                            _ptr(o, "o", dt), _ptr(lse, "lse", torch.float32, optional=True),
                                            _stream(stream)))
     return o

@@ -92,6 +92,14 @@ struct ProfScope {
   }
 };
 
+StageTiming::StageTiming(int kind, cudaStream_t st) : rec_(nullptr), st_(st) {
+  ProfScope* ps = new ProfScope(kind, st);
+  if (ps->on) rec_ = ps;
+  else delete ps;
+}
+
+StageTiming::~StageTiming() { delete static_cast<ProfScope*>(rec_); }
+
 static void prof_clear() {
   for (auto& r : g_prof) {
     cudaEventDestroy(r.a);
@@ -106,6 +114,7 @@ Workspace plan_workspace(const v4_config& c) {
   Workspace w;
   const size_t es = c.dtype == V4_BF16 ? 2 : 4;
   const size_t B = c.batch, S = c.seqlen, D = c.head_dim;
+  const size_t Sq = (size_t)q_rows(c);            // query rows of the call
   const size_t N = c.ratio > 0 ? S / c.ratio : 0;
   const bool sel = c.topk > 0 && c.ratio > 0;
   size_t off = 0;
@@ -118,16 +127,16 @@ Workspace plan_workspace(const v4_config& c) {
   take(w.ent, w.ent_bytes, B * N * D * es);
   take(w.ikey, w.ikey_bytes, sel ? B * N * c.idx_dim * es : 0);
   // bf16 prepared queries (the E4M3 path writes codes instead)
-  take(w.iqp, w.iqp_bytes, sel && !c.indexer_fp8 ? B * S * c.idx_heads * c.idx_dim * es : 0);
-  take(w.scores, w.scores_bytes, sel ? B * S * N * 4 : 0);
-  take(w.idx, w.idx_bytes, sel ? B * S * c.topk * 4 : 0);
+  take(w.iqp, w.iqp_bytes, sel && !c.indexer_fp8 ? B * Sq * c.idx_heads * c.idx_dim * es : 0);
+  take(w.scores, w.scores_bytes, sel ? B * Sq * N * 4 : 0);
+  take(w.idx, w.idx_bytes, sel ? B * Sq * c.topk * 4 : 0);
   take(w.knorm, w.knorm_bytes, key_norm_floats(c) * 4);
   // redo list: one entry per (query, 64-head slice) at most
-  take(w.counters, w.counters_bytes, (2 + B * S * (size_t)(c.n_heads > 64 ? (c.n_heads + 63) / 64 : 1)) * 4);
+  take(w.counters, w.counters_bytes, (2 + B * Sq * (size_t)(c.n_heads > 64 ? (c.n_heads + 63) / 64 : 1)) * 4);
   take(w.rope, w.rope_bytes, S * (size_t)(c.rope_dim / 2) * 8);
   const bool e4m3 = sel && c.indexer_fp8 == 1;
-  take(w.qc8, w.qc8_bytes, e4m3 ? B * S * c.idx_heads * c.idx_dim : 0);
-  take(w.qs8, w.qs8_bytes, e4m3 ? B * S * c.idx_heads * 4 : 0);
+  take(w.qc8, w.qc8_bytes, e4m3 ? B * Sq * c.idx_heads * c.idx_dim : 0);
+  take(w.qs8, w.qs8_bytes, e4m3 ? B * Sq * c.idx_heads * 4 : 0);
   take(w.kc8, w.kc8_bytes, e4m3 ? B * N * c.idx_dim : 0);
   take(w.ks8, w.ks8_bytes, e4m3 ? B * N * 4 : 0);
   w.total = off;
@@ -187,6 +196,8 @@ static v4_status check_cfg(const v4_config* c) {
   if (c->path < V4_PATH_AUTO || c->path > V4_PATH_TC) return fail(V4_ERR_INVALID_ARG, "unknown path");
   if (!(c->rms_eps >= 0.f)) return fail(V4_ERR_INVALID_ARG, "rms_eps must be >= 0");
   if (c->indexer_fp8 != 0 && c->indexer_fp8 != 1) return fail(V4_ERR_INVALID_ARG, "indexer_fp8 must be 0 or 1");
+  if (c->q_begin < 0 || c->q_begin >= c->seqlen)
+    return fail(V4_ERR_INVALID_ARG, "q_begin must be in [0, seqlen)");
   return V4_OK;
 }
 
@@ -251,7 +262,7 @@ static v4_status do_indexer(const v4_config& c, const void* iq, int prepared, co
     uint8_t* kc = (uint8_t*)(ws + plan.kc8);
     float* ks = (float*)(ws + plan.ks8);
     const long long N = c.seqlen / c.ratio;
-    const long long qrows = (long long)c.batch * c.seqlen * c.idx_heads;
+    const long long qrows = (long long)c.batch * q_rows(c) * c.idx_heads;
     if (!prepared) {
       ProfScope ps(K_IDX_PREP, st);
       CU(launch_indexer_prep_e4m3(c, iq, table, f, qc, qs, st), "indexer prep kernel (E4M3)");
@@ -520,6 +531,7 @@ v4_status v4_sparse_mqa_bwd(const v4_config* cfg, const void* q, const void* kv,
   v4_status s = check_cfg(cfg);
   if (s != V4_OK) return s;
   const v4_config& c = *cfg;
+  if (c.q_begin != 0) return fail(V4_ERR_UNSUPPORTED, "attention backward needs q_begin = 0");
   if (!mqa_bwd_tc_supported(c))
     return fail(V4_ERR_UNSUPPORTED,
                 "attention backward needs bf16, H a multiple of 64 up to 512, D=512, R=64, 1 <= W <= 128, K <= 1024");
@@ -617,6 +629,7 @@ v4_status v4_indexer_kl_target(const v4_config* cfg, const void* q, const void* 
   if (s != V4_OK) return s;
   const v4_config& c = *cfg;
   if (c.topk < 1 || c.ratio < 1) return fail(V4_ERR_INVALID_ARG, "the target needs a selection (topk >= 1, ratio >= 1)");
+  if (c.q_begin != 0) return fail(V4_ERR_UNSUPPORTED, "the distillation target needs q_begin = 0");
   if (!kl_target_tc_supported(c))
     return fail(V4_ERR_UNSUPPORTED, "the distillation target needs bf16, H a multiple of 64 up to 512, D=512, R=64, "
                                     "K <= 1024");
@@ -667,7 +680,7 @@ v4_status v4_q_proj(const v4_config* cfg, const void* qlat, int32_t rank, const 
   int* status = status_ptr();
   if (!status) return fail(V4_ERR_CUDA, "device status word unavailable");
   cudaStream_t st = (cudaStream_t)stream;
-  const long long T = (long long)c.batch * c.seqlen;
+  const long long T = (long long)c.batch * q_rows(c);          // the call's query rows
   ProfScope ps(K_QPROJ, st);
   CU(launch_qproj_tc(T, rank, qlat, wq, (int)nq, q, q_norm, c.rms_eps, q_norm ? q_norm_w : nullptr, status, st),
      "query projection kernel");

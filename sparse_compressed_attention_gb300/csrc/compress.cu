@@ -322,14 +322,14 @@ key_bounds_kernel(const float* __restrict__ kv_norm, const float* __restrict__ e
   }
 }
 
-// Indexer query prep: rows of Di elements (row = (b,t,h)), RoPE at t on the
-// last R dims, then the normalised Hadamard via butterflies: stages 1,2,4
+// Indexer query prep: rows of Di elements (row = (b, query row i, h) with
+// Sq query rows per sequence, position t = t0 + i), RoPE at t on the last R dims, then the normalised Hadamard via butterflies: stages 1,2,4
 // inside a thread's 8 elements, larger stages across the Di/8 lanes of the
 // row with warp shuffles.  Requires Di/8 <= 32.
 template <typename T>
 __global__ void indexer_prep_kernel(const T* __restrict__ iq, const float2* __restrict__ cs_table,
                                     const float* __restrict__ inv_freq, T* __restrict__ out,
-                                    long long rows, int S, int Hi, int Di, int R) {
+                                    long long rows, int Sq, int t0, int Hi, int Di, int R) {
   const int lanes = Di / 8;                                  // lanes per row (power of 2)
   const long long gt = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   const long long row = gt / lanes;
@@ -343,7 +343,7 @@ __global__ void indexer_prep_kernel(const T* __restrict__ iq, const float2* __re
   }
   const int c0 = lane * 8;
   if (live && c0 >= Di - R) {
-    const long long t = (row / Hi) % S;
+    const long long t = t0 + (row / Hi) % Sq;
     const int j0 = (c0 - (Di - R)) / 2;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -398,7 +398,7 @@ template <typename T, bool kCodes = false>
 __global__ void __launch_bounds__(256)
 indexer_prep_d128_kernel(const T* __restrict__ iq, const float2* __restrict__ cs_table,
                          const float* __restrict__ inv_freq, T* __restrict__ out,
-                         long long rows, int S, int Hi, int R, uint8_t* __restrict__ codes = nullptr,
+                         long long rows, int Sq, int t0, int Hi, int R, uint8_t* __restrict__ codes = nullptr,
                          float* __restrict__ scales = nullptr) {
   constexpr int Di = 128, kLanes = 4, kPer = 32;
   const long long gt = blockIdx.x * (long long)blockDim.x + threadIdx.x;
@@ -418,7 +418,7 @@ indexer_prep_d128_kernel(const T* __restrict__ iq, const float2* __restrict__ cs
     }
   }
   if (live) {
-    const long long t = (row / Hi) % S;
+    const long long t = t0 + (row / Hi) % Sq;
 #pragma unroll
     for (int k = 0; k < kPer / 2; ++k) {
       const int c = 32 * (k / 4) + 8 * lane + 2 * (k % 4);       // dim of e[2k]
@@ -737,27 +737,31 @@ cudaError_t launch_key_prep(const v4_config& c, const void* kv, const void* ent,
 cudaError_t launch_indexer_prep_e4m3(const v4_config& c, const void* iq, const float2* cs_table,
                                      const float* inv_freq, uint8_t* codes, float* scales, cudaStream_t st) {
   if (c.idx_dim != 128 || c.dtype != V4_BF16) return cudaErrorInvalidValue;
-  const long long rows = (long long)c.batch * c.seqlen * c.idx_heads;
+  const long long rows = (long long)c.batch * q_rows(c) * c.idx_heads;
+  if (rows == 0) return cudaSuccess;
   const int threads = 256;
   const long long blocks = (rows * 4 + threads - 1) / threads;
   indexer_prep_d128_kernel<bf16, true><<<(unsigned)blocks, threads, 0, st>>>(
-      (const bf16*)iq, cs_table, inv_freq, nullptr, rows, c.seqlen, c.idx_heads, c.rope_dim, codes, scales);
+      (const bf16*)iq, cs_table, inv_freq, nullptr, rows, q_rows(c), c.q_begin, c.idx_heads, c.rope_dim, codes,
+      scales);
   note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_indexer_prep(const v4_config& c, const void* iq, const float2* cs_table,
                                 const float* inv_freq, void* iqp, cudaStream_t st) {
-  const long long rows = (long long)c.batch * c.seqlen * c.idx_heads;
+  const long long rows = (long long)c.batch * q_rows(c) * c.idx_heads;
+  if (rows == 0) return cudaSuccess;
   const int threads = 256;
+  const int Sq = q_rows(c), t0 = c.q_begin;
   if (c.idx_dim == 128) {
     const long long blocks = (rows * 4 + threads - 1) / threads;
     if (c.dtype == V4_BF16)
       indexer_prep_d128_kernel<bf16><<<(unsigned)blocks, threads, 0, st>>>(
-          (const bf16*)iq, cs_table, inv_freq, (bf16*)iqp, rows, c.seqlen, c.idx_heads, c.rope_dim);
+          (const bf16*)iq, cs_table, inv_freq, (bf16*)iqp, rows, Sq, t0, c.idx_heads, c.rope_dim);
     else
       indexer_prep_d128_kernel<float><<<(unsigned)blocks, threads, 0, st>>>(
-          (const float*)iq, cs_table, inv_freq, (float*)iqp, rows, c.seqlen, c.idx_heads, c.rope_dim);
+          (const float*)iq, cs_table, inv_freq, (float*)iqp, rows, Sq, t0, c.idx_heads, c.rope_dim);
     note_launch();
     return cudaGetLastError();
   }
@@ -765,10 +769,10 @@ cudaError_t launch_indexer_prep(const v4_config& c, const void* iq, const float2
   const long long blocks = (rows * lanes + threads - 1) / threads;
   if (c.dtype == V4_BF16)
     indexer_prep_kernel<bf16><<<(unsigned)blocks, threads, 0, st>>>(
-        (const bf16*)iq, cs_table, inv_freq, (bf16*)iqp, rows, c.seqlen, c.idx_heads, c.idx_dim, c.rope_dim);
+        (const bf16*)iq, cs_table, inv_freq, (bf16*)iqp, rows, Sq, t0, c.idx_heads, c.idx_dim, c.rope_dim);
   else
     indexer_prep_kernel<float><<<(unsigned)blocks, threads, 0, st>>>(
-        (const float*)iq, cs_table, inv_freq, (float*)iqp, rows, c.seqlen, c.idx_heads, c.idx_dim,
+        (const float*)iq, cs_table, inv_freq, (float*)iqp, rows, Sq, t0, c.idx_heads, c.idx_dim,
         c.rope_dim);
   note_launch();
   return cudaGetLastError();

@@ -17,28 +17,29 @@ namespace {
 constexpr int kScoreThreads = 256;
 constexpr int kHeadChunk = 16;
 
-// One block per (query t, batch b).  Prepared queries and scaled weights of
-// the row sit in shared memory; thread j scores entries s = j, j+256, ...
+// One block per (query row i, batch b), position t = t0 + i of Sq query rows
+// per sequence.  Prepared queries and scaled weights of the row sit in shared memory; thread j scores entries s = j, j+256, ...
 // for s < n_vis(t).  Per head: d = sum_c q[h][c] k[s][c] accumulated in
 // order c = 0..Di-1 in fp32, then I += w'[h] * max(d, 0) in head order.
 template <typename T>
 __global__ void __launch_bounds__(kScoreThreads)
 indexer_scores_kernel(const T* __restrict__ iqp, const T* __restrict__ ikey,
                       const float* __restrict__ w, float* __restrict__ scores,
-                      int S, int N, int Hi, int Di, int ratio, float wscale) {
+                      int Sq, int t0, int N, int Hi, int Di, int ratio, float wscale) {
   extern __shared__ float sm[];
   float* s_q = sm;                 // [Hi][Di]
   float* s_w = sm + Hi * Di;       // [Hi]
-  const int t = blockIdx.x;
+  const int t = t0 + blockIdx.x;
   const int b = blockIdx.y;
+  const size_t qr = (size_t)b * Sq + blockIdx.x;     // query row
   const int nv = min(n_visible(t, ratio), N);
   if (nv == 0) return;
-  const T* qrow = iqp + ((size_t)b * S + t) * Hi * Di;
+  const T* qrow = iqp + qr * Hi * Di;
   for (int i = threadIdx.x; i < Hi * Di; i += kScoreThreads) s_q[i] = to_f(qrow[i]);
   for (int i = threadIdx.x; i < Hi; i += kScoreThreads)
-    s_w[i] = w[((size_t)b * S + t) * Hi + i] * wscale;
+    s_w[i] = w[qr * Hi + i] * wscale;
   __syncthreads();
-  float* out = scores + ((size_t)b * S + t) * N;
+  float* out = scores + qr * N;
   const T* keys = ikey + (size_t)b * N * Di;
   for (int s = threadIdx.x; s < nv; s += kScoreThreads) {
     const T* k = keys + (size_t)s * Di;
@@ -75,7 +76,8 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
 
 constexpr int kTopkThreads = 256;
 
-// One block per (t, b): exact top-K of the row's n_vis scores.  The row is
+// One block per (query row i, batch b), position t = t0 + i: exact top-K of
+// the row's n_vis(t) scores.  The row is
 // held in shared memory as order-preserving 32-bit keys; a 4-pass MSB-first
 // radix select (8 bits per pass) finds the K-th key, and a compaction keeps
 // every key above it plus the lowest-index keys equal to it.  Output in
@@ -131,17 +133,18 @@ __device__ __forceinline__ void hist_add4(int* whist, uint4 k4, int s, int nv, u
 
 __global__ void __launch_bounds__(kTopkThreads, 8)
 topk_kernel(const float* __restrict__ scores, int32_t* __restrict__ idx, float* __restrict__ iscore,
-            int S, int N, int K, int ratio, int smem_cap) {
+            int Sq, int t0, int N, int K, int ratio, int smem_cap) {
   extern __shared__ uint4 skeys4[];
   __shared__ int s_hist[kTopkWarps][256];
   __shared__ uint32_t s_prefix, s_mask;
   __shared__ int s_krem, s_done;
-  const int t = blockIdx.x, b = blockIdx.y;
+  const int t = t0 + blockIdx.x, b = blockIdx.y;
+  const size_t qr = (size_t)b * Sq + blockIdx.x;     // query row
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int nv = min(n_visible(t, ratio), N);
-  const float* row = scores + ((size_t)b * S + t) * N;
-  int32_t* orow = idx + ((size_t)b * S + t) * K;
-  float* srow = iscore ? iscore + ((size_t)b * S + t) * K : nullptr;
+  const float* row = scores + qr * N;
+  int32_t* orow = idx + qr * K;
+  float* srow = iscore ? iscore + qr * K : nullptr;
   if (nv <= K) {
     for (int j = tid; j < K; j += kTopkThreads) {
       orow[j] = j < nv ? j : -1;
@@ -328,8 +331,8 @@ cudaError_t scores_t(const v4_config& c, const void* iqp, const void* ikey, cons
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const float wscale = 1.0f / sqrtf((float)c.idx_heads) / sqrtf((float)c.idx_dim);
-  dim3 grid(c.seqlen, c.batch);
-  kern<<<grid, kScoreThreads, smem, st>>>((const T*)iqp, (const T*)ikey, w, scores, c.seqlen, N,
+  dim3 grid(q_rows(c), c.batch);
+  kern<<<grid, kScoreThreads, smem, st>>>((const T*)iqp, (const T*)ikey, w, scores, q_rows(c), c.q_begin, N,
                                           c.idx_heads, c.idx_dim, c.ratio, wscale);
   note_launch();
   return cudaGetLastError();
@@ -353,8 +356,9 @@ cudaError_t launch_topk(const v4_config& c, const float* scores, int32_t* idx, f
   const size_t smem = (size_t)((cap + 3) & ~3) * sizeof(uint32_t);      // whole 4-key chunks
   cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(c.seqlen, c.batch);
-  topk_kernel<<<grid, kTopkThreads, smem, st>>>(scores, idx, iscore, c.seqlen, N, c.topk, c.ratio, cap);
+  dim3 grid(q_rows(c), c.batch);
+  topk_kernel<<<grid, kTopkThreads, smem, st>>>(scores, idx, iscore, q_rows(c), c.q_begin, N, c.topk, c.ratio,
+                                                cap);
   note_launch();
   return cudaGetLastError();
 }

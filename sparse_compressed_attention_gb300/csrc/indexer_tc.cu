@@ -82,12 +82,12 @@ constexpr uint32_t smem_bytes() {
 static_assert(smem_bytes<false>() <= 232448 && smem_bytes<true>() <= 232448, "shared memory budget");
 
 struct Params {
-  const float* w;          // [B,S,64] unscaled weights
-  const float* qscale;     // [B,S,64] query-row scales (E4M3 only)
+  const float* w;          // [B,Sq,64] unscaled weights
+  const float* qscale;     // [B,Sq,64] query-row scales (E4M3 only)
   const float* kscale;     // [B,N] key-row scales (E4M3 only)
-  float* scores;           // [B,S,N]
+  float* scores;           // [B,Sq,N]
   int* status;
-  int B, S, N, ratio;
+  int B, Sq, t0, N, ratio; // Sq query rows per sequence at positions t0 .. t0+Sq-1
   float wscale;
 };
 
@@ -102,12 +102,14 @@ __device__ __forceinline__ void fma2_relu(float& a0, float& a1, float w0, float 
       : "f"(w0), "f"(w1), "f"(r0), "f"(r1));
 }
 
-__device__ __forceinline__ void group_of(int gi, const Params& p, int groups_per_b, int& b, int& t0,
+// Group gi: batch b, first query row r0 of its kQG rows (positions p.t0 + r0 ..),
+// entry tiles of its last query.
+__device__ __forceinline__ void group_of(int gi, const Params& p, int groups_per_b, int& b, int& r0,
                                          int& tiles) {
   b = gi % p.B;
   const int grp = groups_per_b - 1 - gi / p.B;
-  t0 = grp * kQG;
-  const int tmax = min(t0 + kQG - 1, p.S - 1);
+  r0 = grp * kQG;
+  const int tmax = p.t0 + min(r0 + kQG - 1, p.Sq - 1);
   const int nv = min((tmax + 1) / p.ratio, p.N);
   tiles = (nv + 127) / 128;
 }
@@ -148,7 +150,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = c->tmem_base;
-  const int groups_per_b = (p.S + kQG - 1) / kQG;
+  const int groups_per_b = (p.Sq + kQG - 1) / kQG;
   const int total = p.B * groups_per_b;
 
   if (warp == 0) {
@@ -157,15 +159,15 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       int gq = 0, st = 0, use = 0;
       bool ok = true;
       for (int gi = blockIdx.x; gi < total && ok; gi += gridDim.x) {
-        int b, t0, tiles;
-        group_of(gi, p, groups_per_b, b, t0, tiles);
+        int b, r0, tiles;
+        group_of(gi, p, groups_per_b, b, r0, tiles);
         if (tiles == 0) continue;
         const int bb = gq & 1;
         if (gq >= 2) ok = mbar_wait(&c->b_empty[bb], ((gq >> 1) - 1) & 1, &c->abort, p.status);
         if (!ok) break;
         mbar_expect_tx(&c->b_full[bb], kKB * kBBlock);
         for (int kb = 0; kb < kKB; ++kb)
-          tma_load_2d(smem + OFF_B + (kKB * bb + kb) * kBBlock, &map_q, kXStep * kb, (b * p.S + t0) * kHi,
+          tma_load_2d(smem + OFF_B + (kKB * bb + kb) * kBBlock, &map_q, kXStep * kb, (b * p.Sq + r0) * kHi,
                       &c->b_full[bb]);
         for (int j = 0; j < tiles && ok; ++j) {
           if (use >= kStages) ok = mbar_wait(&c->a_empty[st], ((use / kStages) - 1) & 1, &c->abort, p.status);
@@ -190,8 +192,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       int gq = 0, st = 0, use = 0, tile_ct = 0;
       bool ok = true;
       for (int gi = blockIdx.x; gi < total && ok; gi += gridDim.x) {
-        int b, t0, tiles;
-        group_of(gi, p, groups_per_b, b, t0, tiles);
+        int b, r0, tiles;
+        group_of(gi, p, groups_per_b, b, r0, tiles);
         if (tiles == 0) continue;
         const int bb = gq & 1;
         ok = mbar_wait(&c->b_full[bb], (gq >> 1) & 1, &c->abort, p.status);
@@ -243,9 +245,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
       int bg = 0, tg = 0, tl = 0;
       if (g >= total) return 0.f;
       group_of(g, p, groups_per_b, bg, tg, tl);
-      const int t = tg + ts / kHi;
-      if (t >= p.S) return 0.f;
-      const size_t wi = ((size_t)bg * p.S + t) * kHi + (ts % kHi);
+      const int r = tg + ts / kHi;             // query row
+      if (r >= p.Sq) return 0.f;
+      const size_t wi = ((size_t)bg * p.Sq + r) * kHi + (ts % kHi);
       if constexpr (kE4M3)
         return p.w[wi] * p.wscale * p.qscale[wi];
       else
@@ -255,8 +257,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     pf_gi = blockIdx.x;
     int gq = 0, tile_ct = 0;
     for (int gi = blockIdx.x; gi < total; gi += gridDim.x) {
-      int b, t0, tiles;
-      group_of(gi, p, groups_per_b, b, t0, tiles);
+      int b, r0, tiles;
+      group_of(gi, p, groups_per_b, b, r0, tiles);
       if (tiles == 0) continue;
       const float wv = pf_gi == gi ? pf_w : fetch_w(gi);
       // buffer gq & 1 was last read for group gq-2, which every thread has
@@ -298,8 +300,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         }
 #pragma unroll
         for (int qq = 0; qq < 2; ++qq) {
-          const int t = t0 + q0 + qq;
-          if (t < p.S && s < min((t + 1) / p.ratio, p.N)) p.scores[((size_t)b * p.S + t) * p.N + s] = sc[qq];
+          const int r = r0 + q0 + qq;            // query row, position p.t0 + r
+          if (r < p.Sq && s < min((p.t0 + r + 1) / p.ratio, p.N))
+            p.scores[((size_t)b * p.Sq + r) * p.N + s] = sc[qq];
         }
         ++tile_ct;
       }
@@ -333,7 +336,7 @@ static cudaError_t launch_scores(const v4_config& cfg, const CUtensorMap& mq, co
   int sms = 0, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int total = cfg.batch * ((cfg.seqlen + kQG - 1) / kQG);
+  const int total = cfg.batch * ((q_rows(cfg) + kQG - 1) / kQG);
   const int grid = total < sms ? total : sms;
   indexer_tc_kernel<kE4M3><<<grid, kThreads, bytes, st>>>(mq, mk, prm);
   note_launch();
@@ -348,7 +351,8 @@ static Params make_params(const v4_config& cfg, const float* w, float* scores, i
   prm.scores = scores;
   prm.status = status;
   prm.B = cfg.batch;
-  prm.S = cfg.seqlen;
+  prm.Sq = q_rows(cfg);
+  prm.t0 = cfg.q_begin;
   prm.N = cfg.seqlen / cfg.ratio;
   prm.ratio = cfg.ratio;
   prm.wscale = 1.0f / sqrtf((float)kHi) / sqrtf((float)kDi);
@@ -362,7 +366,7 @@ cudaError_t launch_indexer_scores_tc(const v4_config& cfg, const void* iqp, cons
   if (N == 0) return cudaSuccess;
   CUtensorMap mq, mk;
   int e = 0;
-  e |= make_tmap_bf16_2d(&mq, iqp, kDi, (uint64_t)B * S * kHi, 64, 256, true);
+  e |= make_tmap_bf16_2d(&mq, iqp, kDi, (uint64_t)B * q_rows(cfg) * kHi, 64, 256, true);
   e |= make_tmap_bf16_2d(&mk, ikey, kDi, (uint64_t)B * N, 64, 128, true);
   if (e) return cudaErrorInvalidValue;
   return launch_scores<false>(cfg, mq, mk, make_params(cfg, w, scores, status), st);
@@ -376,7 +380,7 @@ cudaError_t launch_indexer_scores_e4m3(const v4_config& cfg, const uint8_t* qc, 
   if (N == 0) return cudaSuccess;
   CUtensorMap mq, mk;
   int e = 0;
-  e |= make_tmap_u8_2d(&mq, qc, kDi, (uint64_t)B * S * kHi, 128, 256, true);
+  e |= make_tmap_u8_2d(&mq, qc, kDi, (uint64_t)B * q_rows(cfg) * kHi, 128, 256, true);
   e |= make_tmap_u8_2d(&mk, kc, kDi, (uint64_t)B * N, 128, 128, true);
   if (e) return cudaErrorInvalidValue;
   Params prm = make_params(cfg, w, scores, status);

@@ -14,24 +14,45 @@ namespace v4 {
 // Counts kernel launches made by the library (reported by v4_launch_count).
 void note_launch(int n = 1);
 
+// Query rows per sequence of a call: positions q_begin .. seqlen-1.  Row
+// tensors (q, iq, w, o, lse, idx, scores) are indexed by b * q_rows + (t - q_begin);
+// sequence tensors (kv, entries) by b * seqlen + t.
+inline int q_rows(const v4_config& c) { return c.seqlen - c.q_begin; }
+
 // Argument checks, error text and the device status word (api.cu).
 v4_status validate_config(const v4_config* c);
 v4_status set_error(v4_status st, const char* msg);
 int* device_status_ptr();
 
-// Workspace carve-up for one configuration.  Offsets are 256-byte aligned.
+// Per-stage timing (v4_profile_*): while timing is on, the launches between
+// construction and destruction are bracketed by two CUDA events on `st`
+// (api.cu).  `kind` is a stage number of v4_profile_enable's list.
+class StageTiming {
+ public:
+  StageTiming(int kind, cudaStream_t st);
+  ~StageTiming();
+  StageTiming(const StageTiming&) = delete;
+  StageTiming& operator=(const StageTiming&) = delete;
+
+ private:
+  void* rec_;
+  cudaStream_t st_;
+};
+
+// Workspace carve-up for one configuration (Sq = q_rows).  Offsets are
+// 256-byte aligned.
 struct Workspace {
   size_t kv_rot = 0, kv_rot_bytes = 0;     // rotated window keys [B,S,D]
   size_t ent = 0, ent_bytes = 0;           // entries [B,N,D] (layer call)
   size_t ikey = 0, ikey_bytes = 0;         // indexer keys [B,N,Di] (layer call)
-  size_t iqp = 0, iqp_bytes = 0;           // prepared indexer queries [B,S,Hi,Di]
-  size_t scores = 0, scores_bytes = 0;     // indexer scores [B,S,N] fp32
-  size_t idx = 0, idx_bytes = 0;           // selected entries [B,S,K] (layer call)
+  size_t iqp = 0, iqp_bytes = 0;           // prepared indexer queries [B,Sq,Hi,Di]
+  size_t scores = 0, scores_bytes = 0;     // indexer scores [B,Sq,N] fp32
+  size_t idx = 0, idx_bytes = 0;           // selected entries [B,Sq,K] (layer call)
   size_t knorm = 0, knorm_bytes = 0;       // key-row norms [B*S + B*N] (tensor-core attention)
-  size_t counters = 0, counters_bytes = 0; // work counter, redo count, redo list [2 + B*S]
+  size_t counters = 0, counters_bytes = 0; // work counter, redo count, redo list [2 + B*Sq*slices]
   size_t rope = 0, rope_bytes = 0;         // cos/sin table [S][R/2] float2
-  size_t qc8 = 0, qc8_bytes = 0;           // E4M3 indexer: query codes [B,S,Hi,Di] u8
-  size_t qs8 = 0, qs8_bytes = 0;           //   query scales [B,S,Hi] fp32
+  size_t qc8 = 0, qc8_bytes = 0;           // E4M3 indexer: query codes [B,Sq,Hi,Di] u8
+  size_t qs8 = 0, qs8_bytes = 0;           //   query scales [B,Sq,Hi] fp32
   size_t kc8 = 0, kc8_bytes = 0;           //   key codes [B,N,Di] u8
   size_t ks8 = 0, ks8_bytes = 0;           //   key scales [B,N] fp32
   size_t total = 0;
@@ -71,7 +92,7 @@ int make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t 
 cudaError_t launch_indexer_prep(const v4_config& c, const void* iq, const float2* cs_table,
                                 const float* inv_freq, void* iqp, cudaStream_t st);
 // The same preparation quantised to E4M3 rows in the kernel (bf16, Di = 128):
-// codes [B,S,Hi,128] and scales [B,S,Hi] instead of the bf16 rows.
+// codes [B,Sq,Hi,128] and scales [B,Sq,Hi] instead of the bf16 rows.
 cudaError_t launch_indexer_prep_e4m3(const v4_config& c, const void* iq, const float2* cs_table,
                                      const float* inv_freq, uint8_t* codes, float* scales, cudaStream_t st);
 
@@ -83,7 +104,7 @@ cudaError_t launch_indexer_scores_tc(const v4_config& c, const void* iqp, const 
                                      float* scores, int* status, cudaStream_t st);
 // Opt-in E4M3 indexer (indexer_tc.cu): per-row absmax quantisation of bf16
 // rows (dim a multiple of 128, <= 1024) and the scores of quantised
-// operands (Hi = 64, Di = 128): q codes [B,S,64,128] with scales [B,S,64],
+// operands (Hi = 64, Di = 128): q codes [B,Sq,64,128] with scales [B,Sq,64],
 // key codes [B,N,128] with scales [B,N].
 cudaError_t launch_quant_e4m3(const void* x, long long rows, int dim, uint8_t* codes, float* scales,
                               cudaStream_t st);
@@ -95,8 +116,8 @@ cudaError_t launch_topk(const v4_config& c, const float* scores, int32_t* idx, f
                         cudaStream_t st);
 
 // ---- attention (mqa.cu)
-// `list` (nullable): list[0] = number of queries, list[1..] = b*S + t of each;
-// when given, only those queries are computed.
+// `list` (nullable): list[0] = number of queries, list[1..] = b*Sq + (t - q_begin)
+// of each (its query row); when given, only those queries are computed.
 cudaError_t launch_mqa_simt(const v4_config& c, const void* q, const void* kv_rot,
                             const void* ent, const int32_t* idx, const float* sink,
                             const float* inv_freq, void* o, float* lse, int* status,

@@ -36,8 +36,8 @@ __global__ void __launch_bounds__(kMqaThreads)
 mqa_simt_kernel(const T* __restrict__ q, const T* __restrict__ kv_rot, const T* __restrict__ ent,
                 const int32_t* __restrict__ idx, const float* __restrict__ sink,
                 const float* __restrict__ inv_freq, T* __restrict__ o, float* __restrict__ lse,
-                int* __restrict__ status, const int* __restrict__ list, int S, int H, int D, int R,
-                int N, int ratio, int window, int K, float scale) {
+                int* __restrict__ status, const int* __restrict__ list, int S, int Sq, int t0, int H, int D,
+                int R, int N, int ratio, int window, int K, float scale) {
   extern __shared__ float sm[];
   const int ldk = D + 1;                      // padded key rows: conflict-free columns
   float* s_q = sm;                            // [kHG][D] rotated query rows
@@ -50,20 +50,23 @@ mqa_simt_kernel(const T* __restrict__ q, const T* __restrict__ kv_rot, const T* 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = h0 + warp;
   const bool head_live = h < H;
-  // without a list: query t = blockIdx.x of batch blockIdx.z; with a list:
-  // the listed queries, strided over blockIdx.x
+  // without a list: query row blockIdx.x of batch blockIdx.z; with a list:
+  // the listed query rows, strided over blockIdx.x.  Query row r of batch b
+  // is position t = t0 + r; q, o, lse and idx are indexed by query row.
   for (int item = blockIdx.x;; item += gridDim.x) {
-  int t, b;
+  int t, b, r;
   if (list != nullptr) {
     if (item >= list[0]) break;
-    const int bt = list[1 + item];
-    b = bt / S;
-    t = bt % S;
+    const int br = list[1 + item];
+    b = br / Sq;
+    r = br % Sq;
   } else {
-    if (item >= S) break;
-    t = item;
+    if (item >= Sq) break;
+    r = item;
     b = blockIdx.z;
   }
+  t = t0 + r;
+  const size_t qrow = (size_t)b * Sq + r;
   __syncthreads();
 
   // RoPE angles of position t (shared by all heads)
@@ -79,7 +82,7 @@ mqa_simt_kernel(const T* __restrict__ q, const T* __restrict__ kv_rot, const T* 
     const int hh = h0 + i / D, c = i % D;
     float v = 0.f;
     if (hh < H) {
-      const T* qr = q + (((size_t)b * S + t) * H + hh) * D;
+      const T* qr = q + (qrow * H + hh) * D;
       v = to_f(qr[c]);
       if (c >= D - R) {
         const int j = (c - (D - R)) >> 1;
@@ -114,7 +117,7 @@ mqa_simt_kernel(const T* __restrict__ q, const T* __restrict__ kv_rot, const T* 
       if (j < ks.ne) {
         int s = j;
         if (K > 0) {
-          s = idx[((size_t)b * S + t) * K + j];
+          s = idx[qrow * K + j];
           if (s < -1 || s >= nv) { set_status(status, kStatusBadIndex); s = -1; }
         }
         if (s >= 0) p = ent + ((size_t)b * N + s) * D;
@@ -173,7 +176,7 @@ mqa_simt_kernel(const T* __restrict__ q, const T* __restrict__ kv_rot, const T* 
 
   if (head_live) {
   const float inv_l = l > 0.f ? 1.f / l : 0.f;
-  T* orow = o + (((size_t)b * S + t) * H + h) * D;
+  T* orow = o + (qrow * H + h) * D;
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
     if (i < per_lane) {
@@ -189,7 +192,7 @@ mqa_simt_kernel(const T* __restrict__ q, const T* __restrict__ kv_rot, const T* 
       from_f(orow + c, v);
     }
   }
-  if (lse && lane == 0) lse[((size_t)b * S + t) * H + h] = l > 0.f ? m + logf(l) : -INFINITY;
+  if (lse && lane == 0) lse[qrow * H + h] = l > 0.f ? m + logf(l) : -INFINITY;
   }
   }
 }
@@ -205,11 +208,11 @@ cudaError_t mqa_t(const v4_config& c, const void* q, const void* kv_rot, const v
   if (e != cudaSuccess) return e;
   const int N = c.ratio > 0 ? c.seqlen / c.ratio : 0;
   const float scale = c.softmax_scale > 0.f ? c.softmax_scale : 1.0f / sqrtf((float)D);
-  dim3 grid(c.seqlen, (c.n_heads + kHG - 1) / kHG, c.batch);
+  dim3 grid(q_rows(c), (c.n_heads + kHG - 1) / kHG, c.batch);
   if (list != nullptr) grid = dim3(256, (c.n_heads + kHG - 1) / kHG, 1);
   kern<<<grid, kMqaThreads, smem, st>>>((const T*)q, (const T*)kv_rot, (const T*)ent, idx, sink,
-                                        inv_freq, (T*)o, lse, status, list, c.seqlen, c.n_heads, D,
-                                        c.rope_dim, N, c.ratio, c.window, c.topk, scale);
+                                        inv_freq, (T*)o, lse, status, list, c.seqlen, q_rows(c), c.q_begin,
+                                        c.n_heads, D, c.rope_dim, N, c.ratio, c.window, c.topk, scale);
   note_launch();
   return cudaGetLastError();
 }

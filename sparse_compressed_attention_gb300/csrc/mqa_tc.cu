@@ -94,18 +94,19 @@ constexpr uint32_t kSmemBytes = OFF_CTL + sizeof(Ctl);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Params {
-  const bf16* q;               // [B,S,H,512] (L2 prefetch of upcoming queries)
+  const bf16* q;               // [B,Sq,H,512] (L2 prefetch of upcoming queries)
   const bf16* ent;             // [B,N,512] gathered entries
-  bf16* o;                     // [B,S,H,512]
-  const int32_t* idx;          // [B,S,K] or null
+  bf16* o;                     // [B,Sq,H,512]
+  const int32_t* idx;          // [B,Sq,K] or null
   const float* sink;           // [H] or null
   const float2* rope_cs;       // [S][32] cos/sin
   const float* wmax;           // [B*S]   max |key| over the window of each query
   const float* emax;           // [B*(N+1)] prefix max |entry|
-  float* lse;                  // [B,S,H] or null
+  float* lse;                  // [B,Sq,H] or null
   int* status;
-  int* counters;               // [0] work item, [1] redo count, [2..] redo list
+  int* counters;               // [0] work item, [1] redo count, [2..] redo list (query rows)
   int B, S, N, ratio, window, K;
+  int Sq, t0;                  // query rows per sequence, at positions t0 .. t0+Sq-1
   int H, HS;                   // heads, head slices of 64
   float scale;
 };
@@ -199,7 +200,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = c->tmem_base;
-  const int total = p.B * p.S * p.HS;        // work items: (query, head slice)
+  const int total = p.B * p.Sq * p.HS;       // work items: (query, head slice)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -213,9 +214,9 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     auto fetch_ahead = [&](int it) {
       if (it >= total) return;
       const int qi = it / p.HS;
-      const int nb = qi % p.B, nt = p.S - 1 - qi / p.B;
+      const int nb = qi % p.B, nr = p.Sq - 1 - qi / p.B, nt = p.t0 + nr;
       if (gathered) {
-        const int32_t* row = p.idx + ((size_t)nb * p.S + nt) * p.K;
+        const int32_t* row = p.idx + ((size_t)nb * p.Sq + nr) * p.K;
 #pragma unroll
         for (int i = 0; i < kMaxSel / 32; ++i) {
           const int j = lane + 32 * i;
@@ -232,7 +233,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       QInfo inf;
       inf.done = it >= total ? 1 : 0;
       inf.b = inf.done ? 0 : (it / p.HS) % p.B;
-      inf.t = inf.done ? 0 : p.S - 1 - (it / p.HS) / p.B;
+      inf.t = inf.done ? 0 : p.t0 + p.Sq - 1 - (it / p.HS) / p.B;
       inf.hs = inf.done ? 0 : it % p.HS;
       // kmax bounds |k| over every key the query can see (for a selection,
       // over all visible entries: a superset, so still a bound)
@@ -241,7 +242,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       inf.w_lo = 0;
       if (!inf.done) {
         if (lane == 0) {                      // warm L2 with its query rows, loaded one query later
-          const bf16* qn_rows = p.q + (((size_t)inf.b * p.S + inf.t) * p.H + kH * inf.hs) * kD;
+          const bf16* qn_rows = p.q + (((size_t)inf.b * p.Sq + inf.t - p.t0) * p.H + kH * inf.hs) * kD;
           asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(qn_rows), "r"(kH * kD * 2) : "memory");
         }
         const int nv = p.ratio > 0 ? min((inf.t + 1) / p.ratio, p.N) : 0;
@@ -299,8 +300,8 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       if (lane == 0) mbar_expect_tx(&c->q_full, 8 * kQBlockBytes);
       __syncwarp();
       if (lane < 8)
-        tma_load_2d(smem + OFF_Q + lane * kQBlockBytes, &map_q, 64 * lane, (cur.b * p.S + cur.t) * p.H + kH * cur.hs,
-                    &c->q_full);
+        tma_load_2d(smem + OFF_Q + lane * kQBlockBytes, &map_q, 64 * lane,
+                    (cur.b * p.Sq + cur.t - p.t0) * p.H + kH * cur.hs, &c->q_full);
       const uint16_t* lst = lists + (qc & 1) * kMaxSel;
       QInfo nxt;
       nxt.done = 1;
@@ -634,13 +635,13 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         // too little mass under the bound: exp underflow may have lost keys
         const bool bad = !(l >= (float)nk_total * 1.0e-26f) || !(l < INFINITY);
         if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&c->redo, 1);
-        if (p.lse) p.lse[((size_t)b * p.S + t) * p.H + kH * hsl + ts] = m + logf(l);
+        if (p.lse) p.lse[((size_t)b * p.Sq + t - p.t0) * p.H + kH * hsl + ts] = m + logf(l);
         hs[256 + ts] = 1.0f / l;
       }
       named_bar_sync(1, kSoftThreads);
       if (ts == 0 && c->redo) {                 // queue the query once for the running-max kernel
         const int slot = atomicAdd(&p.counters[1], 1);
-        p.counters[2 + slot] = b * p.S + t;
+        p.counters[2 + slot] = b * p.Sq + t - p.t0;
         c->redo = 0;
       }
       float inv_l[32];
@@ -654,7 +655,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       }
       // o[t, h, 128m + krow]: for each head the 32 lanes of a warp write 64
       // contiguous bytes
-      bf16* obase = p.o + (((size_t)b * p.S + t) * p.H + kH * hsl + h0) * kD + krow;
+      bf16* obase = p.o + (((size_t)b * p.Sq + t - p.t0) * p.H + kH * hsl + h0) * kD + krow;
       for (int m = 0; m < 4; ++m) {
         float v[32];
         tmem_ld32(tmem + lane_base + 128 + 64 * m + h0, v);
@@ -721,7 +722,7 @@ cudaError_t launch_mqa_tc(const v4_config& cfg, const void* q, const void* kv_ro
   const int B = cfg.batch, S = cfg.seqlen;
   const int N = cfg.ratio > 0 ? S / cfg.ratio : 0;
   CUtensorMap mq, mkv, ment;
-  const uint64_t qrows = (uint64_t)B * S * cfg.n_heads;
+  const uint64_t qrows = (uint64_t)B * q_rows(cfg) * cfg.n_heads;
   int e = 0;
   e |= make_tmap_bf16_2d(&mq, q, kD, qrows, 64, 64, true);
   e |= make_tmap_bf16_2d(&mkv, kv_rot, kD, (uint64_t)B * S, 64, kTileKeys, true);
@@ -749,6 +750,8 @@ cudaError_t launch_mqa_tc(const v4_config& cfg, const void* q, const void* kv_ro
   prm.K = cfg.topk;
   prm.H = cfg.n_heads;
   prm.HS = cfg.n_heads / kH;
+  prm.Sq = q_rows(cfg);
+  prm.t0 = cfg.q_begin;
   prm.scale = cfg.softmax_scale > 0.f ? cfg.softmax_scale : 1.0f / sqrtf((float)kD);
   cudaError_t err = cudaFuncSetAttribute(mqa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
@@ -756,7 +759,7 @@ cudaError_t launch_mqa_tc(const v4_config& cfg, const void* q, const void* kv_ro
   int sms = 0, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long total = (long long)B * S * (cfg.n_heads / kH);
+  const long long total = (long long)B * q_rows(cfg) * (cfg.n_heads / kH);
   const int grid = (int)(total < sms ? total : sms);
   err = cudaMemsetAsync(counters + 1, 0, sizeof(int), st);
   if (err != cudaSuccess) return err;

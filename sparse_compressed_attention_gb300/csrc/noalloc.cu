@@ -106,19 +106,33 @@ extern "C" v4_status v4_sparse_mqa_fwd_noalloc(const v4_config* cfg, const void*
   float2* table = (float2*)(base + kOffRope);
   const int32_t* sel = c.topk > 0 ? idx : nullptr;
   cudaError_t e;
+  // stage timing as in v4_sparse_mqa_fwd: kind 1 (window keys), kind 5 (attention)
+  constexpr int kKindRotate = 1, kKindAttention = 5;
   if (c.path != V4_PATH_SIMT && mqa_tc_supported(c)) {
-    if ((e = launch_rope_table(c, inv_freq, table, st)) != cudaSuccess) return set_error(V4_ERR_CUDA, cudaGetErrorString(e));
-    if ((e = launch_key_prep(c, kv, ent, table, kv_rot, kv_norm, ent_norm, wmax, emax, st)) != cudaSuccess)
-      return set_error(V4_ERR_CUDA, cudaGetErrorString(e));
-    // launch_mqa_tc clears the redo count it needs before its kernel runs
-    if ((e = launch_mqa_tc(c, q, kv_rot, ent, sel, sink, table, wmax, emax, o, lse, counters, status, st)) !=
-        cudaSuccess)
-      return set_error(V4_ERR_CUDA, cudaGetErrorString(e));
+    {
+      StageTiming tm(kKindRotate, st);
+      if ((e = launch_rope_table(c, inv_freq, table, st)) != cudaSuccess)
+        return set_error(V4_ERR_CUDA, cudaGetErrorString(e));
+      if ((e = launch_key_prep(c, kv, ent, table, kv_rot, kv_norm, ent_norm, wmax, emax, st)) != cudaSuccess)
+        return set_error(V4_ERR_CUDA, cudaGetErrorString(e));
+    }
+    {
+      StageTiming tm(kKindAttention, st);
+      // launch_mqa_tc clears the redo count it needs before its kernel runs
+      if ((e = launch_mqa_tc(c, q, kv_rot, ent, sel, sink, table, wmax, emax, o, lse, counters, status, st)) !=
+          cudaSuccess)
+        return set_error(V4_ERR_CUDA, cudaGetErrorString(e));
+    }
     if ((e = launch_mqa_simt(c, q, kv_rot, ent, sel, sink, inv_freq, o, lse, status, counters + 1, st)) != cudaSuccess)
       return set_error(V4_ERR_CUDA, cudaGetErrorString(e));
     return V4_OK;
   }
-  if ((e = launch_rotate_rows(c, kv, inv_freq, kv_rot, st)) != cudaSuccess) return set_error(V4_ERR_CUDA, cudaGetErrorString(e));
+  {
+    StageTiming tm(kKindRotate, st);
+    if ((e = launch_rotate_rows(c, kv, inv_freq, kv_rot, st)) != cudaSuccess)
+      return set_error(V4_ERR_CUDA, cudaGetErrorString(e));
+  }
+  StageTiming tm(kKindAttention, st);
   if ((e = launch_mqa_simt(c, q, kv_rot, ent, sel, sink, inv_freq, o, lse, status, nullptr, st)) != cudaSuccess)
     return set_error(V4_ERR_CUDA, cudaGetErrorString(e));
   return V4_OK;

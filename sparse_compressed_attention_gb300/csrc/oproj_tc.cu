@@ -266,7 +266,7 @@ bool oproj_tc_supported(const v4_config& c) {
 
 cudaError_t launch_oproj_tc(const v4_config& cfg, const void* o, const void* wo_a, void* y, int* status,
                             cudaStream_t st) {
-  const long long T = (long long)cfg.batch * cfg.seqlen;
+  const long long T = (long long)cfg.batch * q_rows(cfg);      // the call's query rows
   const int G = cfg.o_groups, N = cfg.o_rank;
   const int Kg = (cfg.n_heads / G) * cfg.head_dim;
   CUtensorMap mx, mw;

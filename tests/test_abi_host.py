@@ -151,3 +151,29 @@ def test_error_text_is_per_thread(lib):
     th.join()
     assert seen == [""]
     assert "head_dim" in lib.v4_last_error().decode()
+
+
+def test_row_slice_argument_checks(lib):
+    # q_begin must name a query position; the backward and the distillation
+    # target take whole sequences only (both refused before any GPU work)
+    p = SI.preset("hca_bf16_16k", S=256, q_mode="direct")
+    with pytest.raises(L.V4Error, match="q_begin"):
+        L.v4_workspace_size(L.config_from_preset(p, q_begin=256))
+    with pytest.raises(L.V4Error, match="q_begin"):
+        L.v4_workspace_size(L.config_from_preset(p, q_begin=-1))
+    cfg = L.config_from_preset(p, q_begin=64)
+    st = lib.v4_sparse_mqa_bwd(C.byref(cfg), *([None] * 14), 0, None)
+    assert st == L.V4_ERR_UNSUPPORTED and "q_begin" in lib.v4_last_error().decode()
+    csa = L.config_from_preset(SI.preset("csa_bf16_4k", S=256, q_mode="direct"), q_begin=8)
+    st = lib.v4_indexer_kl_target(C.byref(csa), *([None] * 9), None, 0, None)
+    assert st == L.V4_ERR_UNSUPPORTED and "q_begin" in lib.v4_last_error().decode()
+
+
+def test_workspace_of_a_row_slice_scales_with_its_rows(lib):
+    p = SI.preset("csa_bf16_16k")
+    whole = L.v4_workspace_size(L.config_from_preset(p))
+    tail = L.v4_workspace_size(L.config_from_preset(p, q_begin=12288))
+    # the prepared queries, scores and selection shrink to a quarter of the rows
+    S, N = 16384, 4096
+    row_bytes = 64 * 128 * 2 + N * 4 + 512 * 4
+    assert whole - tail >= 0.75 * S * row_bytes - 4096

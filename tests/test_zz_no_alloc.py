@@ -2,8 +2,9 @@
 
 v4_sparse_mqa_fwd_noalloc serves callers that cannot allocate device memory
 where they run the attention; it keeps its scratch in a library-owned device
-array.  Its results must match v4_sparse_mqa_fwd on the same inputs, on two
-calls in a row (the second call reuses the array the first one left behind).
+array.  Its results must match v4_sparse_mqa_fwd on the same inputs, on calls in a
+row with a different problem in between (each call starts from whatever the
+previous one left in the array).
 """
 import ctypes as C
 
@@ -36,35 +37,51 @@ def _ptr(t):
     return None if t is None else C.c_void_p(t.data_ptr())
 
 
-@pytest.mark.parametrize("mode,base,over", [
-    ("csa", "csa_bf16_4k", dict(S=2048, q_mode="direct")),
-    ("hca", "hca_bf16_16k", dict(S=3000, q_mode="direct")),
-    ("csa_tiny_f32", "tiny_csa_f32", dict()),
-])
-def test_noalloc_matches_workspace_entry_point(mode, base, over):
-    from sparse_compressed_attention_gb300 import build
-    build.build()
-    lib = V.lib()
+def _problem(mode, base, over, seed):
     p = SI.preset(base, **over)
     sel = "csa" if mode.startswith("csa") else "hca"
-    x, f, ent, idx = _inputs(p, sel, seed=3)
+    x, f, ent, idx = _inputs(p, sel, seed=seed)
     cfg = V.config_from_preset(p, K=p["K"] if sel == "csa" else 0)
     B, S, H = p["B"], p["S"], p["H"]
     o_ref = torch.empty_like(x["q"])
     l_ref = torch.empty(B, S, H, device="cuda")
     V.v4_sparse_mqa_fwd(cfg, x["q"], x["kv"], ent, idx, x["sink"], f, o_ref, l_ref, V.alloc_workspace(cfg))
+    return dict(p=p, x=x, f=f, ent=ent, idx=idx, cfg=cfg, o_ref=o_ref, l_ref=l_ref)
+
+
+def _call_and_check(lib, pr, tag):
+    p, x = pr["p"], pr["x"]
+    B, S, H = p["B"], p["S"], p["H"]
+    o = torch.full_like(x["q"], float("nan"))
+    lse = torch.full((B, S, H), float("nan"), device="cuda")
     stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    st = lib.v4_sparse_mqa_fwd_noalloc(C.byref(pr["cfg"]), _ptr(x["q"]), _ptr(x["kv"]), _ptr(pr["ent"]),
+                                       _ptr(pr["idx"]), _ptr(x["sink"]), _ptr(pr["f"]), _ptr(o), _ptr(lse), stream)
+    assert st == 0, lib.v4_last_error().decode()
+    torch.cuda.synchronize()
     tol = 1e-5 if p["dtype"] == "f32" else 1e-2
-    for call in range(2):
-        o = torch.full_like(x["q"], float("nan"))
-        lse = torch.full((B, S, H), float("nan"), device="cuda")
-        st = lib.v4_sparse_mqa_fwd_noalloc(C.byref(cfg), _ptr(x["q"]), _ptr(x["kv"]), _ptr(ent), _ptr(idx),
-                                           _ptr(x["sink"]), _ptr(f), _ptr(o), _ptr(lse), stream)
-        assert st == 0, lib.v4_last_error().decode()
-        torch.cuda.synchronize()
-        assert rel_l2(np64(o), np64(o_ref)) < tol, call
-        assert torch.isfinite(lse).all()
-        assert np.max(np.abs(np64(lse) - np64(l_ref))) < 1e-3, call
+    assert rel_l2(np64(o), np64(pr["o_ref"])) < tol, tag
+    assert torch.isfinite(lse).all(), tag
+    assert np.max(np.abs(np64(lse) - np64(pr["l_ref"]))) < 1e-3, tag
+
+
+@pytest.mark.parametrize("mode,base,over,other", [
+    ("csa", "csa_bf16_4k", dict(S=2048, q_mode="direct"), ("hca", "hca_bf16_16k", dict(S=8000, q_mode="direct"))),
+    ("hca", "hca_bf16_16k", dict(S=3000, q_mode="direct"), ("csa", "csa_bf16_4k", dict(S=6000, q_mode="direct"))),
+    ("csa_tiny_f32", "tiny_csa_f32", dict(), ("csa_tiny_f32", "tiny_csa_f32", dict(S=200))),
+])
+def test_noalloc_matches_workspace_entry_point(mode, base, over, other):
+    """Three calls in a row, each checked against v4_sparse_mqa_fwd: the
+    problem, a different and larger one (which leaves other contents in the
+    shared array), then the first problem again."""
+    from sparse_compressed_attention_gb300 import build
+    build.build()
+    lib = V.lib()
+    a = _problem(mode, base, over, seed=3)
+    b = _problem(*other, seed=7)
+    _call_and_check(lib, a, "first call")
+    _call_and_check(lib, b, "different problem")
+    _call_and_check(lib, a, "first problem again")
     assert V.v4_get_device_status() == 0
 
 
