@@ -85,13 +85,20 @@ def topk_fp32_band(iqp, ikey, w, t, nvis, c):
     return float(b.max()) if b.size else 0.0
 
 
-def check_topk_rows(gpu_idx, scores, iqp, ikey, w, ratio, K, rows, c):
+def check_topk_rows(gpu_idx, scores, iqp, ikey, w, ratio, K, rows, c, detail=False):
     """Set-exact selection outside the tie band around the K-th score.
 
     gpu_idx [T, K] int; scores [T, N] oracle float64; iqp/ikey/w: the exact
-    inputs (float64 numpy) of one batch.  Returns the number of in-band swaps.
+    inputs (float64 numpy) of one batch.  The band is the larger of
+    1e-6 * |I_K| (the tie rule of the selection's specification) and the
+    forward-error bound of the fp32 score arithmetic.  Returns the number of
+    in-band swaps (entries of the exact top-K the GPU left out); with
+    ``detail`` also the number of swapped entries (left out or taken) whose
+    exact score lies outside the strict 1e-6 * |I_K| band, i.e. swaps that
+    only the fp32 error bound allows.
     """
     swaps = 0
+    wide = 0
     for i, t in enumerate(rows):
         nv = min(O.n_visible(int(t), ratio), ikey.shape[0])
         g = gpu_idx[i]
@@ -112,4 +119,6 @@ def check_topk_rows(gpu_idx, scores, iqp, ikey, w, ratio, K, rows, c):
         assert not (s & must_out), "row %d takes %s" % (t, sorted(s & must_out)[:5])
         ref = set(O.topk_select(row, nv, K)[0].tolist())
         swaps += len(ref - s)
-    return swaps
+        strict = 1e-6 * abs(kth)
+        wide += sum(1 for e in (ref ^ s) if abs(row[e] - kth) > strict)
+    return (swaps, wide) if detail else swaps
