@@ -523,6 +523,11 @@ def run_ours(args):
         line["note"] = graph_note
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args, full)
+    if ws_ == 1 and not args.shard_of and args.configs:
+        # the benchmark's other configurations, after the headline timing
+        del layers, full
+        torch.cuda.empty_cache()
+        line["configs"] = {k: measure_config(k, dev, args, peaks) for k in args.configs.split(",") if k}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws_ > 1:
@@ -856,12 +861,140 @@ def run_workload(args):
 
 
 # ---------------------------------------------------------------------------
+# The other workloads of the benchmark definition, measured in the same run
+# (one GPU): the CSA layer at S=4096 and at S=65536, and the 43-layer stack at
+# B=2 with the grouped output projection.  Each gets its tokens/s, its
+# roofline and the oracle's time on a bounded sample.
+# ---------------------------------------------------------------------------
+EXTRA_CONFIGS = {
+    "csa_s4096": dict(kind="csa", B=1, S=4096,
+                      workload="DeepSeek-V4-Flash CSA layer fwd (ratio 4 overlapped, indexer 64x128 fp32 scoring, "
+                               "top-512, window 128), B=1, S=4096, H=64, D=512, R=64, bf16"),
+    "csa_s65536": dict(kind="csa", B=1, S=65536,
+                       workload="DeepSeek-V4-Flash long-context CSA layer fwd (ratio 4 overlapped, indexer 64x128 "
+                                "fp32 scoring, top-512, window 128), B=1, S=65536, H=64, D=512, R=64, bf16"),
+    "stack_b2_s16384": dict(kind="stack", B=2, S=16384,
+                            workload="DeepSeek-V4-Flash 43-layer attention stack fwd (2 SWA + 21 CSA + 20 HCA) with "
+                                     "the 8-group x 1024 grouped O projection, B=2, S=16384, H=64, D=512, R=64, "
+                                     "bf16"),
+}
+STACK_COUNTS = {"swa": 2, "csa": 21, "hca": 20}
+
+
+def measure_config(key, dev, args, peaks):
+    """Time one extra workload: warm-up, --cfg-steps timed steps (CUDA events
+    on the launching stream), then one step with per-stage events."""
+    import torch
+
+    import sparse_compressed_attention_gb300 as V
+    c = EXTRA_CONFIGS[key]
+    B, S = c["B"], c["S"]
+    if c["kind"] == "stack":
+        kinds = {k: make_stack_layer(k, B, S, dev, seed=2000 + i) for i, k in enumerate(("swa", "csa", "hca"))}
+        order = [kinds[k] for k in STACK_ORDER]
+        counts = STACK_COUNTS
+    else:
+        L = make_layer("csa_bf16_16k", S, dev, seed=3000)
+        L["name"] = "csa"
+        kinds, order, counts = {"csa": L}, [L], {"csa": 1}
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.cfg_warmup):
+        for L in order:
+            run_layer(L)
+    torch.cuda.synchronize(dev)
+    clk = ClockSampler(smi_index(dev.index or 0))
+    clk.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.cfg_steps):
+        for L in order:
+            run_layer(L)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    clk.stop()
+    ms = ev0.elapsed_time(ev1) / args.cfg_steps
+    V.v4_profile_enable(True)
+    marks = []
+    for L in order:
+        run_layer(L)
+        marks.append((L["name"], V.v4_profile_count()))
+    torch.cuda.synchronize(dev)
+    recs = V.v4_profile_records()
+    V.v4_profile_enable(False)
+    per, start = {}, 0
+    for name, end in marks:
+        for kind, t in recs[start:end]:
+            per.setdefault((name, kind), []).append(t)
+        start = end
+    entry = {"workload": c["workload"], "value": round(B * S / (ms / 1e3), 1), "unit": "tokens/s",
+             "ms_per_step": round(ms, 4), "steps": args.cfg_steps, "warmup": args.cfg_warmup,
+             "global_batch": B, "seq_len": S, "layers_per_step": len(order), "clocks": clk.summary(t0, t1)}
+    wk = layer_work(kinds["csa"]["p"])
+    a = per.get(("csa", "attention"), [])
+    if a:
+        a_ms = sum(a) / len(a)
+        tf = wk["attn_flops"] / (a_ms / 1e3) / 1e12
+        entry["roofline"] = {"kernel": "csa attention", "bound": "tensor", "achieved": round(tf, 2),
+                             "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": round(tf / peaks["bf16"], 4),
+                             "flops_per_launch": wk["attn_flops"], "avg_launch_ms": round(a_ms, 4),
+                             "traffic": None}
+    isc, tk = per.get(("csa", "indexer_scores"), []), per.get(("csa", "topk"), [])
+    if isc and tk:
+        entry["roofline_indexer_unit"] = indexer_unit(wk["idx_flops"], sum(isc) / len(isc), sum(tk) / len(tk),
+                                                      peaks["bf16"])
+    if c["kind"] == "stack":
+        # the whole stack against its roofline: every layer's FLOPs and bytes,
+        # plus the projection's (2*B*S*8*4096*1024 FLOPs, its weights and y)
+        fl = by = 0.0
+        for k, n in counts.items():
+            w = layer_work(kinds[k]["p"])
+            fl += n * (w["layer_flops"] + 2.0 * B * S * 8 * 4096 * 1024)
+            by += n * (w["layer_bytes"] + 8 * 4096 * 1024 * 2 + B * S * 8 * 1024 * 2)
+        t_tc, t_hbm = fl / (peaks["bf16_sustained"] * 1e12) * 1e3, by / (peaks["hbm"] * 1e9) * 1e3
+        entry["roofline_stack"] = {"bound": "tensor" if t_tc >= t_hbm else "hbm", "flops": fl, "bytes": by,
+                                   "bound_ms": round(max(t_tc, t_hbm), 4), "ms": round(ms, 4),
+                                   "frac": round(max(t_tc, t_hbm) / ms, 4),
+                                   "peak_source": "bf16 sustained (a long step) and HBM copy, MEASURED_PEAKS.json"}
+        op = [t for (n, k), v in per.items() if k == "o_proj" for t in v]
+        if op:
+            o_ms = sum(op) / len(op)
+            fl1 = 2.0 * B * S * 8 * 4096 * 1024
+            entry["roofline_o_proj"] = {"kernel": "grouped wo_a projection", "bound": "tensor",
+                                        "achieved": round(fl1 / (o_ms / 1e3) / 1e12, 2), "peak": peaks["bf16"],
+                                        "unit": "TFLOP/s",
+                                        "frac": round(fl1 / (o_ms / 1e3) / 1e12 / peaks["bf16"], 4),
+                                        "avg_launch_ms": round(o_ms, 4)}
+    if not args.no_cpu_baseline:
+        rows = 16
+        while True:
+            inputs = gather_oracle_inputs(list(kinds.values()), rows)
+            est, spent = oracle_sample(inputs, rows, counts)
+            if spent >= args.cfg_cpu_seconds or rows >= S:
+                break
+            rows = min(S, rows * 2)
+        entry["cpu_baseline"] = {"value": round(B * S / est, 3), "unit": "tokens/s", "cores": os.cpu_count(),
+                                 "kind": "oracle",
+                                 "sample": "numpy float64 oracle: full compressors + indexer/attention%s for %d evenly "
+                                           "spaced query rows per layer kind, extrapolated to B=%d, S=%d%s (%.1f s of "
+                                           "CPU work)" % (" + grouped projection" if c["kind"] == "stack" else "",
+                                                          rows, B, S, " and the 2+21+20 layer mix"
+                                                          if c["kind"] == "stack" else "", spent)}
+    del order, kinds
+    torch.cuda.empty_cache()
+    return entry
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle on a bounded sample (rank 0 only)
 # ---------------------------------------------------------------------------
-def oracle_sample(inputs_by_layer, rows_per_layer):
-    """Time the oracle on: the full compressors of both layers, plus indexer
-    and attention for `rows_per_layer` evenly spaced query rows per layer.
-    Returns (seconds extrapolated to all S rows of both layers, seconds spent)."""
+def oracle_sample(inputs_by_layer, rows_per_layer, counts=None):
+    """Time the oracle on: the full compressors of every layer, plus indexer,
+    attention (and, with wo_a, the grouped projection) for `rows_per_layer`
+    evenly spaced query rows per layer.  `counts` (name -> layers of that
+    kind) scales each layer's estimate.  Returns (seconds extrapolated to all
+    S rows of every layer, seconds spent)."""
     from oracle import v4_oracle as O
     total_est = 0.0
     spent = 0.0
@@ -869,9 +1002,10 @@ def oracle_sample(inputs_by_layer, rows_per_layer):
         S = p["S"]
         rows = np.linspace(0, S - 1, rows_per_layer).round().astype(np.int64)
         ta = time.perf_counter()
-        ent = O.compress(x["ckv"], x["cscore"], x["ape"], x["norm_w"], x["inv_freq"], p["ratio"],
-                         p["overlap"], 1e-6, store_bf16=True)
-        ikey = None
+        ent = ikey = None
+        if p["ratio"] > 0:
+            ent = O.compress(x["ckv"], x["cscore"], x["ape"], x["norm_w"], x["inv_freq"], p["ratio"],
+                             p["overlap"], 1e-6, store_bf16=True)
         if p["K"] > 0:
             ikey = O.compress(x["ickv"], x["icscore"], x["iape"], x["inorm_w"], x["inv_freq"],
                               p["ratio"], p["overlap"], 1e-6, hadamard=True, store_bf16=True)
@@ -881,10 +1015,13 @@ def oracle_sample(inputs_by_layer, rows_per_layer):
             sel = O.indexer_topk(x["iq_rows"], ikey, x["w_rows"], x["inv_freq"], p["ratio"], p["K"],
                                  store_bf16=True, rows=rows, rows_only=True)
             idx_rows = sel["idx"]
-        O.sparse_mqa(x["q_rows"], x["kv"], ent, idx_rows, None, x["inv_freq"], p["ratio"], p["W"],
-                     store_bf16=True, rows=rows, rows_only=True)
+        o, _ = O.sparse_mqa(x["q_rows"], x["kv"], ent, idx_rows, None, x["inv_freq"], p["ratio"], p["W"],
+                            store_bf16=True, rows=rows, rows_only=True)
+        if x.get("wo_a") is not None:
+            O.grouped_wo_a(o, x["wo_a"], store_bf16=True)
         tc = time.perf_counter()
-        total_est += (tb - ta) + (tc - tb) * S / len(rows)
+        n = (counts or {}).get(name, 1)
+        total_est += n * ((tb - ta) + (tc - tb) * S / len(rows))
         spent += tc - ta
     return total_est, spent
 
@@ -897,7 +1034,7 @@ def gather_oracle_inputs(layers, rows_per_layer):
         S = p["S"]
         rows = torch.from_numpy(np.linspace(0, S - 1, rows_per_layer).round().astype(np.int64))
         d = {k: x[k].detach().double().cpu().numpy() for k in
-             ("kv", "ckv", "cscore", "ape", "norm_w") if x.get(k) is not None}
+             ("kv", "ckv", "cscore", "ape", "norm_w", "wo_a") if x.get(k) is not None}
         d["inv_freq"] = x["inv_freq"].cpu().numpy()
         d["q_rows"] = x["q"][:, rows.to(x["q"].device)].double().cpu().numpy()
         if p["K"] > 0:
@@ -992,6 +1129,11 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager calls instead of a captured step")
+    ap.add_argument("--configs", default="csa_s4096,csa_s65536,stack_b2_s16384",
+                    help="extra workloads measured after the headline pair (one GPU), comma-separated; '' = none")
+    ap.add_argument("--cfg-steps", type=int, default=5)
+    ap.add_argument("--cfg-warmup", type=int, default=3)
+    ap.add_argument("--cfg-cpu-seconds", type=float, default=4.0)
     ap.add_argument("--split", choices=["contiguous", "zigzag"], default="contiguous",
                     help="N > 1: how the query rows of the sequence are split (both balanced by per-row cost)")
     ap.add_argument("--shard-of", default="", help="r/n: one process times rank r's query rows of an n-GPU "
