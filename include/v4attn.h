@@ -52,7 +52,10 @@ typedef enum {
   V4_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
   V4_ERR_CUDA = 4,          /* a CUDA runtime call failed */
   V4_ERR_TIMEOUT = 5,       /* device status: a bounded wait gave up */
-  V4_ERR_BAD_INDEX = 6      /* device status: a selected index was not visible */
+  V4_ERR_BAD_INDEX = 6,     /* device status: a selected index was not visible */
+  V4_ERR_BOUND = 7          /* device status, V4_DEBUG builds only: an index failed its
+                               bound check (gather row, ring slot, TMEM column) and the
+                               access was skipped */
 } v4_status;
 
 typedef enum { V4_F32 = 0, V4_BF16 = 1 } v4_dtype;
@@ -401,6 +404,10 @@ v4_status v4_attn_layer_fwd(const v4_config* cfg, const v4_layer_inputs* in,
 /* Text of the last non-OK status returned on this host thread ("" if none). */
 const char* v4_last_error(void);
 
+/* Static text naming the build: the target architecture and, for the
+ * bound-checking build (compiled with V4_DEBUG), "V4_DEBUG". */
+const char* v4_build_info(void);
+
 /* Copy the sticky device status word (a v4_status value, 0 = clean) after
  * synchronising `stream`.  v4_reset_device_status clears it (async). */
 v4_status v4_get_device_status(void* stream, int32_t* status);
@@ -408,6 +415,18 @@ v4_status v4_reset_device_status(void* stream);
 
 /* Number of kernels this library has launched since it was loaded. */
 uint64_t v4_launch_count(void);
+
+/* ----------------------------------------------------------------------
+ * Self-test of the device-side failure path (no counterpart in the method).
+ * Launches one warp whose lane 0 waits, with the same bounded wait the
+ * tensor-core kernels use, on a shared-memory barrier that nothing ever
+ * completes; after limit_us microseconds (1 .. 1000000) the wait gives up,
+ * records V4_ERR_TIMEOUT in the sticky device status word and the kernel
+ * returns.  Nothing traps and no tensor-core or TMA work is in flight, so the
+ * context stays usable: the host reads the status with
+ * v4_get_device_status and clears it with v4_reset_device_status.
+ * --------------------------------------------------------------------*/
+v4_status v4_selftest_wait_timeout(int32_t limit_us, void* stream);
 
 /* ----------------------------------------------------------------------
  * Per-stage timing.  While enabled, every stage launch is bracketed by two

@@ -10,4 +10,5 @@ from ._lib import (EXPORTS, V4Error, V4_BF16, V4_F32, V4_PATH_AUTO, V4_PATH_SIMT
                    v4_profile_get, v4_profile_records,
                    v4_reset_device_status, v4_rope_inv_freq, v4_sparse_mqa_fwd, v4_sparse_mqa_fwd_noalloc,
                    v4_workspace_size, v4_bwd_workspace_size, v4_sparse_mqa_bwd, v4_quantize_e4m3,
-                   v4_indexer_topk_e4m3, v4_q_proj, v4_indexer_kl_target)
+                   v4_indexer_topk_e4m3, v4_q_proj, v4_indexer_kl_target, v4_selftest_wait_timeout,
+                   v4_build_info)

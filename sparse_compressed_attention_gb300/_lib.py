@@ -15,12 +15,12 @@ import torch
 from . import build as _build
 
 V4_OK, V4_ERR_INVALID_ARG, V4_ERR_UNSUPPORTED, V4_ERR_WORKSPACE, V4_ERR_CUDA, \
-    V4_ERR_TIMEOUT, V4_ERR_BAD_INDEX = range(7)
+    V4_ERR_TIMEOUT, V4_ERR_BAD_INDEX, V4_ERR_BOUND = range(8)
 V4_F32, V4_BF16 = 0, 1
 V4_PATH_AUTO, V4_PATH_SIMT, V4_PATH_TC = 0, 1, 2
 
 STATUS_NAMES = {0: "V4_OK", 1: "V4_ERR_INVALID_ARG", 2: "V4_ERR_UNSUPPORTED", 3: "V4_ERR_WORKSPACE",
-                4: "V4_ERR_CUDA", 5: "V4_ERR_TIMEOUT", 6: "V4_ERR_BAD_INDEX"}
+                4: "V4_ERR_CUDA", 5: "V4_ERR_TIMEOUT", 6: "V4_ERR_BAD_INDEX", 7: "V4_ERR_BOUND"}
 
 # every symbol include/v4attn.h declares
 EXPORTS = ["v4_rope_inv_freq", "v4_workspace_size", "v4_compress", "v4_indexer_prep",
@@ -28,7 +28,7 @@ EXPORTS = ["v4_rope_inv_freq", "v4_workspace_size", "v4_compress", "v4_indexer_p
            "v4_last_error", "v4_get_device_status", "v4_reset_device_status", "v4_launch_count",
            "v4_profile_enable", "v4_profile_count", "v4_profile_get", "v4_sparse_mqa_fwd_noalloc",
            "v4_bwd_workspace_size", "v4_sparse_mqa_bwd", "v4_quantize_e4m3", "v4_indexer_topk_e4m3",
-           "v4_q_proj", "v4_indexer_kl_target"]
+           "v4_q_proj", "v4_indexer_kl_target", "v4_selftest_wait_timeout", "v4_build_info"]
 PROFILE_KINDS = {0: "compress", 1: "window_rotate", 2: "indexer_prep", 3: "indexer_scores", 4: "topk",
                  5: "attention", 6: "o_proj", 7: "bwd_prep", 8: "bwd_attention", 9: "bwd_derotate",
                  10: "indexer_quant", 11: "q_proj", 12: "kl_target"}
@@ -62,11 +62,13 @@ _lib = None
 
 
 def lib(path=None):
-    """Load the library (once).  Raises if it has not been built."""
+    """Load the library (once).  Raises if it has not been built.  The
+    environment variable V4ATTN_LIB names another build of it (e.g. the
+    bound-checking one, build.DEBUG_LIB)."""
     global _lib
     if _lib is not None:
         return _lib
-    path = path or _build.LIB
+    path = path or os.environ.get("V4ATTN_LIB") or _build.LIB
     if not os.path.exists(path):
         raise RuntimeError("CUDA library %s is missing: build it with "
                            "sparse_compressed_attention_gb300.build.build()" % path)
@@ -93,6 +95,7 @@ def lib(path=None):
         "v4_reset_device_status": [vp],
         "v4_profile_enable": [i32],
         "v4_profile_get": [i32, C.POINTER(i32), C.POINTER(f32)],
+        "v4_selftest_wait_timeout": [i32, vp],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -100,6 +103,8 @@ def lib(path=None):
         fn.restype = C.c_int
     L.v4_last_error.argtypes = []
     L.v4_last_error.restype = C.c_char_p
+    L.v4_build_info.argtypes = []
+    L.v4_build_info.restype = C.c_char_p
     L.v4_launch_count.argtypes = []
     L.v4_launch_count.restype = C.c_uint64
     L.v4_profile_count.argtypes = []
@@ -334,6 +339,10 @@ def v4_last_error():
     return lib().v4_last_error().decode()
 
 
+def v4_build_info():
+    return lib().v4_build_info().decode()
+
+
 def v4_get_device_status(stream=None):
     v = C.c_int32(0)
     _check(lib().v4_get_device_status(_stream(stream), C.byref(v)))
@@ -342,6 +351,11 @@ def v4_get_device_status(stream=None):
 
 def v4_reset_device_status(stream=None):
     _check(lib().v4_reset_device_status(_stream(stream)))
+
+
+def v4_selftest_wait_timeout(limit_us, stream=None):
+    """Launch the self-test kernel whose bounded wait runs out (see the header)."""
+    _check(lib().v4_selftest_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def v4_launch_count():

@@ -765,6 +765,14 @@ v4_status v4_attn_layer_fwd(const v4_config* cfg, const v4_layer_inputs* in, v4_
 
 const char* v4_last_error(void) { return g_err.c_str(); }
 
+const char* v4_build_info(void) {
+#ifdef V4_DEBUG
+  return "sm_103a V4_DEBUG (bound checks)";
+#else
+  return "sm_103a";
+#endif
+}
+
 v4_status v4_get_device_status(void* stream, int32_t* status) {
   if (!status) return fail(V4_ERR_INVALID_ARG, "status is NULL");
   int* p = status_ptr();

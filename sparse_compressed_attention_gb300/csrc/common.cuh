@@ -82,6 +82,17 @@ __device__ __forceinline__ void set_status(int* status, int code) {
 
 constexpr int kStatusTimeout = 5;
 constexpr int kStatusBadIndex = 6;
+constexpr int kStatusBound = 7;
+
+// Bound checks of the V4_DEBUG build (compiled out otherwise): an index that
+// fails its bound records kStatusBound and the guarded access is skipped, so
+// a bad gather row, ring slot or TMEM column shows up in the status word
+// instead of touching memory outside its buffer.
+#ifdef V4_DEBUG
+#define V4_BOUND(cond, status) ((cond) ? true : (::v4::set_status((status), ::v4::kStatusBound), false))
+#else
+#define V4_BOUND(cond, status) true
+#endif
 
 __device__ __forceinline__ int n_visible(long long t, int ratio) {
   return ratio > 0 ? (int)((t + 1) / ratio) : 0;

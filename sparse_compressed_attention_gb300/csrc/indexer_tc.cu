@@ -283,6 +283,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
           // both halves of the query's 64 heads in one wait; four partial
           // sums (heads h mod 4), two of them per paired fp32 FMA
           float v[64];
+          if (!V4_BOUND(256 * ab + 64 * q + 64 <= 512, p.status)) break;   // accumulator columns
           tmem_ld32(tmem + lane_base + 256 * ab + 64 * q, v);
           tmem_ld32(tmem + lane_base + 256 * ab + 64 * q + 32, v + 32);
           tmem_wait_ld();
@@ -301,7 +302,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 #pragma unroll
         for (int qq = 0; qq < 2; ++qq) {
           const int r = r0 + q0 + qq;            // query row, position p.t0 + r
-          if (r < p.Sq && s < min((p.t0 + r + 1) / p.ratio, p.N))
+          if (r < p.Sq && s < min((p.t0 + r + 1) / p.ratio, p.N) && V4_BOUND(b < p.B && s >= 0, p.status))
             p.scores[((size_t)b * p.Sq + r) * p.N + s] = sc[qq];
         }
         ++tile_ct;

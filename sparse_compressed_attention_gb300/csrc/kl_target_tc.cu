@@ -91,7 +91,7 @@ __device__ __forceinline__ bool wait_ok(uint64_t* bar, uint32_t parity, Ctl* c, 
 // 4*grp + lane/8, 16-byte chunk lane%8 (128-byte-swizzled K-major layout);
 // one arrival when the copies land.
 __device__ __forceinline__ void gather_kblock(uint8_t* slot, const bf16* ent, const int* sidx, int gw, int nw,
-                                              int lane, int kb, uint64_t* full) {
+                                              int lane, int kb, uint64_t* full, int n_rows, int* status) {
   const int chunk = lane & 7;
   const bf16* src = ent + kb * 64 + chunk * 8;
   const uint32_t d0 = smem_u32(slot);
@@ -100,7 +100,8 @@ __device__ __forceinline__ void gather_kblock(uint8_t* slot, const bf16* ent, co
     const int grp = gw + nw * i;
     if (grp < 32) {
       const int row = 4 * grp + (lane >> 3);
-      cp_async_16(d0 + row * 128 + ((chunk ^ (row & 7)) << 4), src + (size_t)sidx[i] * kD);
+      if (V4_BOUND(sidx[i] >= 0 && sidx[i] < n_rows, status))
+        cp_async_16(d0 + row * 128 + ((chunk ^ (row & 7)) << 4), src + (size_t)sidx[i] * kD);
     }
   }
   cp_async_mbar_arrive(full);
@@ -245,7 +246,8 @@ kl_target_tc_kernel(const __grid_constant__ CUtensorMap map_q, const Params p) {
           if (lane == 0 && g >= 1) ok = wait_ok(&c->empty[kb], (g - 1) & 1, c, p.status);
           ok = __shfl_sync(0xffffffffu, (int)ok, 0);
           if (!ok) break;
-          gather_kblock(smem + OFF_SLOT + kb * kSlotBytes, p.ent, sidx, 0, 3, lane, kb, &c->full[kb]);
+          gather_kblock(smem + OFF_SLOT + kb * kSlotBytes, p.ent, sidx, 0, 3, lane, kb, &c->full[kb], p.B * p.N,
+                        p.status);
         }
         ++g;
       }
@@ -268,7 +270,8 @@ kl_target_tc_kernel(const __grid_constant__ CUtensorMap map_q, const Params p) {
           if (lane == 0 && g >= 1) ok = wait_ok(&c->empty[kb], (g - 1) & 1, c, p.status);
           ok = __shfl_sync(0xffffffffu, (int)ok, 0);
           if (!ok) break;
-          gather_kblock(smem + OFF_SLOT + kb * kSlotBytes, p.ent, sidx, gw, 3, lane, kb, &c->full[kb]);
+          gather_kblock(smem + OFF_SLOT + kb * kSlotBytes, p.ent, sidx, gw, 3, lane, kb, &c->full[kb], p.B * p.N,
+                        p.status);
         }
         ++g;
       }

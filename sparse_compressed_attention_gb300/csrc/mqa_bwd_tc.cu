@@ -132,7 +132,7 @@ __device__ __forceinline__ bool wait_ok(uint64_t* bar, uint32_t parity, Ctl* c, 
 // One arrival on `full` when this lane's copies have landed.
 __device__ __forceinline__ void gather_tile(uint8_t* kbuf, const QInfo& q, const int32_t* lst, int j, int gl,
                                             const bf16* ent, const bf16* kr, int N, int S, int BN,
-                                            uint64_t* full) {
+                                            uint64_t* full, int kv_rows, int* status) {
 #pragma unroll
   for (int i = 0; i < 3; ++i) {
     const int pr = gl + kGatherLanes * i;
@@ -143,8 +143,10 @@ __device__ __forceinline__ void gather_tile(uint8_t* kbuf, const QInfo& q, const
       const int r = key_row(q, lst, k, N, S, BN);
       const bf16* src = (r < BN ? ent + (size_t)r * kD : kr + (size_t)(r - BN) * kD) + ch * 8;
       const uint32_t d0 = smem_u32(kbuf) + row * 128 + ((ch ^ (row & 7)) << 4);
+      if (V4_BOUND(r >= 0 && r < BN + kv_rows, status)) {
 #pragma unroll
-      for (int kb = 0; kb < 8; ++kb) cp_async_16(d0 + kb * kKBlock, src + kb * 64);
+        for (int kb = 0; kb < 8; ++kb) cp_async_16(d0 + kb * kKBlock, src + kb * 64);
+      }
     }
   }
   cp_async_mbar_arrive(full);
@@ -315,8 +317,8 @@ mqa_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         if (lane == 0 && g >= 2) ok = wait_ok(&c->kempty[g & 1], ((g >> 1) - 1) & 1, c, p.status);
         ok = __shfl_sync(0xffffffffu, (int)ok, 0);
         if (!ok) break;
-        gather_tile(smem + OFF_K + (g & 1) * kKBuf, cur, lst, j, lane, p.ent, p.kr, p.N, p.S, BN,
-                    &c->kfull[g & 1]);
+        gather_tile(smem + OFF_K + (g & 1) * kKBuf, cur, lst, j, lane, p.ent, p.kr, p.N, p.S, BN, &c->kfull[g & 1],
+                    p.B * p.S, p.status);
         if (j == 0) nxt = prepare(qc + 1, item + gridDim.x);
         ++g;
       }
@@ -338,7 +340,8 @@ mqa_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         if (lane == 0 && g >= 2) ok = wait_ok(&c->kempty[g & 1], ((g >> 1) - 1) & 1, c, p.status);
         ok = __shfl_sync(0xffffffffu, (int)ok, 0);
         if (!ok) break;
-        gather_tile(smem + OFF_K + (g & 1) * kKBuf, inf, lst, j, gl, p.ent, p.kr, p.N, p.S, BN, &c->kfull[g & 1]);
+        gather_tile(smem + OFF_K + (g & 1) * kKBuf, inf, lst, j, gl, p.ent, p.kr, p.N, p.S, BN, &c->kfull[g & 1],
+                    p.B * p.S, p.status);
         ++g;
       }
       mbar_arrive(&c->list_free[is]);

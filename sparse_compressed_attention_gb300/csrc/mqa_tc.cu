@@ -127,7 +127,7 @@ constexpr int kMaxGroups = 11;
 // covers row 4*grp + lane/8, 16-byte chunk lane%8, written into the
 // 128-byte-swizzled K-major slot layout; one arrival when the copies land.
 __device__ __forceinline__ void gather_kblock(uint8_t* slot, const bf16* ent_b, const int* sidx, int gw, int nw,
-                                              int lane, int kb, uint64_t* full) {
+                                              int lane, int kb, uint64_t* full, int n_rows, int* status) {
   const int chunk = lane & 7;
   const bf16* src = ent_b + kb * 64 + chunk * 8;
   const uint32_t d0 = smem_u32(slot);
@@ -136,7 +136,8 @@ __device__ __forceinline__ void gather_kblock(uint8_t* slot, const bf16* ent_b, 
     const int grp = gw + nw * i;
     if (grp < 32) {
       const int row = 4 * grp + (lane >> 3);
-      cp_async_16(d0 + row * 128 + ((chunk ^ (row & 7)) << 4), src + (size_t)sidx[i] * kD);
+      if (V4_BOUND(sidx[i] >= 0 && sidx[i] < n_rows && kb >= 0 && kb < kSlots, status))
+        cp_async_16(d0 + row * 128 + ((chunk ^ (row & 7)) << 4), src + (size_t)sidx[i] * kD);
     }
   }
   cp_async_mbar_arrive(full);
@@ -266,7 +267,8 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           int base = 0;
 #pragma unroll
           for (int i = 0; i < kMaxSel / 32; ++i) {
-            if (sv[i] >= 0) lst[base + __popc(msk[i] & below)] = (uint16_t)sv[i];
+            const int pos = base + __popc(msk[i] & below);
+            if (sv[i] >= 0 && V4_BOUND(pos < kMaxSel, p.status)) lst[pos] = (uint16_t)sv[i];
             base += __popc(msk[i]);
           }
           inf.n_ent = base;
@@ -333,7 +335,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             ok = __shfl_sync(0xffffffffu, (int)ok, 0);
             if (!ok) break;
             gather_kblock(smem + OFF_SLOT + kb * kSlotBytes, p.ent + (size_t)cur.b * p.N * kD, sidx, 0, nw, lane,
-                          kb, &c->full_g[kb]);
+                          kb, &c->full_g[kb], p.N, p.status);
           }
         }
         if (j == 0) nxt = prepare(qc + 1, item + gridDim.x);
@@ -377,7 +379,8 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           ok = __shfl_sync(0xffffffffu, (int)ok, 0);
           if (!ok) break;
           if (!contiguous)
-            gather_kblock(smem + OFF_SLOT + kb * kSlotBytes, ent_b, sidx, gw, nw, lane, kb, &c->full_g[kb]);
+            gather_kblock(smem + OFF_SLOT + kb * kSlotBytes, ent_b, sidx, gw, nw, lane, kb, &c->full_g[kb], p.N,
+                          p.status);
         }
         ++g;
       }
@@ -567,7 +570,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       const int nk_total = inf.n_ent + (t - inf.w_lo + 1);
       float lsum = 0.f;                         // this warp's denominator of head h0 + lane
       for (int j = 0; j < inf.tiles; ++j) {
-        const int sb = g & 1;
+        int sb = g & 1;
         bool valid;
         if (j < inf.ent_tiles) {
           valid = j * kTileKeys + krow < inf.n_ent;
@@ -578,6 +581,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         wait_ok(&c->s_full[sb], (g >> 1) & 1, c, p.status);
         tc_fence_after();
         float v[32];
+        if (!V4_BOUND(64 * sb + h0 + 32 <= 128, p.status)) sb = 0;     // S columns [0, 128)
         tmem_ld32(tmem + lane_base + 64 * sb + h0, v);
         tmem_wait_ld();
         uint32_t pk[16];
@@ -593,8 +597,9 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         uint8_t* prow = smem + OFF_P + krow * 16 + (4 * hh) * 2048;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
-          *reinterpret_cast<uint4*>(prow + cc * 2048) =
-              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+          if (V4_BOUND(krow * 16 + (4 * hh + cc) * 2048 + 16 <= (int)kPBytes, p.status))
+            *reinterpret_cast<uint4*>(prow + cc * 2048) =
+                make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&c->p_ready[sb]);
@@ -662,7 +667,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       named_bar_sync(1, kSoftThreads);
       if (ts == 0 && c->redo) {                 // queue the query once for the running-max kernel
         const int slot = atomicAdd(&p.counters[1], 1);
-        p.counters[2 + slot] = b * p.Sq + t - p.t0;
+        if (V4_BOUND(slot < p.B * p.Sq * p.HS, p.status)) p.counters[2 + slot] = b * p.Sq + t - p.t0;
         c->redo = 0;
       }
       float inv_l[32];
@@ -679,6 +684,7 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       bf16* obase = p.o + (((size_t)b * p.Sq + t - p.t0) * p.H + kH * hsl + h0) * kD + krow;
       for (int m = 0; m < 4; ++m) {
         float v[32];
+        if (!V4_BOUND(128 + 64 * m + h0 + 32 <= 384, p.status)) break;   // O columns [128, 384)
         tmem_ld32(tmem + lane_base + 128 + 64 * m + h0, v);
         tmem_wait_ld();
         if (m == 3) {
