@@ -20,7 +20,8 @@ tensor between steps (pooled entries, indexer keys, prepared indexer queries,
 the attention output), the oracle rounds to bf16 (nearest, ties to even) at the
 same point when ``store_bf16`` is set.
 
-Readings of points the pages leave open (each is listed in the design doc):
+Readings of points the pages leave open (the plainest reading consistent with
+the rest of the pages):
   * pooling scores are per channel (a per-token scalar score is the special
     case of a score that is constant across channels);
   * a group member that does not exist (the previous group of entry 0) is left
