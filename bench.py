@@ -94,30 +94,36 @@ def layer_roofline(name, w, kernel_ms, peaks):
             "flops": w["layer_flops"], "bytes": w["layer_bytes"]}
 
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch at
-# S=16384, from one ncu capture of each kernel.  A figure is reported only
-# while its kernel source is unchanged (sha256).
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch
+# from an ncu capture of a smaller case of the same step: (kernel source, its
+# sha256, bytes, sequence length of the capture).  The attention kernel's
+# traffic is q + o, proportional to the query rows, so it is scaled by
+# S / capture length.  A figure is reported only while its kernel source is
+# unchanged.
 NCU_TRAFFIC = {
-    "csa_attention": ("mqa_tc.cu", "9d14665343ab875b9a9c974edb5cd0a8594cd8a6f8a360ca40ded6bfa03ef2ff", 2162648832),
-    "hca_attention": ("mqa_tc.cu", "9d14665343ab875b9a9c974edb5cd0a8594cd8a6f8a360ca40ded6bfa03ef2ff", 2121747968),
-    "csa_indexer": ("indexer_tc.cu", "f649d2ee00405a246972c64eaac6e25974ae18b5f9dabc20e18c441ef48084c2", 398966784),
+    "csa_attention": ("mqa_tc.cu", "1e42e7073199bc8b4719d2d27b6f409ddf58428e35533b17eab1e214d09164ea",
+                      506971904, 4096),
+    "hca_attention": ("mqa_tc.cu", "1e42e7073199bc8b4719d2d27b6f409ddf58428e35533b17eab1e214d09164ea",
+                      493873152, 4096),
 }
 
 
-TRAFFIC_SOURCE = ("dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture of the "
-                  "same kernel source at S=16384 (a constant keyed to the source hash, not measured in this run; "
-                  "null when the kernel changed since)")
+TRAFFIC_SOURCE = ("dram__bytes_read.sum + dram__bytes_write.sum of one launch from an ncu capture of the same "
+                  "kernel source on the S=4096 step, scaled by S/4096 (the kernel's DRAM traffic is q + o); a "
+                  "constant keyed to the source hash, not measured in this run; null when the kernel changed since")
 
 
 def ncu_traffic(key, seq):
     import hashlib
-    src, sha, val = NCU_TRAFFIC[key]
+    if key not in NCU_TRAFFIC:
+        return None
+    src, sha, val, seq0 = NCU_TRAFFIC[key]
     path = os.path.join(ROOT, "sparse_compressed_attention_gb300", "csrc", src)
     try:
         cur = hashlib.sha256(open(path, "rb").read()).hexdigest()
     except OSError:
         return None
-    return val if (cur == sha and seq == 16384) else None
+    return int(round(val * seq / seq0)) if cur == sha else None
 
 
 def indexer_unit(flops, scores_ms, topk_ms, peak):

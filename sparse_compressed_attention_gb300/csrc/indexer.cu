@@ -74,7 +74,11 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-constexpr int kTopkThreads = 256;
+// Four warps per row: the per-row fixed work (block barriers, the digit
+// scan, clears, compaction offsets) is shared by fewer warps and more rows
+// are resident per SM (measured 0.162 -> 0.156 ms at S=16384, 0.031 ->
+// 0.024 ms at B=2, S=3000, K=64 against eight warps per row).
+constexpr int kTopkThreads = 128;
 
 // One block per (query row i, batch b), position t = t0 + i: exact top-K of
 // the row's n_vis(t) scores.  The row is
@@ -131,7 +135,7 @@ __device__ __forceinline__ void hist_add4(int* whist, uint4 k4, int s, int nv, u
   }
 }
 
-__global__ void __launch_bounds__(kTopkThreads, 8)
+__global__ void __launch_bounds__(kTopkThreads, 12)
 topk_kernel(const float* __restrict__ scores, int32_t* __restrict__ idx, float* __restrict__ iscore,
             int Sq, int t0, int N, int K, int ratio, int smem_cap) {
   extern __shared__ uint4 skeys4[];
@@ -185,8 +189,7 @@ topk_kernel(const float* __restrict__ scores, int32_t* __restrict__ idx, float* 
       __syncthreads();
     }
     // totals per digit
-    {
-      const int d = tid;                       // kTopkThreads == 256 digits
+    for (int d = tid; d < 256; d += kTopkThreads) {
       int sum = 0;
 #pragma unroll
       for (int w = 0; w < kTopkWarps; ++w) sum += s_hist[w][d];
