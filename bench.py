@@ -313,7 +313,8 @@ def rank_chunks(p, world, rank, split="contiguous"):
     per-row cost: one contiguous range, or the zig-zag pair of chunks (the
     whole sequence at N=1)."""
     from sparse_compressed_attention_gb300 import rows as R
-    cost = R.layer_cost(p["ratio"], p["K"], p["W"], heads=p["H"], dim=p["D"], idx_heads=p["Hi"], idx_dim=p["Di"])
+    cost = R.layer_cost(p["ratio"], p["K"], p["W"], heads=p["H"], dim=p["D"], idx_heads=p["Hi"], idx_dim=p["Di"],
+                        tile=128)
     if world == 1:
         return [(0, p["S"])]
     if split == "zigzag":

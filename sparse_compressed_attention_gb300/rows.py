@@ -100,10 +100,25 @@ def row_bytes(ratio, topk, heads=64, dim=512, idx_heads=64, idx_dim=128):
     return b
 
 
-def layer_cost(ratio, topk, window, flop_per_byte=FLOP_PER_BYTE, **shape):
-    """Per-row cost of one layer in flop-equivalents: its FLOPs plus its HBM
-    bytes at the machine balance."""
+def row_tile_flops(t, ratio, topk, window, tile=128, heads=64, dim=512, idx_heads=64, idx_dim=128):
+    """row_flops with the attention keys rounded up to whole key tiles: the
+    tensor-core attention runs a ragged tile (a short selection, a window cut
+    by the sequence start) as a full one."""
+    nv = (t + 1) // ratio if ratio > 0 else 0
+    ent = (min(nv, topk) if topk > 0 else nv) if ratio > 0 else 0
+    win = t + 1 if window < 0 else min(t + 1, window)
+    idx = 2 * idx_heads * idx_dim * nv if (ratio > 0 and topk > 0) else 0
+    tiles = -(-ent // tile) + -(-win // tile)
+    return idx + 4 * heads * dim * tile * tiles
+
+
+def layer_cost(ratio, topk, window, flop_per_byte=FLOP_PER_BYTE, tile=None, **shape):
+    """Per-row cost of one layer in flop-equivalents: its FLOPs (attention keys
+    rounded to whole tiles when `tile` is given) plus its HBM bytes at the
+    machine balance."""
     rb = row_bytes(ratio, topk, **shape) * flop_per_byte
+    if tile:
+        return lambda t: row_tile_flops(t, ratio, topk, window, tile=tile, **shape) + rb
     return lambda t: row_flops(t, ratio, topk, window, **shape) + rb
 
 

@@ -84,6 +84,15 @@ def test_contiguous_cost_split_covers_once_and_balances(layer, world):
     assert max(loads) / min(loads) - 1 < 0.002
 
 
+def test_tile_cost_charges_ragged_tiles_in_full():
+    # 5 selected entries and a window cut to 21 tokens: two 128-key tiles
+    assert R.row_tile_flops(20, 4, 512, 128) == 2 * 64 * 128 * 5 + 4 * 64 * 512 * 128 * 2
+    # a full selection and window: the same as the exact count
+    assert R.row_tile_flops(8191, 4, 512, 128) == R.row_flops(8191, 4, 512, 128)
+    c = R.layer_cost(4, 512, 128, tile=128)
+    assert c(20) > R.layer_cost(4, 512, 128)(20)
+
+
 def test_rejects_bad_arguments():
     with pytest.raises(ValueError):
         R.zigzag_chunks(10, 2, 2)
