@@ -52,3 +52,29 @@ def test_layer_rooflines_at_the_benchmark_sizes():
     assert abs(rc["bound_ms"] - csa["layer_flops"] / 1932.6e12 * 1e3) < 1e-4
     at_bound = bench.layer_roofline("hca", hca, hca["layer_bytes"] / 6779e9 * 1e3, peaks)
     assert abs(at_bound["frac"] - 1.0) < 1e-3
+
+
+def test_row_chunk_work_adds_up_to_the_whole_sequence():
+    """The work of a rank's query rows: the chunks of a split add up to the
+    whole layer's FLOPs (attention keys and indexer pairs) and q + o bytes."""
+    from sparse_compressed_attention_gb300 import rows as R
+    for name in ("csa_bf16_16k", "hca_bf16_16k"):
+        p = SI.preset(name, S=3000)
+        whole = bench.layer_work(p)
+        cost = R.layer_cost(p["ratio"], p["K"], p["W"], tile=128)
+        parts = [bench.layer_work(p, R.contiguous_chunks(p["S"], 4, r, cost)) for r in range(4)]
+        for key in ("attn_flops", "attn_bytes", "idx_flops", "attn_keys", "idx_pairs"):
+            assert sum(w[key] for w in parts) == whole[key], (name, key)
+        # bench's rank chunks: whole sequence at N=1, the contiguous split otherwise
+        assert bench.rank_chunks(p, 1, 0) == [(0, p["S"])]
+        assert sum(b - a for r in range(3) for a, b in bench.rank_chunks(p, 3, r)) == p["S"]
+
+
+def test_stack_mix_and_its_roofline_inputs():
+    """The 43-layer stack the bench measures: 2 window-only + 21 CSA + 20 HCA
+    layers in the Flash order, and the per-kind counts its roofline sums."""
+    assert bench.STACK_ORDER[:2] == ["swa", "swa"] and bench.STACK_ORDER[-1] == "csa"
+    assert {k: bench.STACK_ORDER.count(k) for k in set(bench.STACK_ORDER)} == bench.STACK_COUNTS
+    assert sum(bench.STACK_COUNTS.values()) == 43
+    ratios = [{"swa": 0, "csa": 4, "hca": 128}[k] for k in bench.STACK_ORDER]
+    assert ratios == SI.flash_layer_ratios()
