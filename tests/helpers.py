@@ -122,3 +122,86 @@ def check_topk_rows(gpu_idx, scores, iqp, ikey, w, ratio, K, rows, c, detail=Fal
         strict = 1e-6 * abs(kth)
         wide += sum(1 for e in (ref ^ s) if abs(row[e] - kth) > strict)
     return (swaps, wide) if detail else swaps
+
+
+def check_attention_rows(o, lse, ro, rl, tol=1e-2):
+    """Attention outputs against the oracle: relative L2 over all rows,
+    every row within 5 * tol, and lse within the bf16 operand error."""
+    assert rel_l2(o, ro) < tol
+    B, S, H, D = o.shape
+    num = np.linalg.norm((o - ro).reshape(B * S, -1), axis=1)
+    den = np.linalg.norm(ro.reshape(B * S, -1), axis=1) + 1e-30
+    assert np.max(num / den) < 5 * tol, "worst row %d: %.3e" % (np.argmax(num / den), np.max(num / den))
+    fin = np.isfinite(rl)
+    assert np.array_equal(fin, np.isfinite(lse))
+    # the kernel feeds the tensor cores bf16 copies of the rotated query and
+    # window keys: a relative 2^-8 on the rotated part of each logit
+    assert np.all(np.abs(lse[fin] - rl[fin]) < 2e-2 + 4e-3 * np.abs(rl[fin]))
+
+
+def check_layer_sampled_rows(p, x, outs, rows, f, iqp, b=0, tol=1e-2):
+    """Oracle check of batch element b of a whole-layer call on sampled query
+    rows, all heads: the stored entries (and index keys), the top-K sets of
+    those rows (>= 99% agreement, and at most two swaps in the tie band, none
+    outside the strict 1e-6 * |I_K| band beyond two), o and lse, and the
+    projected rows y when the call made them.
+
+    x: the layer's inputs (any device); outs: its outputs; iqp: the
+    library's own prepared indexer queries [B, S, Hi, Di] (CSA), for the
+    stage-wise selection check; f: the rotary inverse frequencies.
+    """
+    sl = slice(b, b + 1)
+    K = p["K"]
+    rws = torch.from_numpy(np.asarray(rows)).to(x["q"].device)
+    ent = None
+    if p["ratio"] > 0:
+        ent = O.compress(np64(x["ckv"][sl]), np64(x["cscore"][sl]), np64(x["ape"]), None, f, p["ratio"],
+                         p["overlap"], 1e-6, store_bf16=True)
+        assert rel_l2(np64(outs["ent"][sl]), ent) < 1e-3
+    idx_rows = None
+    if K:
+        ikey = O.compress(np64(x["ickv"][sl]), np64(x["icscore"][sl]), np64(x["iape"]), None, f, p["ratio"],
+                          p["overlap"], 1e-6, hadamard=True, store_bf16=True)
+        assert rel_l2(np64(outs["ikey"][sl]), ikey) < 1e-3
+        iq_rows = np64(x["iq"][sl][:, rws])
+        w_rows = np64(x["w"][sl][:, rws])
+        sel = O.indexer_topk(iq_rows, ikey, w_rows, f, p["ratio"], K, store_bf16=True, rows=rows, rows_only=True)
+        gi = outs["idx"][b, rws.to(outs["idx"].device)].cpu().numpy()
+        agree = total = 0
+        for i in range(len(rows)):
+            a = set(gi[i][gi[i] >= 0].tolist())
+            r = set(sel["idx"][0, i][sel["idx"][0, i] >= 0].tolist())
+            assert len(a) == len(r)
+            agree += len(a & r)
+            total += len(r)
+        assert agree >= 0.99 * total, (agree, total)
+        idx_rows = sel["idx"]
+        # stage-wise: the oracle's scores of the library's own prepared
+        # queries and index keys select the same sets outside the tie band
+        iqp_rows = np64(iqp[sl][:, rws.to(iqp.device)])
+        ikey_g = np64(outs["ikey"][sl])
+        sc = O.indexer_scores(iqp_rows, ikey_g, w_rows, p["ratio"], rows=rows, rows_only=True)[0]
+        S = p["S"]
+        iqp_full = np.zeros((S,) + iqp_rows.shape[2:])
+        iqp_full[rows] = iqp_rows[0]
+        w_full = np.zeros((S, p["Hi"]))
+        w_full[rows] = w_rows[0]
+        swaps, wide = check_topk_rows(gi, sc, iqp_full, ikey_g[0], w_full, p["ratio"], K, rows,
+                                      O.indexer_scale(p["Hi"], p["Di"]), detail=True)
+        print("batch %d sampled rows: in-band swaps %d, swaps outside 1e-6*|I_K| %d" % (b, swaps, wide))
+        assert swaps <= 2, swaps
+        assert wide <= 2, wide            # only the fp32 error bound would allow these
+    q_rows = np64(x["q"][sl][:, rws])
+    # the oracle attends with its own entries and its own selection
+    ro, rl = O.sparse_mqa(q_rows, np64(x["kv"][sl]), ent, idx_rows, None, f, p["ratio"], p["W"],
+                          store_bf16=True, rows=rows, rows_only=True)
+    go = np64(outs["o"][sl][:, rws.to(outs["o"].device)])
+    gl = np64(outs["lse"][sl][:, rws.to(outs["lse"].device)])
+    check_attention_rows(go, gl, ro, rl, tol)
+    if "y" in outs:
+        ry = O.grouped_wo_a(ro, np64(x["wo_a"]), store_bf16=True)
+        gy = np64(outs["y"][sl][:, rws.to(outs["y"].device)])
+        assert rel_l2(gy, ry) < tol
+        num = np.linalg.norm((gy - ry).reshape(len(rows), -1), axis=1)
+        den = np.linalg.norm(ry.reshape(len(rows), -1), axis=1) + 1e-30
+        assert np.max(num / den) < 5 * tol

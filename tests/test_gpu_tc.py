@@ -14,7 +14,7 @@ import torch
 import seeded_inputs as SI
 import sparse_compressed_attention_gb300 as V
 from oracle import v4_oracle as O
-from tests.helpers import check_topk_rows, inv_freq_for, np64, rel_l2, to_dev
+from tests.helpers import check_attention_rows, check_layer_sampled_rows, inv_freq_for, np64, rel_l2, to_dev
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-2
@@ -58,16 +58,7 @@ def _run(p, mode, sink, path, seed=0, q_scale=1.0, idx_seed=7):
 
 
 def _check(o, lse, ro, rl, tol=TOL):
-    assert rel_l2(o, ro) < tol
-    B, S, H, D = o.shape
-    num = np.linalg.norm((o - ro).reshape(B * S, -1), axis=1)
-    den = np.linalg.norm(ro.reshape(B * S, -1), axis=1) + 1e-30
-    assert np.max(num / den) < 5 * tol, "worst row %d: %.3e" % (np.argmax(num / den), np.max(num / den))
-    fin = np.isfinite(rl)
-    assert np.array_equal(fin, np.isfinite(lse))
-    # the kernel feeds the tensor cores bf16 copies of the rotated query and
-    # window keys: a relative 2^-8 on the rotated part of each logit
-    assert np.all(np.abs(lse[fin] - rl[fin]) < 2e-2 + 4e-3 * np.abs(rl[fin]))
+    check_attention_rows(o, lse, ro, rl, tol)
 
 
 CASES = [
@@ -146,46 +137,5 @@ def test_full_size_layer_sampled_rows(name):
     assert V.v4_get_device_status() == 0
     rows = np.unique(np.concatenate([np.linspace(0, S - 1, 504).round().astype(int),
                                      [0, 1, 127, 128, 511, 512, 2047, S - 1]]))
-    ent = O.compress(np64(x["ckv"]), np64(x["cscore"]), np64(x["ape"]), None, f, p["ratio"], p["overlap"],
-                     1e-6, store_bf16=True)
-    assert rel_l2(np64(outs["ent"]), ent) < 1e-3
-    idx_rows = None
-    if K:
-        ikey = O.compress(np64(x["ickv"]), np64(x["icscore"]), np64(x["iape"]), None, f, p["ratio"],
-                          p["overlap"], 1e-6, hadamard=True, store_bf16=True)
-        iq_rows = np64(x["iq"][:, torch.from_numpy(rows).cuda()])
-        w_rows = np64(x["w"][:, torch.from_numpy(rows).cuda()])
-        sel = O.indexer_topk(iq_rows, ikey, w_rows, f, p["ratio"], K, store_bf16=True, rows=rows,
-                             rows_only=True)
-        gi = outs["idx"][0, torch.from_numpy(rows).cuda()].cpu().numpy()
-        agree = total = 0
-        for i in range(len(rows)):
-            a = set(gi[i][gi[i] >= 0].tolist())
-            r = set(sel["idx"][0, i][sel["idx"][0, i] >= 0].tolist())
-            assert len(a) == len(r)
-            agree += len(a & r)
-            total += len(r)
-        assert agree >= 0.99 * total, (agree, total)
-        idx_rows = sel["idx"]
-        # stage-wise: the oracle's scores fed the GPU's own prepared queries
-        # and index keys select the same sets outside the tie band
-        iqp_g = V.v4_indexer_prep(cfg, x["iq"], xd["inv_freq"], torch.empty_like(x["iq"]))
-        iqp_rows = np64(iqp_g[:, torch.from_numpy(rows).cuda()])
-        ikey_g = np64(outs["ikey"])
-        sc = O.indexer_scores(iqp_rows, ikey_g, w_rows, p["ratio"], rows=rows, rows_only=True)[0]
-        iqp_full = np.zeros((S,) + iqp_rows.shape[2:])
-        iqp_full[rows] = iqp_rows[0]
-        w_full = np.zeros((S, p["Hi"]))
-        w_full[rows] = w_rows[0]
-        swaps, wide = check_topk_rows(gi, sc, iqp_full, ikey_g[0], w_full, p["ratio"], K, rows,
-                                      O.indexer_scale(p["Hi"], p["Di"]), detail=True)
-        print("sampled rows: in-band swaps %d, swaps outside 1e-6*|I_K| %d" % (swaps, wide))
-        assert swaps <= 2, swaps
-        assert wide <= 2, wide            # only the fp32 error bound would allow these
-    q_rows = np64(x["q"][:, torch.from_numpy(rows).cuda()])
-    # the oracle attends with its own entries and its own selection
-    ro, rl = O.sparse_mqa(q_rows, np64(x["kv"]), ent, idx_rows, None, f, p["ratio"], p["W"],
-                          store_bf16=True, rows=rows, rows_only=True)
-    go = np64(outs["o"][:, torch.from_numpy(rows).cuda()])
-    gl = np64(outs["lse"][:, torch.from_numpy(rows).cuda()])
-    _check(go, gl, ro, rl)
+    iqp = V.v4_indexer_prep(cfg, x["iq"], xd["inv_freq"], torch.empty_like(x["iq"])) if K else None
+    check_layer_sampled_rows(p, x, outs, rows, f, iqp)
