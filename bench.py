@@ -109,8 +109,20 @@ NCU_TRAFFIC = {
 
 
 TRAFFIC_SOURCE = ("dram__bytes_read.sum + dram__bytes_write.sum of one launch from an ncu capture of the same "
-                  "kernel source on the S=4096 step, scaled by S/4096 (the kernel's DRAM traffic is q + o); a "
-                  "constant keyed to the source hash, not measured in this run; null when the kernel changed since")
+                  "kernel source on the B=1, S=4096 step, scaled by the query rows B*S / 4096 (the kernel's DRAM "
+                  "traffic is q + o); a constant keyed to the source hash, not measured in this run; null when "
+                  "the kernel changed since")
+
+
+def traffic_fields(key, seq, world):
+    """The roofline's traffic and where it comes from (null with the reason
+    when no capture of the kernel's current source exists)."""
+    t = ncu_traffic(key, seq) if world == 1 else None
+    if t is not None:
+        return {"traffic": t, "traffic_source": TRAFFIC_SOURCE}
+    why = ("no DRAM capture of this kernel's current source" if world == 1 else
+           "not given for a row slice (the capture covers whole-sequence launches)")
+    return {"traffic": None, "traffic_source": why}
 
 
 def ncu_traffic(key, seq):
@@ -465,8 +477,7 @@ def run_ours(args):
         roof = {"kernel": "csa attention (sparse MQA, 64 heads x 512, top-512 + window 128)",
                 "bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16"],
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4),
-                "traffic": ncu_traffic("csa_attention", S) if ws_ == 1 else None,
-                "traffic_source": TRAFFIC_SOURCE,
+                **traffic_fields("csa_attention", S, ws_),
                 "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % peaks["src"],
                 "flops_per_launch": work["csa_bf16_16k"]["attn_flops"] / nlaunch["csa_bf16_16k"],
                 "avg_launch_ms": round(a_ms / nlaunch["csa_bf16_16k"], 4),
@@ -477,8 +488,7 @@ def run_ours(args):
         gbs = work["hca_bf16_16k"]["attn_bytes"] / (a_ms / 1e3) / 1e9
         extra_roofs.append({"kernel": "hca attention", "bound": "hbm", "achieved": round(gbs, 1),
                             "peak": peaks["hbm"], "unit": "GB/s", "frac": round(gbs / peaks["hbm"], 4),
-                            "traffic": ncu_traffic("hca_attention", S) if ws_ == 1 else None,
-                            "traffic_source": TRAFFIC_SOURCE,
+                            **traffic_fields("hca_attention", S, ws_),
                             "bytes_per_launch": work["hca_bf16_16k"]["attn_bytes"] / nlaunch["hca_bf16_16k"],
                             "avg_launch_ms": round(a_ms / nlaunch["hca_bf16_16k"], 4),
                             "launches_per_step": nlaunch["hca_bf16_16k"]})
@@ -487,8 +497,7 @@ def run_ours(args):
         tf = work["csa_bf16_16k"]["idx_flops"] / (s_ms / 1e3) / 1e12
         extra_roofs.append({"kernel": "csa indexer scores", "bound": "tensor", "achieved": round(tf, 2),
                             "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": round(tf / peaks["bf16"], 4),
-                            "traffic": ncu_traffic("csa_indexer", S) if ws_ == 1 else None,
-                            "traffic_source": TRAFFIC_SOURCE,
+                            **traffic_fields("csa_indexer", S, ws_),
                             "flops_per_launch": work["csa_bf16_16k"]["idx_flops"] / nlaunch["csa_bf16_16k"],
                             "avg_launch_ms": round(s_ms / nlaunch["csa_bf16_16k"], 4)})
         tk = per_step_ms(("csa_bf16_16k", "topk"))
@@ -686,7 +695,9 @@ def run_qproj(args):
                                    "B=1, S=%d" % S, "global_batch": 1, "seq_len": S},
             "clocks": clk.summary(t0, t1), "gpu_launches": V.v4_launch_count() - launches0,
             "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16"], "unit": "TFLOP/s",
-                         "frac": round(tf / peaks["bf16"], 4), "traffic": None, "flops_per_launch": flops}}
+                         "frac": round(tf / peaks["bf16"], 4), "traffic": None,
+                         "traffic_source": "no DRAM capture of this kernel's current source",
+                         "flops_per_launch": flops}}
     print(json.dumps(line), flush=True)
 
 
@@ -745,7 +756,9 @@ def run_kl(args):
             "clocks": clk.summary(t0, t1), "gpu_launches": V.v4_launch_count() - launches0,
             "device_status": V.v4_get_device_status(),
             "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16"], "unit": "TFLOP/s",
-                         "frac": round(tf / peaks["bf16"], 4), "traffic": None, "flops_per_launch": flops}}
+                         "frac": round(tf / peaks["bf16"], 4), "traffic": None,
+                         "traffic_source": "no DRAM capture of this kernel's current source",
+                         "flops_per_launch": flops}}
     print(json.dumps(line), flush=True)
 
 
@@ -831,7 +844,8 @@ def run_workload(args):
         a_ms = sum(a) / len(a)
         tf = wk["attn_flops"] / (a_ms / 1e3) / 1e12
         roof = {"kernel": "csa attention", "bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16"],
-                "unit": "TFLOP/s", "frac": round(tf / peaks["bf16"], 4), "traffic": None,
+                "unit": "TFLOP/s", "frac": round(tf / peaks["bf16"], 4),
+                **traffic_fields("csa_attention", csa["p"]["B"] * csa["p"]["S"], 1),
                 "flops_per_launch": wk["attn_flops"], "avg_launch_ms": round(a_ms, 4)}
     isc = per.get(("csa", "indexer_scores"), [])
     if isc:
@@ -946,7 +960,7 @@ def measure_config(key, dev, args, peaks):
         entry["roofline"] = {"kernel": "csa attention", "bound": "tensor", "achieved": round(tf, 2),
                              "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": round(tf / peaks["bf16"], 4),
                              "flops_per_launch": wk["attn_flops"], "avg_launch_ms": round(a_ms, 4),
-                             "traffic": None}
+                             **traffic_fields("csa_attention", B * S, 1)}
     isc, tk = per.get(("csa", "indexer_scores"), []), per.get(("csa", "topk"), [])
     if isc and tk:
         entry["roofline_indexer_unit"] = indexer_unit(wk["idx_flops"], sum(isc) / len(isc), sum(tk) / len(tk),
