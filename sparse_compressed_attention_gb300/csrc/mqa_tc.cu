@@ -8,10 +8,14 @@
 // attention types, interleaved" and "Kernel fusions" (row "SWA / CSA / HCA
 // attention": in-kernel gather of the selected entries, window branch and
 // sink in one softmax); Primus PR #930 item 1 (scale D^-1/2) and item 3
-// (output de-rotated at -t).  The page's "fixed max via shift invariance"
-// idea (section "Attention kernels for the three layer types") is used with
-// a provable bound: m_h = scale * |q_h| * max_k |k| >= every logit, so the
-// softmax needs no running max and no rescaling; partial sums simply add.
+// (output de-rotated at -t).  The softmax follows the page's "fixed max via
+// shift invariance" (section "Attention kernels for the three layer types"):
+// each head's largest logit over the query's first key tile is the shift
+// for all its tiles, so there is no running max and no rescaling and
+// partial sums simply add.  A later key above that shift only makes its P
+// exceed 1; a query whose denominator leaves [nk * 1e-26, 2^100) (an
+// overflow, or mass lost to underflow) is recomputed by the CUDA-core
+// kernel with a running max.
 //
 // Layout per query t (one CTA, persistent over queries):
 //   S^T[key, head] = K_tile[128 keys x 512] . Q^T          (M=128 keys, N=64)
@@ -84,6 +88,7 @@ struct Ctl {
   uint64_t fin;
   QInfo info[2];
   float mlog2[2][kH];          // per-query shift (log2 units), double-buffered by query parity
+  float hmax[4][kH];           // first tile: each TMEM lane quarter's largest logit per head
   uint32_t tmem_base;
   int abort;
   int decision;
@@ -497,10 +502,8 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       named_bar_sync(1, kSoftThreads);
       return more;
     };
-    // Rotate the last 64 dims of each head of query qc at position t, take
-    // the head norms of the stored bf16 values and publish the shift table.
-    // Four threads per head: two 16-byte chunks of the rotated K-block and
-    // two K-blocks of the norm each.
+    // Rotate the last 64 dims of each head of query qc at position t (four
+    // threads per head, two 16-byte chunks each) and publish the rows.
     auto setup_query = [&](int qc, const QInfo& inf) {
       const int h = ts >> 2, part = ts & 3;
       // cos/sin of this thread's 8 rotation pairs, fetched before the wait
@@ -528,36 +531,8 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         }
         *ptr = u;
       }
-      __syncwarp();                            // the head's four threads share this warp
-      float ss4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        const int kb = 2 * part + kk;
-        const uint4* r = reinterpret_cast<const uint4*>(smem + OFF_Q + kb * kQBlockBytes + h * 128);
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          uint4 u = r[cc ^ (h & 7)];            // spread the heads of a warp over the banks
-          const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float2 f = __bfloat1622float2(hv[i]);
-            ss4[i] = fmaf(f.x, f.x, ss4[i]);
-            ss4[i] = fmaf(f.y, f.y, ss4[i]);
-          }
-        }
-      }
-      float ss = (ss4[0] + ss4[1]) + (ss4[2] + ss4[3]);
-      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-      if (part == 0) {
-        float m = p.scale * sqrtf(ss) * inf.kmax;
-        m = m * (1.0f + 1e-5f) + 1e-6f;                     // covers rounding of the bound itself
-        if (p.sink != nullptr) m = fmaxf(m, p.sink[kH * inf.hs + h]);
-        c->mlog2[qc & 1][h] = m * log2e;
-      }
       fence_proxy_async_smem();
-      named_bar_sync(1, kSoftThreads);
-      mbar_arrive(&c->q_ready);
+      mbar_arrive(&c->q_ready);                // the products wait for all 256 arrivals
     };
 
     int qc = 0, g = 0;
@@ -584,6 +559,35 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         if (!V4_BOUND(64 * sb + h0 + 32 <= 128, p.status)) sb = 0;     // S columns [0, 128)
         tmem_ld32(tmem + lane_base + 64 * sb + h0, v);
         tmem_wait_ld();
+        if (j == 0) {
+          // the query's shift: each head's largest logit over this tile's
+          // valid keys (the tile always holds one: entry 0 or the query's
+          // own token).  Five butterfly rounds leave lane L with head h0 + L
+          // of this warp's 32 rows, the four lane quarters meet in shared
+          // memory.
+          float r[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = valid ? v[i] : -INFINITY;
+#pragma unroll
+          for (int o = 16, w = 16; o >= 1; o >>= 1, w >>= 1) {
+            const bool hi = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < w; ++i) {
+              const float send = hi ? r[i] : r[w + i];
+              const float keep = hi ? r[w + i] : r[i];
+              r[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
+            }
+          }
+          c->hmax[quarter][h0 + lane] = r[0];
+          named_bar_sync(1, kSoftThreads);
+          // lane L publishes head h0 + L's shift for its warp (the four
+          // warps of a head half write the same values)
+          const int hd = h0 + lane;
+          float m = fmaxf(fmaxf(c->hmax[0][hd], c->hmax[1][hd]), fmaxf(c->hmax[2][hd], c->hmax[3][hd])) * c1;
+          if (p.sink != nullptr) m = fmaxf(m, p.sink[kH * hsl + hd] * log2e);
+          c->mlog2[qc & 1][hd] = m;
+          __syncwarp();
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -658,8 +662,9 @@ mqa_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         float l = (hs[ts] + hs[64 + ts]) + (hs[128 + ts] + hs[192 + ts]);
         const float m = mlog2_all[ts] * 0.6931471805599453f;
         if (p.sink != nullptr) l += expf(p.sink[kH * hsl + ts] - m);
-        // too little mass under the bound: exp underflow may have lost keys
-        const bool bad = !(l >= (float)nk_total * 1.0e-26f) || !(l < INFINITY);
+        // too little mass under the shift (exp underflow may have lost keys)
+        // or so much above it that the fp32 output sums could overflow
+        const bool bad = !(l >= (float)nk_total * 1.0e-26f) || !(l < 0x1p100f);
         if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&c->redo, 1);
         if (p.lse) p.lse[((size_t)b * p.Sq + t - p.t0) * p.H + kH * hsl + ts] = m + logf(l);
         hs[256 + ts] = 1.0f / l;
