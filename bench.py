@@ -101,10 +101,10 @@ def layer_roofline(name, w, kernel_ms, peaks):
 # S / capture length.  A figure is reported only while its kernel source is
 # unchanged.
 NCU_TRAFFIC = {
-    "csa_attention": ("mqa_tc.cu", "1e42e7073199bc8b4719d2d27b6f409ddf58428e35533b17eab1e214d09164ea",
-                      506971904, 4096),
-    "hca_attention": ("mqa_tc.cu", "1e42e7073199bc8b4719d2d27b6f409ddf58428e35533b17eab1e214d09164ea",
-                      493873152, 4096),
+    "csa_attention": ("mqa_tc.cu", "758f21ab174dce6f6663aa4a8742805787fdc833af4c7b4cc7fe5bd0bf72bc74",
+                      507511296, 4096),
+    "hca_attention": ("mqa_tc.cu", "758f21ab174dce6f6663aa4a8742805787fdc833af4c7b4cc7fe5bd0bf72bc74",
+                      493794560, 4096),
 }
 
 

@@ -130,7 +130,6 @@ Workspace plan_workspace(const v4_config& c) {
   take(w.iqp, w.iqp_bytes, sel && !c.indexer_fp8 ? B * Sq * c.idx_heads * c.idx_dim * es : 0);
   take(w.scores, w.scores_bytes, sel ? B * Sq * N * 4 : 0);
   take(w.idx, w.idx_bytes, sel ? B * Sq * c.topk * 4 : 0);
-  take(w.knorm, w.knorm_bytes, key_norm_floats(c) * 4);
   // redo list: one entry per (query, 64-head slice) at most
   take(w.counters, w.counters_bytes, (2 + B * Sq * (size_t)(c.n_heads > 64 ? (c.n_heads + 63) / 64 : 1)) * 4);
   take(w.rope, w.rope_bytes, S * (size_t)(c.rope_dim / 2) * 8);
@@ -143,10 +142,10 @@ Workspace plan_workspace(const v4_config& c) {
   return w;
 }
 
-// Backward workspace: cos/sin table, rotated window keys with their norms,
-// rotated queries and output gradients, delta.
+// Backward workspace: cos/sin table, rotated window keys, rotated queries
+// and output gradients, delta.
 struct BwdWorkspace {
-  size_t rope = 0, kv_rot = 0, knorm = 0, qr = 0, dor = 0, delta = 0, total = 0;
+  size_t rope = 0, kv_rot = 0, qr = 0, dor = 0, delta = 0, total = 0;
 };
 
 static BwdWorkspace plan_bwd_workspace(const v4_config& c) {
@@ -160,7 +159,6 @@ static BwdWorkspace plan_bwd_workspace(const v4_config& c) {
   };
   take(w.rope, S * (size_t)(c.rope_dim / 2) * 8);
   take(w.kv_rot, B * S * D * es);
-  take(w.knorm, key_norm_floats(c) * 4);
   take(w.qr, B * S * H * D * es);
   take(w.dor, B * S * H * D * es);
   take(w.delta, B * S * H * 4);
@@ -313,11 +311,6 @@ static v4_status do_mqa(const v4_config& c, const void* q, const void* kv, const
   int* status = status_ptr();
   if (!status) return fail(V4_ERR_CUDA, "device status word unavailable");
   void* kv_rot = ws + plan.kv_rot;
-  float* kv_norm = (float*)(ws + plan.knorm);
-  float* ent_norm = kv_norm + (size_t)c.batch * c.seqlen;
-  const size_t n_ent = c.ratio > 0 ? (size_t)c.batch * (c.seqlen / c.ratio) : 0;
-  float* wmax = ent_norm + n_ent;
-  float* emax = wmax + (size_t)c.batch * c.seqlen;
   const bool tc = use_tc_attention(c);
   {
     ProfScope ps(K_ROTATE, st);
@@ -326,7 +319,7 @@ static v4_status do_mqa(const v4_config& c, const void* q, const void* kv, const
         v4_status s = do_rope_table(c, f, ws, st);
         if (s != V4_OK) return s;
       }
-      CU(launch_key_prep(c, kv, ent, table, kv_rot, kv_norm, ent_norm, wmax, emax, st), "key prep kernel");
+      CU(launch_key_prep(c, kv, table, kv_rot, st), "key prep kernel");
     } else {
       CU(launch_rotate_rows(c, kv, f, kv_rot, st), "window-key rotation kernel");
     }
@@ -335,11 +328,11 @@ static v4_status do_mqa(const v4_config& c, const void* q, const void* kv, const
     int* counters = (int*)(ws + plan.counters);
     {
       ProfScope ps(K_ATTN, st);
-      CU(launch_mqa_tc(c, q, kv_rot, ent, idx, sink, table, wmax, emax, o, lse, counters, status, st),
+      CU(launch_mqa_tc(c, q, kv_rot, ent, idx, sink, table, o, lse, counters, status, st),
          "tensor-core attention kernel");
     }
-    // queries whose bound-shifted softmax kept too little mass are recomputed
-    // with the running-max kernel (normally none)
+    // queries whose fixed-shift softmax overflowed or kept too little mass
+    // are recomputed with the running-max kernel (normally none)
     CU(launch_mqa_simt(c, q, kv_rot, ent, idx, sink, f, o, lse, status, counters + 1, st),
        "attention fix-up kernel");
     return V4_OK;
@@ -570,12 +563,7 @@ v4_status v4_sparse_mqa_bwd(const v4_config* cfg, const void* q, const void* kv,
     if (comp) CU(cudaMemsetAsync(dent, 0, B * N * D * 4, st), "dent clear");
     if (sink) CU(cudaMemsetAsync(dsink, 0, (size_t)c.n_heads * 4, st), "dsink clear");
     CU(launch_rope_table(c, inv_freq, (float2*)(ws + plan.rope), st), "rope table kernel");
-    float* kv_norm = (float*)(ws + plan.knorm);
-    float* ent_norm = kv_norm + B * S;
-    float* wmax = ent_norm + B * N;
-    float* emax = wmax + B * S;
-    CU(launch_key_prep(c, kv, comp ? ent : nullptr, table, kv_rot, kv_norm, ent_norm, wmax, emax, st),
-       "key prep kernel");
+    CU(launch_key_prep(c, kv, table, kv_rot, st), "key prep kernel");
     CU(launch_mqa_bwd_prep(c, q, o, dout, lse, sink, table, ws + plan.qr, ws + plan.dor, delta, sink ? dsink : nullptr,
                            st),
        "backward prep kernel");

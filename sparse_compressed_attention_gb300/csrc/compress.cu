@@ -221,104 +221,27 @@ __global__ void rope_table_kernel(const float* __restrict__ inv_freq, float2* __
   }
 }
 
-// Key prep: one warp per stored key row.  Rows [0, B*S) are window tokens:
-// rotated at their position u (last R dims), stored in the storage dtype,
-// and their norm taken from the stored (rounded) values.  Rows
-// [B*S, B*S + B*N) are entries (already rotated): only their norm.
+// Key prep: one warp per window row u of kv (rows [0, B*S)): rotated at
+// its position on the last R dims and stored in the storage dtype.
 template <typename T>
-__global__ void key_prep_kernel(const T* __restrict__ kv, const T* __restrict__ ent,
-                                const float2* __restrict__ cs_table, T* __restrict__ kv_rot,
-                                float* __restrict__ kv_norm, float* __restrict__ ent_norm,
-                                long long kv_rows, long long ent_rows, int S, int D, int R) {
+__global__ void key_prep_kernel(const T* __restrict__ kv, const float2* __restrict__ cs_table,
+                                T* __restrict__ kv_rot, long long kv_rows, int S, int D, int R) {
   const int lane = threadIdx.x & 31;
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-  for (long long row = blockIdx.x * (long long)(blockDim.x >> 5) + (threadIdx.x >> 5);
-       row < kv_rows + ent_rows; row += warps) {
-    const bool is_kv = row < kv_rows;
-    const T* src = is_kv ? kv + row * D : ent + (row - kv_rows) * D;
-    float ss = 0.f;
+  for (long long row = blockIdx.x * (long long)(blockDim.x >> 5) + (threadIdx.x >> 5); row < kv_rows;
+       row += warps) {
+    const T* src = kv + row * D;
     for (int v = lane; v < D / 8; v += 32) {
       float e[8];
       load8(src + v * 8, e);
       const int c0 = v * 8;
-      if (is_kv) {
-        if (c0 >= D - R) {
-          const float2* cs = cs_table + (row % S) * (R / 2) + (c0 - (D - R)) / 2;
+      if (c0 >= D - R) {
+        const float2* cs = cs_table + (row % S) * (R / 2) + (c0 - (D - R)) / 2;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) rot_pair(e[2 * k], e[2 * k + 1], cs[k].x, cs[k].y);
-        }
-        store8(kv_rot + row * D + c0, e);
-        load8(kv_rot + row * D + c0, e);         // norm of the stored values
+        for (int k = 0; k < 4; ++k) rot_pair(e[2 * k], e[2 * k + 1], cs[k].x, cs[k].y);
       }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) ss = fmaf(e[k], e[k], ss);
+      store8(kv_rot + row * D + c0, e);
     }
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) {
-      if (is_kv) kv_norm[row] = sqrtf(ss);
-      else ent_norm[row - kv_rows] = sqrtf(ss);
-    }
-  }
-}
-
-// Norm bounds for the attention's fixed softmax shift, one value per query
-// instead of a maximum over its keys:
-//   wmax[b, t]     = max |kv_rot[b, u]| over the window rows u of query t
-//   emax[b, n]     = max |ent[b, s]| over the entries s < n   (n = 0..N)
-// Blocks [0, wblocks) each take kBoundThreads consecutive rows of the window
-// maximum (the norms they need staged in shared memory); block wblocks + b
-// takes the prefix maximum of batch b's entries (chunk per thread, then a
-// block-wide scan of the chunk maxima); without entry norms emax is 0.
-constexpr int kBoundThreads = 256;
-constexpr int kMaxWindow = 1024;
-
-__global__ void __launch_bounds__(kBoundThreads)
-key_bounds_kernel(const float* __restrict__ kv_norm, const float* __restrict__ ent_norm,
-                  float* __restrict__ wmax, float* __restrict__ emax, int B, int S, int N, int W, int wblocks) {
-  __shared__ float sh[kBoundThreads + kMaxWindow];
-  const int tid = threadIdx.x;
-  if ((int)blockIdx.x < wblocks) {
-    const long long r0 = (long long)blockIdx.x * kBoundThreads;        // first row of the block
-    const long long rows = (long long)B * S;
-    const int w = min(W, kMaxWindow);
-    // rows r0 - (w-1) .. r0 + kBoundThreads - 1, norms of other batches read as 0
-    for (int i = tid; i < kBoundThreads + w - 1; i += kBoundThreads) {
-      const long long r = r0 - (w - 1) + i;
-      sh[i] = (r >= 0 && r < rows) ? kv_norm[r] : 0.f;
-    }
-    __syncthreads();
-    const long long r = r0 + tid;
-    if (r < rows) {
-      const int t = (int)(r % S);
-      const int lo = max(0, t - w + 1);               // first window position
-      float m = 0.f;
-      for (int u = lo; u <= t; ++u) m = fmaxf(m, sh[tid + (w - 1) - (t - u)]);
-      wmax[r] = m;
-    }
-    return;
-  }
-  const int b = blockIdx.x - wblocks;
-  const float* en = ent_norm ? ent_norm + (size_t)b * N : nullptr;
-  float* em = emax + (size_t)b * (N + 1);
-  const int chunk = (N + kBoundThreads - 1) / kBoundThreads;
-  const int s0 = min(N, tid * chunk), s1 = min(N, s0 + chunk);
-  float local = 0.f;
-  if (ent_norm)
-    for (int s = s0; s < s1; ++s) local = fmaxf(local, en[s]);
-  // exclusive max-scan of the chunk maxima
-  sh[tid] = local;
-  __syncthreads();
-  for (int off = 1; off < kBoundThreads; off <<= 1) {
-    const float v = tid >= off ? sh[tid - off] : 0.f;
-    __syncthreads();
-    sh[tid] = fmaxf(sh[tid], v);
-    __syncthreads();
-  }
-  float run = tid > 0 ? sh[tid - 1] : 0.f;
-  if (tid == 0) em[0] = 0.f;
-  for (int s = s0; s < s1; ++s) {
-    if (ent_norm) run = fmaxf(run, en[s]);
-    em[s + 1] = run;
   }
 }
 
@@ -706,30 +629,19 @@ cudaError_t launch_rope_table(const v4_config& c, const float* inv_freq, float2*
   return cudaGetLastError();
 }
 
-cudaError_t launch_key_prep(const v4_config& c, const void* kv, const void* ent, const float2* cs_table,
-                            void* kv_rot, float* kv_norm, float* ent_norm, float* wmax, float* emax,
+cudaError_t launch_key_prep(const v4_config& c, const void* kv, const float2* cs_table, void* kv_rot,
                             cudaStream_t st) {
   const long long kv_rows = (long long)c.batch * c.seqlen;
-  const int N = c.ratio > 0 ? c.seqlen / c.ratio : 0;
-  const long long ent_rows = ent != nullptr ? (long long)c.batch * N : 0;
   const int threads = 256;
-  long long blocks = (kv_rows + ent_rows + 7) / 8;
+  long long blocks = (kv_rows + 7) / 8;
   if (blocks > 152LL * 16) blocks = 152LL * 16;
   if (blocks < 1) blocks = 1;
   if (c.dtype == V4_BF16)
-    key_prep_kernel<bf16><<<(int)blocks, threads, 0, st>>>((const bf16*)kv, (const bf16*)ent, cs_table,
-                                                            (bf16*)kv_rot, kv_norm, ent_norm, kv_rows,
-                                                            ent_rows, c.seqlen, c.head_dim, c.rope_dim);
+    key_prep_kernel<bf16><<<(int)blocks, threads, 0, st>>>((const bf16*)kv, cs_table, (bf16*)kv_rot, kv_rows,
+                                                            c.seqlen, c.head_dim, c.rope_dim);
   else
-    key_prep_kernel<float><<<(int)blocks, threads, 0, st>>>((const float*)kv, (const float*)ent, cs_table,
-                                                             (float*)kv_rot, kv_norm, ent_norm, kv_rows,
-                                                             ent_rows, c.seqlen, c.head_dim, c.rope_dim);
-  note_launch();
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int wblocks = (int)((kv_rows + kBoundThreads - 1) / kBoundThreads);
-  key_bounds_kernel<<<wblocks + (c.ratio > 0 ? c.batch : 0), kBoundThreads, 0, st>>>(
-      kv_norm, ent_rows > 0 ? ent_norm : nullptr, wmax, emax, c.batch, c.seqlen, N, c.window, wblocks);
+    key_prep_kernel<float><<<(int)blocks, threads, 0, st>>>((const float*)kv, cs_table, (float*)kv_rot, kv_rows,
+                                                             c.seqlen, c.head_dim, c.rope_dim);
   note_launch();
   return cudaGetLastError();
 }

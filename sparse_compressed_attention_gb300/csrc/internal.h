@@ -48,7 +48,6 @@ struct Workspace {
   size_t iqp = 0, iqp_bytes = 0;           // prepared indexer queries [B,Sq,Hi,Di]
   size_t scores = 0, scores_bytes = 0;     // indexer scores [B,Sq,N] fp32
   size_t idx = 0, idx_bytes = 0;           // selected entries [B,Sq,K] (layer call)
-  size_t knorm = 0, knorm_bytes = 0;       // key-row norms [B*S + B*N] (tensor-core attention)
   size_t counters = 0, counters_bytes = 0; // work counter, redo count, redo list [2 + B*Sq*slices]
   size_t rope = 0, rope_bytes = 0;         // cos/sin table [S][R/2] float2
   size_t qc8 = 0, qc8_bytes = 0;           // E4M3 indexer: query codes [B,Sq,Hi,Di] u8
@@ -67,19 +66,10 @@ cudaError_t launch_compress(const v4_config& c, const void* ckv, const void* csc
                             const float2* cs_table, int dim, int hadamard, void* out, cudaStream_t st);
 cudaError_t launch_rotate_rows(const v4_config& c, const void* kv, const float* inv_freq,
                                void* kv_rot, cudaStream_t st);
-// Rotated window keys, the Euclidean norm of every stored key row (window
-// rows then entry rows) and, from them, the per-query bounds the
-// tensor-core attention shifts by: wmax[B*S] (window maximum) and
-// emax[B*(N+1)] (prefix maximum over entries).  Window <= 1024.
-cudaError_t launch_key_prep(const v4_config& c, const void* kv, const void* ent, const float2* cs_table,
-                            void* kv_rot, float* kv_norm, float* ent_norm, float* wmax, float* emax,
+// Rotated window keys: token u of kv rotated at u on the last R dims,
+// stored in the storage dtype, from the per-call cos/sin table.
+cudaError_t launch_key_prep(const v4_config& c, const void* kv, const float2* cs_table, void* kv_rot,
                             cudaStream_t st);
-// Floats of the norm and bound arrays above.
-inline size_t key_norm_floats(const v4_config& c) {
-  const size_t T = (size_t)c.batch * c.seqlen;
-  const size_t N = c.ratio > 0 ? (size_t)(c.seqlen / c.ratio) : 0;
-  return 2 * T + (size_t)c.batch * N + (size_t)c.batch * (N + 1);
-}
 // cos/sin of every (position < S, rotated pair): table[pos * R/2 + j].
 cudaError_t launch_rope_table(const v4_config& c, const float* inv_freq, float2* table, cudaStream_t st);
 
@@ -134,8 +124,7 @@ cudaError_t launch_oproj_tc(const v4_config& c, const void* o, const void* wo_a,
 cudaError_t launch_qproj_tc(long long T, int rank, const void* x, const void* w, int N, void* y, int norm,
                             float eps, const float* norm_w, int* status, cudaStream_t st);
 cudaError_t launch_mqa_tc(const v4_config& c, const void* q, const void* kv_rot, const void* ent,
-                          const int32_t* idx, const float* sink, const float2* cs_table,
-                          const float* wmax, const float* emax, void* o, float* lse,
+                          const int32_t* idx, const float* sink, const float2* cs_table, void* o, float* lse,
                           int* counters, int* status, cudaStream_t st);
 
 // ---- sparse indexer distillation target (kl_target_tc.cu)

@@ -26,11 +26,9 @@ namespace {
 // table).  The Flash shapes (D=512, R=64, bf16) reach all three at B*S=8192.
 constexpr long long kMaxTokens = 8192;
 constexpr size_t kKvBytes = 8u << 20;
-constexpr size_t kNormBytes = 5 * kMaxTokens * sizeof(float);            // norms and their bounds
 constexpr size_t kCounterBytes = (2 + 8 * kMaxTokens) * sizeof(int);      // up to 8 head slices
 constexpr size_t kRopeBytes = 524288 / 2 * sizeof(float2);
-constexpr size_t kOffNorm = kKvBytes;
-constexpr size_t kOffCounters = kOffNorm + kNormBytes;
+constexpr size_t kOffCounters = kKvBytes;
 constexpr size_t kOffRope = (kOffCounters + kCounterBytes + 255) & ~(size_t)255;
 constexpr size_t kScratchBytes = kOffRope + kRopeBytes;
 
@@ -98,10 +96,6 @@ extern "C" v4_status v4_sparse_mqa_fwd_noalloc(const v4_config* cfg, const void*
   if (!status) return set_error(V4_ERR_CUDA, "device status word unavailable");
   cudaStream_t st = (cudaStream_t)stream;
   void* kv_rot = base;
-  float* kv_norm = (float*)(base + kOffNorm);
-  float* ent_norm = kv_norm + tokens;
-  float* wmax = ent_norm + (c.ratio > 0 ? (long long)c.batch * (c.seqlen / c.ratio) : 0);
-  float* emax = wmax + tokens;
   int* counters = (int*)(base + kOffCounters);
   float2* table = (float2*)(base + kOffRope);
   const int32_t* sel = c.topk > 0 ? idx : nullptr;
@@ -113,14 +107,13 @@ extern "C" v4_status v4_sparse_mqa_fwd_noalloc(const v4_config* cfg, const void*
       StageTiming tm(kKindRotate, st);
       if ((e = launch_rope_table(c, inv_freq, table, st)) != cudaSuccess)
         return set_error(V4_ERR_CUDA, cudaGetErrorString(e));
-      if ((e = launch_key_prep(c, kv, ent, table, kv_rot, kv_norm, ent_norm, wmax, emax, st)) != cudaSuccess)
+      if ((e = launch_key_prep(c, kv, table, kv_rot, st)) != cudaSuccess)
         return set_error(V4_ERR_CUDA, cudaGetErrorString(e));
     }
     {
       StageTiming tm(kKindAttention, st);
       // launch_mqa_tc clears the redo count it needs before its kernel runs
-      if ((e = launch_mqa_tc(c, q, kv_rot, ent, sel, sink, table, wmax, emax, o, lse, counters, status, st)) !=
-          cudaSuccess)
+      if ((e = launch_mqa_tc(c, q, kv_rot, ent, sel, sink, table, o, lse, counters, status, st)) != cudaSuccess)
         return set_error(V4_ERR_CUDA, cudaGetErrorString(e));
     }
     if ((e = launch_mqa_simt(c, q, kv_rot, ent, sel, sink, inv_freq, o, lse, status, counters + 1, st)) != cudaSuccess)

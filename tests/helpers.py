@@ -124,9 +124,11 @@ def check_topk_rows(gpu_idx, scores, iqp, ikey, w, ratio, K, rows, c, detail=Fal
     return (swaps, wide) if detail else swaps
 
 
-def check_attention_rows(o, lse, ro, rl, tol=1e-2):
+def check_attention_rows(o, lse, ro, rl, tol=1e-2, lse_extra=0.0):
     """Attention outputs against the oracle: relative L2 over all rows,
-    every row within 5 * tol, and lse within the bf16 operand error."""
+    every row within 5 * tol, and lse within the bf16 operand error
+    (plus lse_extra, broadcast over [B, S, H], for inputs scaled beyond
+    unit size)."""
     assert rel_l2(o, ro) < tol
     B, S, H, D = o.shape
     num = np.linalg.norm((o - ro).reshape(B * S, -1), axis=1)
@@ -136,7 +138,8 @@ def check_attention_rows(o, lse, ro, rl, tol=1e-2):
     assert np.array_equal(fin, np.isfinite(lse))
     # the kernel feeds the tensor cores bf16 copies of the rotated query and
     # window keys: a relative 2^-8 on the rotated part of each logit
-    assert np.all(np.abs(lse[fin] - rl[fin]) < 2e-2 + 4e-3 * np.abs(rl[fin]))
+    extra = np.broadcast_to(np.asarray(lse_extra, dtype=np.float64), rl.shape)
+    assert np.all(np.abs(lse[fin] - rl[fin]) < 2e-2 + 4e-3 * np.abs(rl[fin]) + extra[fin])
 
 
 def check_layer_sampled_rows(p, x, outs, rows, f, iqp, b=0, tol=1e-2):

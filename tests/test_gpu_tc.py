@@ -27,10 +27,12 @@ def _built():
     V.lib()
 
 
-def _run(p, mode, sink, path, seed=0, q_scale=1.0, idx_seed=7):
+def _run(p, mode, sink, path, seed=0, q_scale=1.0, idx_seed=7, kv_scale=1.0):
     x = SI.make_layer_inputs(p, "cpu", seed=seed, sink=sink)
     if q_scale != 1.0:
         x["q"] = (x["q"].float() * q_scale).to(x["q"].dtype)
+    if kv_scale != 1.0:
+        x["kv"] = (x["kv"].float() * kv_scale).to(x["kv"].dtype)
     f = inv_freq_for(p)
     xd = to_dev(x)
     fd = torch.from_numpy(f).cuda()
@@ -95,12 +97,32 @@ def test_tc_and_simt_agree():
 
 
 def test_large_norms_take_the_fixup_path():
-    # q scaled by 16: the Cauchy-Schwarz bound (about 362) sits far above the
-    # logits, exp() underflows for every key, and the fix-up kernel recomputes
-    # those queries with a running max.
+    # q scaled by 16: logits spread over hundreds, so a window key can rise
+    # far above the shift taken from the entry tile; queries whose
+    # denominator overflows the check are recomputed with a running max.
     p = SI.preset("hca_bf16_16k", q_mode="direct", S=400, ratio=16)
     o, lse, ro, rl = _run(p, "hca", False, V.V4_PATH_TC, q_scale=16.0)
     _check(o, lse, ro, rl)
+
+
+def test_keys_far_above_the_first_tile_take_the_fixup_path():
+    # Window keys scaled by 64 (entries, from their own RMSNormed pooling,
+    # are not): for every query with entries the window logits exceed the
+    # first (entry) tile's maximum by far more than exp's range, so the
+    # shifted exponentials overflow; only the running-max fix-up of those
+    # queries gives finite, correct outputs.
+    p = SI.preset("hca_bf16_16k", q_mode="direct", S=400, ratio=16)
+    o, lse, ro, rl = _run(p, "hca", False, V.V4_PATH_TC, kv_scale=64.0)
+    assert np.all(np.isfinite(o))
+    # Both kernels read bf16 copies of the rotated query and window keys: a
+    # logit may move by up to scale * 2^-8 * |q_rot| * |k_rot|, which the
+    # 64-fold keys make larger than the unit-scale allowance of lse.
+    x = SI.make_layer_inputs(p, "cpu", seed=0)
+    R = p["R"]
+    q_rot = np.linalg.norm(np64(x["q"])[..., -R:], axis=-1)                 # [B, S, H]
+    k_rot = np.linalg.norm(np64(x["kv"])[..., -R:], axis=-1).max() * 64.0
+    extra = 2.0 ** -8 * q_rot * k_rot / np.sqrt(p["D"])
+    check_attention_rows(o, lse, ro, rl, TOL, lse_extra=extra)
 
 
 def test_forced_tc_path_rejects_other_shapes():
